@@ -1,0 +1,231 @@
+/*
+ * pa.h -- C ABI of the paged-KV attention library (libpa.so) for GB300.
+ *
+ * The library implements the GPU hot path of one scheduler step of a
+ * paged-KV serving engine, as the following pages describe it:
+ *
+ *  [Anatomy]  "vLLM engine anatomy" (oripoin.cn/posts/vllm-engine-anatomy)
+ *  [V1arch]   "vLLM V1 engine architecture: from single process to
+ *             multi-process EngineCore" (charlestar.github.io)
+ *  [V0vsV1]   "vLLM V0 vs V1" (llm.rainlin.net/.../vllm-v0-v1-comparation)
+ *  [Overview] "01. vLLM: a general inference engine that grew out of paged KV"
+ *             (niuwancheng.cn/blog/docs/ai/inference-engines/01-vllm.html)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every buffer argument is a DEVICE pointer on the current CUDA device,
+ *    allocated and owned by the caller.  The library never allocates,
+ *    frees or retains a buffer between calls.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and performs no host<->device synchronisation,
+ *    except pa_get_device_error, which synchronises `stream`.
+ *  - Arguments are validated on the host before any launch.  A call that
+ *    returns anything other than PA_OK has launched nothing.
+ *  - Index values that live in device memory (slots, block ids, sequence
+ *    lengths, query offsets) are validated by the kernels themselves: an
+ *    out-of-range value is never dereferenced; the kernel skips the access
+ *    and records a flag that pa_get_device_error reports.
+ *  - Unsupported type / shape combinations return PA_ERR_UNSUPPORTED; there
+ *    is no fallback path of any kind.
+ *
+ * KV-cache layout (fixed by this library; the pages do not prescribe one):
+ *    k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *  contiguous, elements of type cache_dtype.  One (block, kv head) page of
+ *  block_size x head_dim elements is contiguous (4 KiB for bf16/fp16 at
+ *  head_dim 128).  Token j of a sequence lives in physical block
+ *  block_table[j / block_size] at offset j % block_size ([Anatomy],
+ *  "PagedAttention: paging the KV cache", Figure 2).  A slot number is
+ *  block * block_size + offset.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* bad pointer, size, alias or value: nothing ran */
+  PA_ERR_UNSUPPORTED = 2, /* valid but not implemented combination          */
+  PA_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed          */
+  PA_ERR_DEVICE = 4       /* a kernel recorded a device-side error flag      */
+} pa_status;
+
+typedef enum {
+  PA_F32 = 0,
+  PA_F16 = 1,
+  PA_BF16 = 2,
+  PA_FP8_E4M3 = 3 /* OCP FP8 E4M3 "FN": bias 7, max 448, no inf, 0x7f NaN */
+} pa_dtype;
+
+/* Device-side error flags (bit mask) reported by pa_get_device_error. */
+#define PA_DEV_ERR_SLOT 0x1u      /* slot >= num_blocks * block_size        */
+#define PA_DEV_ERR_BLOCK_ID 0x2u  /* block id outside [0, num_blocks)       */
+#define PA_DEV_ERR_METADATA 0x4u  /* seq_len / query_start_loc inconsistent */
+#define PA_DEV_ERR_TIMEOUT 0x8u   /* a bounded pipeline wait ran out        */
+
+/* The only block size supported: 16 tokens per physical block, the default
+ * block size named in [Anatomy], "PagedAttention: paging the KV cache", and
+ * in [Overview], "KV cache management and prefix caching". */
+#define PA_BLOCK_SIZE 16
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* pa_status_string(pa_status status);
+
+/*
+ * pa_reshape_and_cache -- write the K and V of this step's tokens into the
+ * paged cache.
+ *
+ * Defines: every token processed by a forward pass has its key and value
+ * written into the KV cache ([Anatomy], "Prefill, decode and the three
+ * latency metrics"); the cache is split into fixed 16-token physical blocks
+ * and a token's place is (block, offset) through the block table ([Anatomy],
+ * "PagedAttention", Figure 2); an FP8 KV cache stores one byte per element
+ * ([Overview], KV cache options table, --kv-cache-dtype fp8).
+ *
+ *   for each token t < num_tokens with slot = slot_mapping[t] >= 0,
+ *   for each kv head h and d < head_dim:
+ *     k_cache[slot/16][h][slot%16][d] = cvt(key  [t*key_stride   + h*head_dim + d])
+ *     v_cache[slot/16][h][slot%16][d] = cvt(value[t*value_stride + h*head_dim + d])
+ *
+ * key, value    : device, kv_dtype (PA_F32 / PA_F16 / PA_BF16); token t's
+ *                 row starts at element t*key_stride (resp. value_stride);
+ *                 within a row, [num_kv_heads][head_dim] is contiguous.
+ * slot_mapping  : device int64 [num_tokens]; a negative slot marks a padding
+ *                 token that is not written.  A slot >= num_blocks*block_size
+ *                 is skipped and flagged PA_DEV_ERR_SLOT.
+ * cache_dtype   : equal to kv_dtype (the bits are copied exactly), or
+ *                 PA_FP8_E4M3: the code is the E4M3 value nearest to
+ *                 fl32(x / scale) (one correctly rounded fp32 division),
+ *                 ties to even, saturating to +-448; scale = k_scale for K
+ *                 and v_scale for V, both finite and > 0.
+ * Two tokens must not map to the same slot (the order of such writes is
+ * unspecified).
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               pa_dtype kv_dtype, int64_t num_tokens,
+                               int64_t key_stride, int64_t value_stride,
+                               void* k_cache, void* v_cache,
+                               pa_dtype cache_dtype, int64_t num_blocks,
+                               int block_size, int num_kv_heads, int head_dim,
+                               const int64_t* slot_mapping, float k_scale,
+                               float v_scale, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks -- block-granular copy-on-write.
+ *
+ * Defines: a shared block is read-only; a sequence that must write into a
+ * block other sequences still reference gets its own copy of that block and
+ * only its own block table changes ([Anatomy], "PagedAttention", the
+ * "copy-on-write" item); V0's scheduler output carries the copies to make as
+ * blocks_to_copy ([V0vsV1], section 2.1 and 3.1).
+ *
+ *   for each pair p < num_pairs: (src, dst) = block_mapping[2p], [2p+1]
+ *     k_cache[dst][:][:][:] = k_cache[src][:][:][:]   (all heads, offsets)
+ *     v_cache[dst][:][:][:] = v_cache[src][:][:][:]
+ *
+ * block_mapping : device int64 [num_pairs][2].  Every dst must be distinct
+ *                 and no dst may also appear as a src (the pairs run in
+ *                 parallel).  An id outside [0, num_blocks) is skipped and
+ *                 flagged PA_DEV_ERR_BLOCK_ID.
+ * The copy is bit-exact for every cache dtype.
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype cache_dtype,
+                         int64_t num_blocks, int block_size, int num_kv_heads,
+                         int head_dim, const int64_t* block_mapping,
+                         int64_t num_pairs, pa_stream_t stream);
+
+/*
+ * pa_attention_workspace_size -- bytes of device workspace pa_attention
+ * needs for the given host-known sizes (work list and split-K partials).
+ * The same arguments must be passed to pa_attention.  Result in *bytes.
+ */
+pa_status pa_attention_workspace_size(int64_t num_tokens, int num_q_heads,
+                                      int num_kv_heads, int head_dim,
+                                      int num_seqs, int max_query_len,
+                                      int max_seq_len, size_t* bytes);
+
+/*
+ * pa_attention -- unified paged attention for one scheduler step.
+ *
+ * Defines: one step is a map {request: number of tokens} that mixes
+ * one-token decodes with chunks of long prompts (chunked prefill)
+ * ([Anatomy], "V1: unified scheduling of prefill and decode", Figure 3;
+ * [V1arch], "Scheduler forms one round of work"); the model runner builds
+ * the attention metadata from each request's query length, context length
+ * and block table ([V0vsV1], section 3.1); generation is autoregressive, each
+ * token attends to the tokens before it ([Anatomy], "Prefill, decode ...");
+ * GQA has fewer KV heads than query heads ([Anatomy], Table 1); the
+ * attention itself is exact softmax attention, computed tile by tile with an
+ * online softmax so the score matrix is never materialised ([Anatomy],
+ * "Boundaries: FlashAttention, SGLang ...").
+ *
+ * For request r: its query tokens are rows [query_start_loc[r],
+ * query_start_loc[r+1]) of q (n_r of them) and L_r = seq_lens[r] is its
+ * number of keys in the cache, THIS step's tokens included (they must have
+ * been written with pa_reshape_and_cache first).  Query i of request r sits
+ * at position L_r - n_r + i and sees keys 0 .. L_r - n_r + i.  Query head h
+ * uses KV head h / (num_q_heads / num_kv_heads).
+ *
+ *   s_j = scale * <q, k_j>,   out = sum_j softmax(s)_j * v_j
+ *
+ * with k_j = k_scale * e4m3(k8_j) and v_j = v_scale * e4m3(v8_j) for an FP8
+ * cache (k_scale, v_scale ignored otherwise).
+ *
+ * q, out          : device [num_tokens][num_q_heads][head_dim] of q_dtype;
+ *                   out receives q_dtype values (round to nearest even).
+ *                   out must not overlap q, the caches or the workspace.
+ *                   Rows of tokens that belong to no request are untouched.
+ * q_dtype         : PA_F32 / PA_F16 / PA_BF16.  For a non-FP8 cache it must
+ *                   equal cache_dtype.
+ * block_tables    : device int32 [num_seqs][max_blocks_per_seq].  Entries
+ *                   past ceil(L_r / 16) are never read.
+ * seq_lens        : device int32 [num_seqs], 0 <= n_r <= L_r <= max_seq_len.
+ * query_start_loc : device int32 [num_seqs + 1], non-decreasing, starting at
+ *                   0, query_start_loc[num_seqs] <= num_tokens, every n_r <=
+ *                   max_query_len.  A request with n_r = 0 produces nothing.
+ * max_query_len, max_seq_len : host upper bounds supplied by the caller (no
+ *                   device read-back happens inside); violations found on
+ *                   the device are flagged PA_DEV_ERR_METADATA and the
+ *                   request is skipped.
+ * workspace       : device, >= the size pa_attention_workspace_size returns
+ *                   for the same sizes, 256-byte aligned; its contents on
+ *                   entry do not matter.
+ * Results are bitwise deterministic from run to run.
+ *
+ * Supported: head_dim 64 or 128; block_size 16; num_q_heads a multiple of
+ * num_kv_heads; caches bf16/fp16 (with q of the same type), fp32 (with fp32
+ * q), FP8 E4M3 (with bf16 or fp16 q).
+ */
+pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
+                       const void* v_cache, pa_dtype cache_dtype,
+                       int64_t num_blocks, int block_size, int num_q_heads,
+                       int num_kv_heads, int head_dim,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int num_seqs,
+                       int64_t num_tokens, int max_query_len, int max_seq_len,
+                       float scale, float k_scale, float v_scale, void* out,
+                       void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream);
+
+/*
+ * pa_get_device_error -- synchronise `stream`, then read and clear the
+ * device-side error flags of the current device (PA_DEV_ERR_* bits, 0 if
+ * none) into *flags.  Returns PA_ERR_DEVICE if any flag was set, PA_OK
+ * otherwise, PA_ERR_CUDA if the synchronisation itself failed.
+ */
+pa_status pa_get_device_error(pa_stream_t stream, uint32_t* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */
