@@ -1,0 +1,456 @@
+"""Benchmark of the paged-KV attention step on GB300.
+
+Headline (``value``): HBM throughput of one decode step of the Llama-3.1-8B-
+shaped batch (64 sequences, context U[512, 4096], 32 query / 8 KV heads,
+head_dim 128, bf16 KV, 20,000-block permuted pool) -- algorithmic bytes (every
+valid key's K and V once, plus q and out) over the device time of the step.
+Beside it, in the same run: the mixed unified step (120 decodes + a 1022-token
+chunk after a shared 2,000-token prefix, one copy-on-write) as tokens/s, the
+roofline of the dominant kernel, an end-to-end number through the public API
+with host buffers, and the CPU oracle on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same step on its own GPU (independent
+replicas: the step has no exchange), timing is max over ranks, and ``value``
+is the sum of all ranks' bytes over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode HBM TB/s (fraction of peak); mixed-step tokens/s"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv",
+                                                    delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu),
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def _device_inputs(wl, dev):
+    import torch
+    from paged_kv_cache_82_gb300.metadata import build_step_metadata
+    md = build_step_metadata(wl.requests)
+    d = {
+        "kc": wl.k_cache.to(dev), "vc": wl.v_cache.to(dev),
+        "q": wl.q.to(dev),
+        "bt": torch.from_numpy(md["block_tables"]).to(dev),
+        "sl": torch.from_numpy(md["seq_lens"]).to(dev),
+        "qsl": torch.from_numpy(md["query_start_loc"]).to(dev),
+        "slots": torch.from_numpy(md["slot_mapping"]).to(dev),
+        "md": md,
+    }
+    if wl.write_new:
+        d["key"] = wl.key.to(dev)
+        d["value"] = wl.value.to(dev)
+    if wl.copy_pairs:
+        d["pairs"] = torch.tensor(wl.copy_pairs, dtype=torch.int64, device=dev)
+    d["out"] = torch.empty_like(d["q"])
+    import paged_kv_cache_82_gb300 as pa
+    nbytes = pa.pa_attention_workspace_size(
+        wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+        len(wl.requests), md["max_query_len"], md["max_seq_len"])
+    d["ws"] = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    return d
+
+
+def _step(pa, wl, d):
+    """One pass of the hot path over the step: copy-on-write copies, K/V
+    writes, attention.  Returns the number of our kernel launches."""
+    launches = 0
+    if wl.copy_pairs:
+        pa.pa_copy_blocks(d["kc"], d["vc"], d["pairs"])
+        launches += 1
+    if wl.write_new:
+        pa.pa_reshape_and_cache(d["key"], d["value"], d["kc"], d["vc"],
+                                d["slots"], k_scale=wl.k_scale,
+                                v_scale=wl.v_scale)
+        launches += 1
+    md = d["md"]
+    pa.pa_attention(d["q"], d["kc"], d["vc"], d["bt"], d["sl"], d["qsl"],
+                    md["max_query_len"], md["max_seq_len"], wl.scale,
+                    wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"])
+    return launches + 3   # plan, main, split merge
+
+
+def _time_steps(pa, wl, d, steps, warmup, flush, kernel_events=True):
+    """Per-step device times (ms) with the L2 flushed between steps, and the
+    main attention kernel's own times from the library's event hook."""
+    import torch
+    for _ in range(warmup):
+        _step(pa, wl, d)
+    torch.cuda.synchronize()
+    step_ms, kern_ms, launches = [], [], 0
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    if kernel_events:
+        pa.pa_set_profile_events(k0, k1)
+    try:
+        for _ in range(steps):
+            flush.add_(1)             # evict the previous step's lines
+            s0.record()
+            launches += _step(pa, wl, d)
+            s1.record()
+            s1.synchronize()
+            step_ms.append(s0.elapsed_time(s1))
+            if kernel_events:
+                kern_ms.append(k0.elapsed_time(k1))
+    finally:
+        if kernel_events:
+            pa.pa_set_profile_events(None, None)
+    return step_ms, kern_ms, launches
+
+
+def _e2e(pa, wl, d, steps, warmup):
+    """Same step through the public API from pinned host buffers: per step the
+    host->device copy of q and the metadata, the step, and the device->host
+    copy of the output, all inside the timed region."""
+    import torch
+    md = d["md"]
+    host = {
+        "q": wl.q.pin_memory(),
+        "bt": torch.from_numpy(md["block_tables"]).pin_memory(),
+        "sl": torch.from_numpy(md["seq_lens"]).pin_memory(),
+        "qsl": torch.from_numpy(md["query_start_loc"]).pin_memory(),
+        "slots": torch.from_numpy(md["slot_mapping"]).pin_memory(),
+    }
+    if wl.write_new:
+        host["key"] = wl.key.pin_memory()
+        host["value"] = wl.value.pin_memory()
+    out_h = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        _step(pa, wl, d)
+        out_h.copy_(d["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(
+        enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def _cpu_baseline(wl, bytes_per_step, budget_s=12.0, max_reps=20):
+    """The oracle, as it stands, on the host cores: whole decode steps of the
+    same workload until about `budget_s` of CPU work."""
+    import oracle
+    md = oracle.step_metadata(wl.requests)
+    cores = os.cpu_count() or 1
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_reps and (time.perf_counter() - t_start) < budget_s:
+        t0 = time.perf_counter()
+        oracle.paged_attention(wl.q, wl.k_cache, wl.v_cache,
+                               md["block_tables"], md["seq_lens"],
+                               md["query_start_loc"], scale=wl.scale,
+                               cache_dtype=wl.cache_dtype, num_threads=cores)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    return {"value": bytes_per_step / t / 1e12, "unit": "TB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": (f"{len(times)} whole decode steps of the same batch "
+                       f"(64 seqs), fp64, {cores} threads, "
+                       f"{t * 1e3:.0f} ms per step")}
+
+
+def _traffic_record(kernel_src_hash):
+    """DRAM bytes per launch of the main kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "attn_fast_cfg2_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != kernel_src_hash:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_fast.cu", "pa_common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_82_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import paged_kv_cache_82_gb300 as pa
+    import workloads
+    pa.load_library()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # ---- decode step (headline)
+    wl = workloads.config2()
+    d = _device_inputs(wl, dev)
+    kv_bytes = wl.kv_bytes()
+    alg_bytes = kv_bytes + wl.qo_bytes()
+    sampler = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    step_ms, kern_ms, launches = _time_steps(pa, wl, d, args.steps,
+                                             args.warmup, flush)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x}")
+    ms = statistics.mean(step_ms)
+    kern = statistics.mean(kern_ms)
+    if ws > 1:
+        t = torch.tensor([ms, kern], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, kern = float(t[0]), float(t[1])
+    value = alg_bytes * ws / (ms * 1e-3) / 1e12
+    peak_gbs, peak_kind = _peaks()
+    achieved_gbs = alg_bytes / (kern * 1e-3) / 1e9
+    traffic = _traffic_record(_kernel_hash())
+
+    # ---- end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = _e2e(pa, wl, d, max(3, args.steps // 2), 2)
+    e2e_value = alg_bytes * ws / (e2e_ms * 1e-3) / 1e12
+    del d
+
+    # ---- mixed unified step (tokens/s)
+    wl4 = workloads.config4()
+    d4 = _device_inputs(wl4, dev)
+    m_step, m_kern, m_launch = _time_steps(pa, wl4, d4, args.steps,
+                                           args.warmup, flush)
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x} (mixed step)")
+    m_ms = statistics.mean(m_step)
+    if ws > 1:
+        t = torch.tensor([m_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        m_ms = float(t[0])
+    m_bytes = wl4.kv_bytes() + wl4.qo_bytes()
+    mixed = {
+        "workload": ("Llama-3.1-8B shape, bf16: 120 decodes (private context "
+                     "U[1024,8192] after a shared 2000-token prefix) + one "
+                     "1022-token chunked prefill after the prefix; 1 "
+                     "copy_blocks, 1142-token reshape_and_cache, attention"),
+        "tokens_per_s": wl4.num_tokens * ws / (m_ms * 1e-3),
+        "ms_per_step": m_ms,
+        "unique_kv_bytes": wl4.kv_bytes(), "logical_kv_bytes":
+            wl4.kv_bytes(unique=False),
+        "hbm_tbs": m_bytes / (m_ms * 1e-3) / 1e12,
+        "frac_of_measured_hbm": m_bytes / (m_ms * 1e-3) / 1e9 / peak_gbs,
+        "attention_kernel_ms": statistics.mean(m_kern),
+    }
+    del d4
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(wl, alg_bytes)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": ("Llama-3.1-8B-shaped decode: 64 seqs, context "
+                         "U[512,4096], 32q/8kv heads, head_dim 128, bf16 KV, "
+                         "block 16, 20,000-block permuted pool"),
+            "kv_bytes": kv_bytes, "q_out_bytes": wl.qo_bytes(),
+            "l2": "flushed between timed steps (512 MiB write); KV 595 MB > L2",
+            "parallelism": f"replicas x{ws}",
+            "wall_s": wall,
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "attn_fast_kernel (bf16)",
+            "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
+            "frac": achieved_gbs / peak_gbs, "peak_kind": peak_kind,
+            "traffic": traffic, "kernel_ms": kern,
+            "frac_of_8TBs_spec": achieved_gbs / 8000.0,
+        },
+        "e2e": {"value": e2e_value, "unit": "TB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "mixed_step": mixed,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    import workloads
+    wl = workloads.config2()
+    alg_bytes = wl.kv_bytes() + wl.qo_bytes()
+    import oracle
+    md = oracle.step_metadata(wl.requests)
+    cores = os.cpu_count() or 1
+
+    def one():
+        oracle.paged_attention(wl.q, wl.k_cache, wl.v_cache,
+                               md["block_tables"], md["seq_lens"],
+                               md["query_start_loc"], scale=wl.scale,
+                               cache_dtype=wl.cache_dtype, num_threads=cores)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    value = alg_bytes / (ms * 1e-3) / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": ("Llama-3.1-8B-shaped decode: 64 seqs, context "
+                                "U[512,4096], 32q/8kv heads, head_dim 128, "
+                                "bf16 KV, block 16, 20,000-block permuted "
+                                "pool")},
+        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "whole decode steps of the batch, fp64"},
+        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -47,8 +47,10 @@
 extern "C" {
 #endif
 
-/* Same type as cudaStream_t, declared without the CUDA headers. */
+/* Same types as cudaStream_t / cudaEvent_t, declared without the CUDA
+ * headers. */
 typedef struct CUstream_st* pa_stream_t;
+typedef struct CUevent_st* pa_event_t;
 
 typedef enum {
   PA_OK = 0,
@@ -223,6 +225,17 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
  * otherwise, PA_ERR_CUDA if the synchronisation itself failed.
  */
 pa_status pa_get_device_error(pa_stream_t stream, uint32_t* flags);
+
+/*
+ * pa_set_profile_events -- measurement hook (no counterpart on the pages).
+ * When both events are non-NULL, every later pa_attention call on this
+ * thread records `start` on its stream immediately before the launch of the
+ * main attention kernel and `stop` immediately after it, so that
+ * cudaEventElapsedTime gives that kernel's device time alone (the planning
+ * and split-merge launches are outside the pair).  NULL, NULL turns it off.
+ * The events are owned by the caller and must outlive the calls.
+ */
+pa_status pa_set_profile_events(pa_event_t start, pa_event_t stop);
 
 #ifdef __cplusplus
 }

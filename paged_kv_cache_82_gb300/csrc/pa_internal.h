@@ -1,0 +1,96 @@
+// pa_internal.h -- host-side interfaces between the C ABI (pa_api.cu) and the
+// translation units that hold the kernels.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ---- cache kernels (cache_kernels.cu) --------------------------------------
+cudaError_t launch_reshape_and_cache(const void* key, const void* value,
+                                     pa_dtype kv_dtype, int64_t num_tokens,
+                                     int64_t key_stride, int64_t value_stride,
+                                     void* k_cache, void* v_cache,
+                                     pa_dtype cache_dtype, int64_t num_blocks,
+                                     int num_kv_heads, int head_dim,
+                                     const int64_t* slot_mapping, float k_scale,
+                                     float v_scale, bool vector_ok,
+                                     unsigned* err, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
+                               int64_t block_bytes,
+                               const int64_t* block_mapping, int64_t num_pairs,
+                               unsigned* err, cudaStream_t stream);
+
+// ---- attention (attn_*.cu) --------------------------------------------------
+// One work item of the attention kernel: request r, KV head g, kind
+// (0 = decode split, 1 = prefill row tile) and the split / tile index x.
+enum : int { kItemDecode = 0, kItemPrefill = 1 };
+
+constexpr int kDecodeMaxRows = 16;   // q_len * group rows handled by one warp
+constexpr int kPrefillTileRows = 64; // rows of a prefill tile (4 warps x 16)
+
+struct AttnPlan {
+  int group;            // Hq / Hkv
+  int blocks_per_split; // decode split size in blocks
+  int max_splits;       // ceil(max_blocks / blocks_per_split)
+  int has_prefill;      // max_query_len * group > kDecodeMaxRows
+  int64_t max_items;    // grid bound of the main kernel
+  // workspace carve-up (byte offsets, 256-aligned)
+  size_t off_items, off_count, off_nsplit, off_acc, off_ml, total_bytes;
+};
+
+// Host planning from host-known sizes only (no device read-back).
+AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
+                   int head_dim, int num_seqs, int max_query_len,
+                   int max_seq_len, int num_sms);
+
+struct AttnArgs {
+  const void* q;
+  pa_dtype q_dtype;
+  const void* k_cache;
+  const void* v_cache;
+  pa_dtype cache_dtype;
+  int64_t num_blocks;
+  int num_q_heads, num_kv_heads, head_dim;
+  const int32_t* block_tables;
+  int max_blocks_per_seq;
+  const int32_t* seq_lens;
+  const int32_t* query_start_loc;
+  int num_seqs;
+  int64_t num_tokens;
+  int max_query_len, max_seq_len;
+  float scale, k_scale, v_scale;
+  void* out;
+  void* workspace;
+  unsigned* err;
+};
+
+// true if the TMA + tensor-core kernel covers these types / shapes
+bool fast_path_supported(const AttnArgs& a);
+
+// events recorded around the main attention launch (measurement hook)
+struct ProfileEvents {
+  cudaEvent_t start = nullptr;
+  cudaEvent_t stop = nullptr;
+};
+ProfileEvents& profile_events();  // thread-local
+
+// plan kernel + main kernel + split merge (fast path)
+cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
+                                  const CUtensorMap& tmap_k,
+                                  const CUtensorMap& tmap_v,
+                                  cudaStream_t stream);
+
+// warp-per-row kernel for the remaining types / shapes
+cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream);
+
+// Encode the tensor maps of the two caches for the fast path.
+bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tmap_k,
+                              CUtensorMap* tmap_v);
+
+}  // namespace pa

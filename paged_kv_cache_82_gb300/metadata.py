@@ -1,0 +1,62 @@
+"""Host-side attention metadata of one scheduler step.
+
+A step is ``{request: num_tokens}`` ("vLLM V1 engine architecture", "Scheduler
+forms one round of work"); the model runner turns it, with each request's
+block table and number of already computed tokens, into the per-step arrays
+the attention kernels read ("vLLM V0 vs V1", section 3.1: query length,
+context length, block table).  Slots follow Figure 2 of "vLLM engine
+anatomy": position j of a request is in block ``block_table[j // 16]`` at
+offset ``j % 16``.
+
+Input: a sequence of requests with ``block_ids``, ``num_computed`` and
+``num_new``.  Output (numpy):
+
+* ``query_start_loc`` int32 [B+1] -- offsets of each request's new tokens
+* ``seq_lens`` int32 [B] -- keys per request, this step's tokens included
+* ``block_tables`` int32 [B, max_blocks] -- unused entries are 0
+* ``slot_mapping`` int64 [T] -- cache slot of every new token
+* ``max_query_len``, ``max_seq_len`` -- host upper bounds for the kernels
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+
+def build_step_metadata(requests, block_size: int = BLOCK_SIZE) -> dict:
+    n_new = np.fromiter((r.num_new for r in requests), dtype=np.int64,
+                        count=len(requests))
+    n_done = np.fromiter((r.num_computed for r in requests), dtype=np.int64,
+                         count=len(requests))
+    lens = n_done + n_new
+    qsl = np.zeros(len(requests) + 1, dtype=np.int64)
+    np.cumsum(n_new, out=qsl[1:])
+    width = max([len(r.block_ids) for r in requests] + [1])
+    tables = np.zeros((len(requests), width), dtype=np.int32)
+    for b, r in enumerate(requests):
+        tables[b, :len(r.block_ids)] = r.block_ids
+    T = int(qsl[-1])
+    # request index and position of every new token
+    req_of_tok = np.repeat(np.arange(len(requests)), n_new)
+    pos = np.arange(T, dtype=np.int64) - qsl[req_of_tok] + n_done[req_of_tok]
+    blocks = tables[req_of_tok, pos // block_size].astype(np.int64)
+    slots = blocks * block_size + pos % block_size
+    return {
+        "query_start_loc": qsl.astype(np.int32),
+        "seq_lens": lens.astype(np.int32),
+        "block_tables": tables,
+        "slot_mapping": slots.astype(np.int64),
+        "max_query_len": int(n_new.max()) if len(requests) else 0,
+        "max_seq_len": int(lens.max()) if len(requests) else 0,
+    }
+
+
+def to_device(md: dict, device) -> dict:
+    """Copy the metadata arrays to `device` (torch tensors); host ints kept."""
+    import torch
+    out = {}
+    for k, v in md.items():
+        out[k] = torch.from_numpy(v).to(device) if isinstance(v, np.ndarray) \
+            else v
+    return out
