@@ -34,6 +34,22 @@
 namespace pa {
 namespace {
 
+#ifndef PA_NARROW_MIN_BLOCKS
+#define PA_NARROW_MIN_BLOCKS 3  // resident CTAs per SM, <= 8-row kernel
+#endif
+#ifndef PA_SPLIT_MIN_BLOCKS
+#define PA_SPLIT_MIN_BLOCKS 16  // smallest decode split, in blocks
+#endif
+#ifndef PA_SPLIT_WAVES
+#define PA_SPLIT_WAVES 16       // target decode items per SM
+#endif
+#ifndef PA_L2_PREFETCH_PAGES
+#define PA_L2_PREFETCH_PAGES 0  // pages prefetched into L2 ahead of the ring (0: off)
+#endif
+#ifndef PA_STAGES_16BIT
+#define PA_STAGES_16BIT 8       // ring depth in pages, bf16 / fp16 caches
+#endif
+
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kPlanThreads = 1024;
@@ -51,18 +67,31 @@ struct Traits {
   static constexpr int kRowBytes = kFp8 ? 128 : 256;    // head_dim 128
   static constexpr int kPageBytes = kBS * kRowBytes;    // one (block, head)
   static constexpr int kStageBytes = 2 * kPageBytes;    // K page + V page
-  static constexpr int kStages = kFp8 ? 16 : 8;
+  static constexpr int kStages = kFp8 ? 2 * PA_STAGES_16BIT : PA_STAGES_16BIT;
   static constexpr int kRingBytes = kStages * kStageBytes;  // 64 KiB
   // Token order inside an 8-token MMA tile (row n of the tile holds token
   // perm(n)).  Chosen so that the fragment reads of both K and V from the
   // 128-byte-swizzled pages are free of shared-memory bank conflicts.
   static constexpr uint32_t kPerm = kFp8 ? 0x36147250u : 0x57463120u;
-  static constexpr int kSmemBytes =
-      1024 + kRingBytes + 2 * kStages * 8 + 16;
+  // A decode item hands page i to warp i % 4 through slot i % kStages.  The
+  // ring depth must be a multiple of the consumer count so that every slot
+  // always serves the same warp: otherwise a fast warp can wait one full
+  // phase ahead on a slot another warp still owns, the parity wait cannot
+  // tell the two phases apart, and the slot's barriers are corrupted.
+  static_assert(kStages % kConsumerWarps == 0,
+                "ring depth must be a multiple of the consumer warp count");
 };
 
 __device__ __forceinline__ int perm_of(uint32_t packed, int n) {
   return (packed >> (4 * n)) & 7;
+}
+
+// the two bf16 halves of a packed pair, as fp32 (exact)
+__device__ __forceinline__ float bf16_lo(uint32_t x) {
+  return __uint_as_float(x << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t x) {
+  return __uint_as_float(x & 0xFFFF0000u);
 }
 
 struct FastParams {
@@ -73,6 +102,7 @@ struct FastParams {
   const int32_t* qsl;
   const int4* items;
   const int* num_items;
+  int* work_counter;     // next unclaimed work item (zeroed by the planner)
   const int* req_nsplit;
   float* ws_acc;
   float* ws_ml;
@@ -205,6 +235,7 @@ plan_kernel(FastParams p, int4* items, int* num_items, int* req_nsplit) {
       n = p.max_items;
     }
     *num_items = (int)n;
+    *p.work_counter = 0;
   }
 }
 
@@ -370,10 +401,13 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
   constexpr bool kB = Tr::kMmaBF16;
   constexpr uint32_t P = Tr::kPerm;
   const int r = lane >> 2, c = lane & 3;
-  float s[2][4];
+  // Q.K^T: two accumulators per 8-key tile (even / odd k-steps) so that four
+  // independent MMA chains are in flight
+  float s[2][4], s2[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
-    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
     const int t = nt * 8 + perm_of(P, r);
     if constexpr (!Tr::kFp8) {
 #pragma unroll
@@ -383,7 +417,7 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
         const int phys = u ^ (((t << 1) | dhi) & 7);
         const uint4 kv = lds128(k_base + t * 256 + dhi * 128 + phys * 16);
         mma_acc<kB, kRows16>(s[nt], qa[2 * j], kv.x, kv.y);
-        mma_acc<kB, kRows16>(s[nt], qa[2 * j + 1], kv.z, kv.w);
+        mma_acc<kB, kRows16>(s2[nt], qa[2 * j + 1], kv.z, kv.w);
       }
     } else {
 #pragma unroll
@@ -395,10 +429,15 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
         for (int tt = 0; tt < 4; ++tt) {
           const uint32_t b0 = e4m3x2_to_f16x2(wv[tt]);
           const uint32_t b1 = e4m3x2_to_f16x2(wv[tt] >> 16);
-          mma_acc<false, kRows16>(s[nt], qa[4 * hh + tt], b0, b1);
+          if (tt & 1)
+            mma_acc<false, kRows16>(s2[nt], qa[4 * hh + tt], b0, b1);
+          else
+            mma_acc<false, kRows16>(s[nt], qa[4 * hh + tt], b0, b1);
         }
       }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
   }
   // scale, mask
   const int tA = perm_of(P, 2 * c), tB = perm_of(P, 2 * c + 1);
@@ -435,17 +474,25 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
       }
     st.l[half] = st.l[half] * alpha[half] + sum;
   }
+#ifndef PA_SKIP_RESCALE
+#define PA_SKIP_RESCALE 1
+#endif
+  const bool moved = alpha[0] != 1.f || (kRows16 && alpha[1] != 1.f);
+  if (!PA_SKIP_RESCALE || __any_sync(~0u, moved)) {
 #pragma unroll
-  for (int T = 0; T < 16; ++T) {
-    st.o[T][0] *= alpha[0];
-    st.o[T][1] *= alpha[0];
-    if constexpr (kRows16) {
-      st.o[T][2] *= alpha[1];
-      st.o[T][3] *= alpha[1];
+    for (int T = 0; T < 16; ++T) {
+      st.o[T][0] *= alpha[0];
+      st.o[T][1] *= alpha[0];
+      if constexpr (kRows16) {
+        st.o[T][2] *= alpha[1];
+        st.o[T][3] *= alpha[1];
+      }
     }
   }
-  // P as the A operand of P.V (k = key within the page)
-  uint32_t pa[4];
+  // P as the A operand of P.V (k = key within the page).  With bf16 MMA
+  // operands P is split into a bf16 head and a bf16 tail (p = hi + lo), so
+  // that P.V keeps ~16 bits of P instead of 8.
+  uint32_t pa[4], pl[4];
   pa[0] = pack2<kB>(s[0][0], s[0][1]);
   pa[2] = pack2<kB>(s[1][0], s[1][1]);
   if constexpr (kRows16) {
@@ -453,6 +500,16 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
     pa[3] = pack2<kB>(s[1][2], s[1][3]);
   } else {
     pa[1] = pa[3] = 0u;
+  }
+  if constexpr (kB) {
+    pl[0] = pack2<true>(s[0][0] - bf16_lo(pa[0]), s[0][1] - bf16_hi(pa[0]));
+    pl[2] = pack2<true>(s[1][0] - bf16_lo(pa[2]), s[1][1] - bf16_hi(pa[2]));
+    if constexpr (kRows16) {
+      pl[1] = pack2<true>(s[0][2] - bf16_lo(pa[1]), s[0][3] - bf16_hi(pa[1]));
+      pl[3] = pack2<true>(s[1][2] - bf16_lo(pa[3]), s[1][3] - bf16_hi(pa[3]));
+    } else {
+      pl[1] = pl[3] = 0u;
+    }
   }
   // V fragments: keys tA, tB, 8 + tA, 8 + tB
   const int tk[4] = {tA, tB, 8 + tA, 8 + tB};
@@ -465,7 +522,11 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
         const int t = tk[k];
         const int phys = r ^ (((t << 1) | h) & 7);
         v[k] = lds128(v_base + t * 256 + h * 128 + phys * 16);
-        if (t >= valid_keys) v[k] = make_uint4(0, 0, 0, 0);
+      }
+      if (valid_keys < kBS) {  // last page: slots past the sequence end
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (tk[k] >= valid_keys) v[k] = make_uint4(0, 0, 0, 0);
       }
       const uint32_t va[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
       const uint32_t vb[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
@@ -474,10 +535,16 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const int T = 8 * h + 2 * w;
-        mma_acc<kB, kRows16>(st.o[T], pa, __byte_perm(va[w], vb[w], 0x5410),
-                             __byte_perm(vc[w], vd[w], 0x5410));
-        mma_acc<kB, kRows16>(st.o[T + 1], pa, __byte_perm(va[w], vb[w], 0x7632),
-                             __byte_perm(vc[w], vd[w], 0x7632));
+        const uint32_t b00 = __byte_perm(va[w], vb[w], 0x5410);
+        const uint32_t b01 = __byte_perm(vc[w], vd[w], 0x5410);
+        const uint32_t b10 = __byte_perm(va[w], vb[w], 0x7632);
+        const uint32_t b11 = __byte_perm(vc[w], vd[w], 0x7632);
+        mma_acc<kB, kRows16>(st.o[T], pa, b00, b01);
+        mma_acc<kB, kRows16>(st.o[T + 1], pa, b10, b11);
+        if constexpr (kB) {
+          mma_acc<kB, kRows16>(st.o[T], pl, b00, b01);
+          mma_acc<kB, kRows16>(st.o[T + 1], pl, b10, b11);
+        }
       }
     }
   } else {
@@ -487,7 +554,11 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
       const int t = tk[k];
       const int phys = r ^ (t & 7);
       v[k] = lds128(v_base + t * 128 + phys * 16);
-      if (t >= valid_keys) v[k] = make_uint4(0, 0, 0, 0);
+    }
+    if (valid_keys < kBS) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (tk[k] >= valid_keys) v[k] = make_uint4(0, 0, 0, 0);
     }
     const uint32_t va[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
     const uint32_t vb[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
@@ -521,27 +592,112 @@ template <int kKind>
 using OutT = typename std::conditional<Traits<kKind>::kQBF16, __nv_bfloat16,
                                        __half>::type;
 
-struct SmemRefs {
-  uint32_t ring;   // shared address of the page ring (1024-aligned)
-  uint32_t bars;   // full[kStages] then empty[kStages]
-  volatile int* abort_flag;
-  float* scratch;  // generic pointer to the ring (epilogue reuse)
+constexpr int kItemQueue = 4;  // work items the producer may run ahead
+
+// Shared-memory carve-up of one CTA (offsets from a 1024-aligned base).
+template <int kKind, bool kWide>
+struct Layout {
+  using Tr = Traits<kKind>;
+  static constexpr int kE = kWide ? 4 : 2;  // accumulator rows kept per lane
+  static constexpr int kRing = 0;
+  static constexpr int kScratch = Tr::kRingBytes;                 // partial O
+  static constexpr int kScratchBytes = kConsumerWarps * 16 * kE * 32 * 4;
+  static constexpr int kML = kScratch + kScratchBytes;            // m, l
+  static constexpr int kMLBytes = kConsumerWarps * 16 * 2 * 4;
+  static constexpr int kBars = kML + kMLBytes;                    // 8 B each
+  static constexpr int kNumBars = 2 * Tr::kStages + 2 * kItemQueue;
+  static constexpr int kItems = kBars + 8 * kNumBars;             // int4 each
+  static constexpr int kAbort = kItems + 16 * kItemQueue;
+  static constexpr int kBytes = kAbort + 16;
+  static constexpr int kSmemBytes = 1024 + kBytes;  // + alignment slack
 };
 
-// Consumer warp: walk this warp's pages, then write (or hand over) results.
-template <int kKind, bool kRows16>
-__device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& rm,
-                        int r, int g, int kind, int x, int page0, int npages,
-                        int wrow0, int wrows, int first, int stride, int warp,
-                        int lane) {
+struct Smem {
+  uint32_t base;          // shared address, 1024-aligned
+  uint8_t* ptr;           // generic pointer to the same byte
+  int stages;
+  __device__ uint32_t full(int s) const { return bars + 8 * s; }
+  __device__ uint32_t empty(int s) const { return bars + 8 * (stages + s); }
+  __device__ uint32_t item_full(int q) const { return bars + 8 * (2 * stages + q); }
+  __device__ uint32_t item_empty(int q) const {
+    return bars + 8 * (2 * stages + kItemQueue + q);
+  }
+  uint32_t bars;
+  int4* items;
+  volatile int* abort_flag;
+  float* scratch;
+  float* ml;
+};
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t cnt) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   bar),
+               "r"(cnt)
+               : "memory");
+}
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Barrier of the consumer warps that also ORs a predicate over all of them,
+// so that every consumer takes the same decision.
+__device__ __forceinline__ bool consumers_sync_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// Geometry of a work item: its pages and its query rows.
+struct ItemGeom {
+  int page0, npages, row0, rows;
+};
+
+__device__ __forceinline__ ItemGeom item_geom(const FastParams& p, int kind,
+                                              int x, const ReqMeta& rm) {
+  ItemGeom ig;
+  if (kind == kItemDecode) {
+    ig.page0 = x * p.blocks_per_split;
+    ig.npages = min(p.blocks_per_split, rm.nb - ig.page0);
+    ig.row0 = 0;
+    ig.rows = rm.n * p.group;
+  } else {
+    ig.row0 = x * kPrefillTileRows;
+    ig.rows = min(kPrefillTileRows, rm.n * p.group - ig.row0);
+    const int lim_last = rm.L - rm.n + (ig.row0 + ig.rows - 1) / p.group;
+    ig.page0 = 0;
+    ig.npages = lim_last / kBS + 1;
+  }
+  return ig;
+}
+
+// One consumer warp's share of one work item.  Pages are numbered by the
+// CTA-wide counter c0 + j; in a decode item page c goes to warp c % 4 (the
+// same warp for a given ring slot, since the ring depth is a multiple of 4),
+// in a prefill tile every warp reads every page for its own 16 rows.
+template <int kKind, bool kRows16, bool kWide>
+__device__ void consume_item(const FastParams& p, const Smem& sm,
+                             const ReqMeta& rm, int r, int g, int kind, int x,
+                             const ItemGeom& ig, uint32_t c0, int warp,
+                             int lane) {
   using Tr = Traits<kKind>;
+  using Ly = Layout<kKind, kWide>;
   constexpr int S = Tr::kStages;
   const int rq = lane >> 2, c = lane & 3;
   const int G = p.group;
+  const bool decode = kind == kItemDecode;
+  const int wrow0 = decode ? 0 : ig.row0 + 16 * warp;
+  const int wrows = decode ? ig.rows : max(0, min(16, ig.rows - 16 * warp));
   uint32_t qa[8][4];
   float rscale[2];
   load_q<kKind, kRows16>(p, rm.q0, g, wrow0, wrows, lane, qa, rscale);
-  // causal limits of my two rows (padding rows: the sequence end)
   int lim[2];
   int my_min = INT_MAX;
 #pragma unroll
@@ -554,39 +710,42 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
     }
   }
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) my_min = min(my_min, __shfl_xor_sync(~0u, my_min, d));
+  for (int d = 1; d < 32; d <<= 1)
+    my_min = min(my_min, __shfl_xor_sync(~0u, my_min, d));
   const int min_lim = min(my_min, rm.L - 1);
   const float ss0 = p.score_scale * rscale[0];
   const float ss1 = p.score_scale * rscale[1];
 
   WarpState st;
 #pragma unroll
-  for (int T = 0; T < 16; ++T) st.o[T][0] = st.o[T][1] = st.o[T][2] = st.o[T][3] = 0.f;
+  for (int T = 0; T < 16; ++T)
+    st.o[T][0] = st.o[T][1] = st.o[T][2] = st.o[T][3] = 0.f;
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.f;
 
-  for (int i = first; i < npages; i += stride) {
-    const int slot = i % S;
-    const uint32_t full = sm.bars + 8 * slot;
-    const uint32_t empty = sm.bars + 8 * (S + slot);
-    const bool ok = __all_sync(~0u, mbar_wait_bounded(full, (i / S) & 1));
-    if (!ok) {
+  const int first = decode ? (int)((warp - (int)(c0 & 3u)) & 3) : 0;
+  const int stride = decode ? kConsumerWarps : 1;
+  bool alive = *sm.abort_flag == 0;
+  for (int j = first; j < ig.npages && alive; j += stride) {
+    const uint32_t cc = c0 + j;
+    const int slot = cc % S;
+    if (!__all_sync(~0u, mbar_wait_bounded(sm.full(slot), (cc / S) & 1))) {
       if (lane == 0) {
         flag_error(p.err, PA_DEV_ERR_TIMEOUT);
         *sm.abort_flag = 1;
       }
+      alive = false;
       break;
     }
-    const int key0 = (page0 + i) * kBS;
+    const int key0 = (ig.page0 + j) * kBS;
     const int valid = min(kBS, rm.L - key0);
     const bool need_mask = key0 + kBS - 1 > min_lim;
-    const uint32_t kb = sm.ring + slot * Tr::kStageBytes;
+    const uint32_t kb = sm.base + Ly::kRing + slot * Tr::kStageBytes;
     process_page<kKind, kRows16>(kb, kb + Tr::kPageBytes, qa, st, key0, valid,
                                  need_mask, lim[0], lim[1], ss0, ss1, lane);
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty);
+    if (lane == 0) mbar_arrive_cnt(sm.empty(slot), decode ? kConsumerWarps : 1);
   }
-  // full row sums
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     st.l[half] += __shfl_xor_sync(~0u, st.l[half], 1);
@@ -595,8 +754,7 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
   const int Hq = p.num_q_heads;
   constexpr int kE = kRows16 ? 4 : 2;
 
-  if (kind == kItemPrefill) {
-    // each warp owns its rows: normalise and store
+  if (!decode) {
 #pragma unroll
     for (int T = 0; T < 16; ++T)
 #pragma unroll
@@ -615,14 +773,16 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
     return;
   }
 
-  // decode item: merge the four warps' partial states through shared memory
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-  float* of = sm.scratch;                            // [4][16][4][32]
-  float* ml = sm.scratch + kConsumerWarps * 16 * 4 * 32;  // [4][16][2]
+  // decode item: merge the four warps' partial states in shared memory (the
+  // scratch is free: every warp passed the item-start barrier after its last
+  // read of it)
+  float* of = sm.scratch;
+  float* ml = sm.ml;
 #pragma unroll
   for (int T = 0; T < 16; ++T)
 #pragma unroll
-    for (int e = 0; e < kE; ++e) of[((warp * 16 + T) * 4 + e) * 32 + lane] = st.o[T][e];
+    for (int e = 0; e < kE; ++e)
+      of[((warp * 16 + T) * Ly::kE + e) * 32 + lane] = st.o[T][e];
   if (c == 0) {
     ml[(warp * 16 + rq) * 2 + 0] = st.m[0];
     ml[(warp * 16 + rq) * 2 + 1] = st.l[0];
@@ -631,7 +791,7 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
       ml[(warp * 16 + rq + 8) * 2 + 1] = st.l[1];
     }
   }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  consumers_sync();
   const int nsplit = __ldg(p.req_nsplit + r);
 #pragma unroll
   for (int Tq = 0; Tq < 4; ++Tq) {
@@ -650,7 +810,7 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) {
         const float a = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
-        num += a * of[((w * 16 + T) * 4 + e) * 32 + lane];
+        num += a * of[((w * 16 + T) * Ly::kE + e) * 32 + lane];
         den += a * ml[(w * 16 + rr) * 2 + 1];
       }
       const int i = rr / G;
@@ -671,129 +831,211 @@ __device__ void consume(const FastParams& p, const SmemRefs& sm, const ReqMeta& 
   }
 }
 
-template <int kKind>
-__global__ void __launch_bounds__(kThreads, 1)
+// kWide = false: every work item has at most 8 query rows (decode steps with
+// q_len * group <= 8) -- half the accumulators.
+// kWide = true: any item (up to 16 rows per warp, prefill tiles).
+//
+// Persistent: each CTA claims work items from a device-wide counter until
+// none are left.  Warp 4 (producer) claims items, publishes them through a
+// small shared-memory queue and streams their pages into the ring; warps 0-3
+// consume.  The ring keeps streaming across item boundaries.
+template <int kKind, bool kWide>
+__global__ void __launch_bounds__(kThreads, 2)
 attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ FastParams p) {
   using Tr = Traits<kKind>;
+  using Ly = Layout<kKind, kWide>;
   constexpr int S = Tr::kStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw);
-  SmemRefs sm;
-  sm.ring = base;
-  sm.bars = base + Tr::kRingBytes;
-  sm.abort_flag = reinterpret_cast<volatile int*>(base_ptr + Tr::kRingBytes + 16 * S);
-  sm.scratch = reinterpret_cast<float*>(base_ptr);
+  Smem sm;
+  sm.base = (raw + 1023u) & ~1023u;
+  sm.ptr = smem_raw + (sm.base - raw);
+  sm.stages = S;
+  sm.bars = sm.base + Ly::kBars;
+  sm.items = reinterpret_cast<int4*>(sm.ptr + Ly::kItems);
+  sm.abort_flag = reinterpret_cast<volatile int*>(sm.ptr + Ly::kAbort);
+  sm.scratch = reinterpret_cast<float*>(sm.ptr + Ly::kScratch);
+  sm.ml = reinterpret_cast<float*>(sm.ptr + Ly::kML);
 
-  if ((int64_t)blockIdx.x >= (int64_t)__ldg(p.num_items)) return;
-  const int4 item = __ldg(p.items + blockIdx.x);
-  const int r = item.x, g = item.y, kind = item.z, x = item.w;
-  const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
-                              p.max_seq_len, p.max_blocks_per_seq);
-  const int G = p.group;
-  int page0, npages, row0, rows, consumers;
-  if (kind == kItemDecode) {
-    page0 = x * p.blocks_per_split;
-    npages = min(p.blocks_per_split, rm.nb - page0);
-    row0 = 0;
-    rows = rm.n * G;
-    consumers = 1;
-  } else {
-    row0 = x * kPrefillTileRows;
-    rows = min(kPrefillTileRows, rm.n * G - row0);
-    const int lim_last = rm.L - rm.n + (row0 + rows - 1) / G;
-    page0 = 0;
-    npages = lim_last / kBS + 1;
-    consumers = kConsumerWarps;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(sm.bars + 8 * s, 1);
-      mbar_init(sm.bars + 8 * (S + s), consumers);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(sm.full(i), 1);
+      mbar_init(sm.empty(i), kConsumerWarps);
+    }
+    for (int q = 0; q < kItemQueue; ++q) {
+      mbar_init(sm.item_full(q), 1);
+      mbar_init(sm.item_empty(q), kConsumerWarps);
     }
     *sm.abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
+  const int num_items = __ldg(p.num_items);
 
   if (warp == kConsumerWarps) {
-    // ---------------- producer warp ----------------
+    // ------------------------------ producer ------------------------------
     if (lane == 0) {
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
     }
-    const int32_t* bt = p.block_tables + (int64_t)r * p.max_blocks_per_seq + page0;
-    int blk_cache = 0;
-    int issued = 0;
-    for (int i = 0; i < npages; ++i) {
-      if ((i & 31) == 0) {
-        const int idx = i + lane;
-        blk_cache = idx < npages ? __ldg(bt + idx) : 0;
-      }
-      int blk = __shfl_sync(~0u, blk_cache, i & 31);
-      int go = 1;
+    uint32_t c = 0;     // pages issued
+    for (int k = 0;; ++k) {
+      const int q = k % kItemQueue;
+      int4 it = make_int4(-1, 0, 0, 0);
       if (lane == 0) {
-        const int slot = i % S;
-        if (i >= S && !mbar_wait_bounded(sm.bars + 8 * (S + slot), ((i / S) - 1) & 1)) {
+        bool ok = k < kItemQueue ||
+                  mbar_wait_bounded(sm.item_empty(q), ((k / kItemQueue) - 1) & 1);
+        if (!ok) {
           flag_error(p.err, PA_DEV_ERR_TIMEOUT);
           *sm.abort_flag = 1;
         }
-        if (*sm.abort_flag) {
-          go = 0;
-        } else {
-          if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-            flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
-            blk = 0;
-          }
-          const int row = (blk * p.num_kv_heads + g) * kBS;
-          const uint32_t full = sm.bars + 8 * slot;
-          const uint32_t dst = sm.ring + slot * Tr::kStageBytes;
-          mbar_arrive_expect_tx(full, Tr::kStageBytes);
-          if constexpr (Tr::kFp8) {
-            tma_load_2d(dst, &tmap_k, full, 0, row);
-            tma_load_2d(dst + Tr::kPageBytes, &tmap_v, full, 0, row);
-          } else {
-            tma_load_3d(dst, &tmap_k, full, 0, 0, row);
-            tma_load_3d(dst + Tr::kPageBytes, &tmap_v, full, 0, 0, row);
-          }
-          issued = i + 1;
+        if (ok && *sm.abort_flag == 0) {
+          const int idx = atomicAdd(p.work_counter, 1);
+          if (idx < num_items) it = __ldg(p.items + idx);
+        }
+        if (ok) {
+          sm.items[q] = it;
+          mbar_arrive(sm.item_full(q));
         }
       }
-      go = __shfl_sync(~0u, go, 0);
-      if (!go) break;
-    }
-    // after an abort, let the copies already in flight land before exiting
-    if (lane == 0 && *sm.abort_flag) {
-      const int from = issued > S ? issued - S : 0;
-      for (int i = from; i < issued; ++i)
-        mbar_wait_bounded(sm.bars + 8 * (i % S), (i / S) & 1);
+      it.x = __shfl_sync(~0u, it.x, 0);
+      it.y = __shfl_sync(~0u, it.y, 0);
+      it.z = __shfl_sync(~0u, it.z, 0);
+      it.w = __shfl_sync(~0u, it.w, 0);
+      if (it.x < 0) break;
+      const ReqMeta rm = load_req(p.qsl, p.seq_lens, it.x, p.num_tokens,
+                                  p.max_query_len, p.max_seq_len,
+                                  p.max_blocks_per_seq);
+      const ItemGeom ig = item_geom(p, it.z, it.w, rm);
+      if (!kWide && (it.z == kItemPrefill || ig.rows > 8)) continue;
+      const int32_t* bt =
+          p.block_tables + (int64_t)it.x * p.max_blocks_per_seq + ig.page0;
+      // block ids of this item, 32 per register, loaded two chunks ahead
+      const int n = ig.npages;
+      int ids0 = lane < n ? __ldg(bt + lane) : 0;
+      int ids1 = 32 + lane < n ? __ldg(bt + 32 + lane) : 0;
+      int ids2 = 64 + lane < n ? __ldg(bt + 64 + lane) : 0;
+      constexpr int PF = PA_L2_PREFETCH_PAGES;
+      static_assert(PF >= 0 && PF <= 32, "prefetch window must fit one id chunk");
+      auto page_row = [&](int blk) {
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+          flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+          blk = 0;
+        }
+        return (blk * p.num_kv_heads + it.y) * kBS;
+      };
+      auto prefetch = [&](int row) {
+        if constexpr (Tr::kFp8) {
+          tma_prefetch_2d(&tmap_k, 0, row);
+          tma_prefetch_2d(&tmap_v, 0, row);
+        } else {
+          tma_prefetch_3d(&tmap_k, 0, 0, row);
+          tma_prefetch_3d(&tmap_v, 0, 0, row);
+        }
+      };
+      // the first window goes to L2 at once
+      if (PF > 0 && lane < min(PF, n)) prefetch(page_row(ids0));
+      int go = 1;
+      for (int j = 0; j < n && go; ++j, ++c) {
+        if (j > 0 && (j & 31) == 0) {
+          ids0 = ids1;
+          ids1 = ids2;
+          const int idx = j + 64 + lane;
+          ids2 = idx < n ? __ldg(bt + idx) : 0;
+        }
+        int blk = __shfl_sync(~0u, ids0, j & 31);
+        const int jp = j + PF;
+        const int blk_pf = __shfl_sync(~0u, (jp >> 5) == (j >> 5) ? ids0 : ids1,
+                                       jp & 31);
+        if (lane == 0) {
+          if (PF > 0 && jp < n) prefetch(page_row(blk_pf));
+          const int slot = c % S;
+          if (c >= (uint32_t)S &&
+              !mbar_wait_bounded(sm.empty(slot), ((c / S) - 1) & 1)) {
+            flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+            *sm.abort_flag = 1;
+          }
+          if (*sm.abort_flag) {
+            go = 0;
+          } else {
+            const int row = page_row(blk);
+            const uint32_t dst = sm.base + Ly::kRing + slot * Tr::kStageBytes;
+            mbar_arrive_expect_tx(sm.full(slot), Tr::kStageBytes);
+            if constexpr (Tr::kFp8) {
+              tma_load_2d(dst, &tmap_k, sm.full(slot), 0, row);
+              tma_load_2d(dst + Tr::kPageBytes, &tmap_v, sm.full(slot), 0, row);
+            } else {
+              tma_load_3d(dst, &tmap_k, sm.full(slot), 0, 0, row);
+              tma_load_3d(dst + Tr::kPageBytes, &tmap_v, sm.full(slot), 0, 0, row);
+            }
+          }
+        }
+        go = __shfl_sync(~0u, go, 0);
+      }
+      if (!go) {
+        // stop claiming; hand the consumers an end marker if a queue slot
+        // frees up, then let the copies already in flight land
+        if (lane == 0) {
+          const int q2 = (k + 1) % kItemQueue;
+          if (k + 1 < kItemQueue ||
+              mbar_wait_bounded(sm.item_empty(q2), (((k + 1) / kItemQueue) - 1) & 1)) {
+            sm.items[q2] = make_int4(-1, 0, 0, 0);
+            mbar_arrive(sm.item_full(q2));
+          }
+          const uint32_t from = c > (uint32_t)S ? c - S : 0;
+          for (uint32_t i = from; i < c; ++i)
+            mbar_wait_bounded(sm.full(i % S), (i / S) & 1);
+        }
+        break;
+      }
     }
     return;
   }
 
-  // ---------------- consumer warps ----------------
-  int wrow0, wrows, first, stride;
-  if (kind == kItemDecode) {
-    wrow0 = 0;
-    wrows = rows;
-    first = warp;
-    stride = kConsumerWarps;
-  } else {
-    wrow0 = row0 + 16 * warp;
-    wrows = max(0, min(16, rows - 16 * warp));
-    first = 0;
-    stride = 1;
+  // ------------------------------ consumers -------------------------------
+  uint32_t c = 0;  // pages consumed (CTA-wide numbering, as issued)
+  for (int k = 0;; ++k) {
+    const int q = k % kItemQueue;
+    const bool got =
+        __all_sync(~0u, mbar_wait_bounded(sm.item_full(q), (k / kItemQueue) & 1));
+    int4 it = make_int4(-1, 0, 0, 0);
+    if (got) {
+      it = sm.items[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.item_empty(q));
+    } else if (lane == 0) {
+      flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+      *sm.abort_flag = 1;
+    }
+    // every consumer warp meets here once per item: decisions below are
+    // uniform, the previous item's shared scratch is no longer read, and all
+    // earlier pages have been consumed by their owners
+    if (consumers_sync_any(it.x < 0 || *sm.abort_flag != 0)) break;
+    const ReqMeta rm = load_req(p.qsl, p.seq_lens, it.x, p.num_tokens,
+                                p.max_query_len, p.max_seq_len,
+                                p.max_blocks_per_seq);
+    const ItemGeom ig = item_geom(p, it.z, it.w, rm);
+    if constexpr (kWide) {
+      if (it.z == kItemPrefill || ig.rows > 8)
+        consume_item<kKind, true, true>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
+                                        c, warp, lane);
+      else
+        consume_item<kKind, false, true>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
+                                         c, warp, lane);
+    } else {
+      if (it.z == kItemPrefill || ig.rows > 8) {
+        // the host never sends such an item to the narrow kernel
+        if (threadIdx.x == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
+        continue;
+      }
+      consume_item<kKind, false, false>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
+                                        c, warp, lane);
+    }
+    c += ig.npages;
   }
-  if (kind == kItemPrefill || rows > 8)
-    consume<kKind, true>(p, sm, rm, r, g, kind, x, page0, npages, wrow0, wrows,
-                         first, stride, warp, lane);
-  else
-    consume<kKind, false>(p, sm, rm, r, g, kind, x, page0, npages, wrow0, wrows,
-                          first, stride, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -843,36 +1085,70 @@ merge_kernel(FastParams p) {
   for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
 }
 
+template <int kKind, bool kWide>
+cudaError_t prepare_kernel(int* grid) {
+  using Ly = Layout<kKind, kWide>;
+  static int blocks_per_sm[64] = {0};
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (blocks_per_sm[dev] == 0) {
+    e = cudaFuncSetAttribute(attn_fast_kernel<kKind, kWide>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ly::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_fast_kernel<kKind, kWide>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &nb, attn_fast_kernel<kKind, kWide>, kThreads, Ly::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n_sm;
+    blocks_per_sm[dev] = nb > 0 ? nb : 1;
+  }
+  *grid = blocks_per_sm[dev] * sms[dev];
+  return cudaSuccess;
+}
+
 template <int kKind>
 cudaError_t launch_kind(const FastParams& fp, const AttnPlan& plan,
                         const CUtensorMap& tk, const CUtensorMap& tv,
                         int4* items, int* count, int* nsplit,
                         cudaStream_t stream) {
   using Tr = Traits<kKind>;
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fast_kernel<kKind>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Tr::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
-  }
+  (void)Tr::kStages;
+  // the narrow kernel covers steps whose every item has <= 8 rows
+  const bool wide = (int64_t)fp.max_query_len * fp.group > 8;
+  int grid = 0;
+  cudaError_t e = wide ? prepare_kernel<kKind, true>(&grid)
+                       : prepare_kernel<kKind, false>(&grid);
+  if (e != cudaSuccess) return e;
+  if ((int64_t)grid > plan.max_items) grid = (int)plan.max_items;
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(fp, items, count, nsplit);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const ProfileEvents& pe = profile_events();
   if (pe.start) cudaEventRecord(pe.start, stream);
-  attn_fast_kernel<kKind><<<(unsigned)plan.max_items, kThreads, Tr::kSmemBytes, stream>>>(
-      tk, tv, fp);
+  if (wide)
+    attn_fast_kernel<kKind, true>
+        <<<grid, kThreads, Layout<kKind, true>::kSmemBytes, stream>>>(tk, tv, fp);
+  else
+    attn_fast_kernel<kKind, false>
+        <<<grid, kThreads, Layout<kKind, false>::kSmemBytes, stream>>>(tk, tv, fp);
   e = cudaGetLastError();
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
   if (plan.max_splits > 1) {
     const int64_t rows = fp.num_tokens * fp.num_q_heads;
-    const unsigned grid = (unsigned)((rows + 3) / 4);
-    merge_kernel<OutT<kKind>><<<grid, 128, 0, stream>>>(fp);
+    const unsigned mgrid = (unsigned)((rows + 3) / 4);
+    merge_kernel<OutT<kKind>><<<mgrid, 128, 0, stream>>>(fp);
     e = cudaGetLastError();
   }
   return e;
@@ -899,14 +1175,14 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
   // Split size: aim for several waves of CTAs (two resident per SM) so that
   // the tail of the step is short, but keep every split long enough to hide
   // its pipeline start-up and bound the number of partial results.
-  const int64_t target = (int64_t)num_sms * 2 * 4;
+  const int64_t target = (int64_t)num_sms * PA_SPLIT_WAVES;
   const int64_t units = (int64_t)num_seqs * num_kv_heads;
   int64_t bps = mb;
   if (units > 0) {
     const int64_t want_splits = (target + units - 1) / units;
     bps = (mb + want_splits - 1) / want_splits;
   }
-  if (bps < 32) bps = 32;
+  if (bps < PA_SPLIT_MIN_BLOCKS) bps = PA_SPLIT_MIN_BLOCKS;
   if (bps > mb) bps = mb;
   if (bps < 1) bps = 1;
   int64_t ms = (mb + bps - 1) / bps;
@@ -956,6 +1232,7 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.qsl = a.query_start_loc;
   fp.items = reinterpret_cast<const int4*>(ws + plan.off_items);
   fp.num_items = reinterpret_cast<const int*>(ws + plan.off_count);
+  fp.work_counter = reinterpret_cast<int*>(ws + plan.off_count + 4);
   fp.req_nsplit = reinterpret_cast<const int*>(ws + plan.off_nsplit);
   fp.ws_acc = reinterpret_cast<float*>(ws + plan.off_acc);
   fp.ws_ml = reinterpret_cast<float*>(ws + plan.off_ml);
