@@ -8,24 +8,28 @@
 // through the block table from 16-token pages.
 //
 // How (GB300):
-//  * A plan kernel turns (query_start_loc, seq_lens) into a work list on the
-//    device: decode-class requests (q_len * group <= 16 rows) are cut into
-//    splits of `blocks_per_split` pages along the context (split-K), long
-//    prompts into 64-row tiles.  Big items first.
-//  * The main kernel runs one work item per CTA: a producer warp walks the
-//    block table and streams each (block, KV head) page of K and V into a
-//    shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte swizzle),
+//  * A planner kernel (one CTA) lays the step's work on one line -- prefill
+//    tiles of 64 query rows (indivisible, weighted by their key pages), then
+//    one segment of key pages per (decode request, KV head) -- and cuts it
+//    into equal contiguous ranges, one per resident CTA of the attention
+//    kernel (stream-K).  A segment cut by a range boundary is finished by the
+//    merge kernel from one partial result per piece.
+//  * The attention kernel is persistent: in every CTA a producer warp walks
+//    the CTA's items and streams each (block, KV head) page of K and V into
+//    a shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte swizzle),
 //    completing on mbarriers; four consumer warps run Q.K^T and P.V on the
-//    warp-level tensor-core MMA straight from the swizzled pages, with an
-//    fp32 online softmax in registers.  A decode item spreads its pages over
-//    the four warps and merges them in shared memory; a prefill tile gives
-//    each warp 16 rows and all pages.
-//  * A merge kernel combines the splits of a request in a fixed order
+//    warp-level tensor-core MMA straight from the swizzled pages with an fp32
+//    online softmax in registers.  Decode pages go round-robin to the four
+//    warps (merged through shared memory at the end of the piece); a prefill
+//    tile gives each warp 16 rows and all pages.  The ring streams across
+//    item boundaries.
+//  * The merge combines the parts of a split segment in a fixed order
 //    (deterministic): M = max m_s, out = sum e^{m_s-M} acc_s / sum e^{m_s-M} l_s.
+//  * The attention kernel and the merge are launched as programmatic
+//    dependents of their predecessors.
 //
-// Decode is HBM-bound: every page is read from HBM exactly once per step and
-// the MMA only keeps the ALU work (group x 128 MACs per key) off the CUDA
-// cores.
+// Decode is HBM-bound: every page is read from HBM once per step and the MMA
+// only keeps the ALU work (group x 128 MACs per key) off the CUDA cores.
 #include <float.h>
 
 #include "pa_common.cuh"
@@ -37,22 +41,27 @@ namespace {
 #ifndef PA_NARROW_MIN_BLOCKS
 #define PA_NARROW_MIN_BLOCKS 3  // resident CTAs per SM, <= 8-row kernel
 #endif
-#ifndef PA_SPLIT_MIN_BLOCKS
-#define PA_SPLIT_MIN_BLOCKS 16  // smallest decode split, in blocks
+constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
+
+#ifndef PA_PREFILL_WEIGHT
+#define PA_PREFILL_WEIGHT 4     // cost of a prefill tile page vs a decode page
 #endif
-#ifndef PA_SPLIT_WAVES
-#define PA_SPLIT_WAVES 16       // target decode items per SM
+#ifndef PA_CONSUMER_WARPS
+#define PA_CONSUMER_WARPS 4     // consumer warps per CTA (one producer warp)
 #endif
-#ifndef PA_L2_PREFETCH_PAGES
-#define PA_L2_PREFETCH_PAGES 0  // pages prefetched into L2 ahead of the ring (0: off)
+#ifndef PA_CTAS_PER_SM
+#define PA_CTAS_PER_SM 2        // resident CTAs per SM the kernel is built for
 #endif
 #ifndef PA_STAGES_16BIT
 #define PA_STAGES_16BIT 8       // ring depth in pages, bf16 / fp16 caches
 #endif
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = PA_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+static_assert(kConsumerWarps == 4 || kConsumerWarps == 8,
+              "4 or 8 consumer warps");
 constexpr int kPlanThreads = 1024;
+
 
 // ---------------------------------------------------------------------------
 // compile-time traits of the four supported (cache, q) type pairs
@@ -70,8 +79,13 @@ struct Traits {
   static constexpr int kStages = kFp8 ? 2 * PA_STAGES_16BIT : PA_STAGES_16BIT;
   static constexpr int kRingBytes = kStages * kStageBytes;  // 64 KiB
   // Token order inside an 8-token MMA tile (row n of the tile holds token
-  // perm(n)).  Chosen so that the fragment reads of both K and V from the
-  // 128-byte-swizzled pages are free of shared-memory bank conflicts.
+  // perm(n)).  A page sits in shared memory as the TMA wrote it under the
+  // 128-byte swizzle: FP8 rows of 128 bytes (16-byte chunk k of token t at
+  // chunk k ^ (t & 7)); 16-bit rows of 256 bytes, two 128-byte segments
+  // (chunk k of segment h of token t at k ^ ((2t + h) & 7)).  With these
+  // orders (0,5,2,7,4,1,6,3 for FP8, 0,2,1,3,6,4,7,5 for 16-bit) the 16-byte
+  // fragment reads of K and V are free of bank conflicts; the transposing
+  // V reads of the decode path are two-way.
   static constexpr uint32_t kPerm = kFp8 ? 0x36147250u : 0x57463120u;
   // A decode item hands page i to warp i % 4 through slot i % kStages.  The
   // ring depth must be a multiple of the consumer count so that every slot
@@ -100,12 +114,13 @@ struct FastParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
-  const int4* items;
-  const int* num_items;
-  int* work_counter;     // next unclaimed work item (zeroed by the planner)
-  const int* req_nsplit;
-  float* ws_acc;
-  float* ws_ml;
+  const int4* items;      // 2 x int4 per work item (see the planner)
+  const int* cta_begin;   // work items of CTA b: [cta_begin[b], cta_begin[b+1])
+  const int4* split_list; // segments cut into parts: {r, g, parts, first}
+  const int* n_split;
+  int max_slots;
+  float* ws_acc;          // partial O: [slot][16 rows][128]
+  float* ws_ml;           // partial (m, l): [slot][16 rows][2]
   unsigned* err;
   int64_t num_tokens;
   int64_t num_blocks;
@@ -113,129 +128,356 @@ struct FastParams {
   int num_seqs;
   int num_q_heads, num_kv_heads, group;
   int max_query_len, max_seq_len;
-  int blocks_per_split, max_splits;
-  int64_t max_items;
   float score_scale;  // softmax scale * log2(e) (* k_scale for FP8)
   float out_scale;    // 1, or v_scale for FP8
 };
 
 // ---------------------------------------------------------------------------
-// plan kernel: one CTA builds the work list
+// planner: one CTA lays the step's work on one line and cuts it into equal
+// contiguous ranges, one per CTA of the attention kernel
+//
+// Work units: a prefill tile (kPrefillTileRows query rows of one KV head,
+// all keys up to the tile's causal limit) is indivisible and costs
+// `prefill_weight` per key page; a decode-class request (q_len * group <= 16
+// rows) contributes one segment per KV head, one unit per key page, which may
+// be cut anywhere.  Prefill tiles come first, then the decode segments in
+// (request, head) order.  CTA b owns the cost interval [b*C/G, (b+1)*C/G):
+// every tile that starts in it, and the pieces of the segments that overlap
+// it.  A segment cut by CTA boundaries is finished by the merge kernel from
+// one partial result per piece (at most 2G of them in total).
 // ---------------------------------------------------------------------------
-struct Counts {
-  int pre, full, last;
+struct PlanArgs {
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  unsigned* err;
+  int64_t num_tokens;
+  int num_seqs, max_query_len, max_seq_len, max_blocks_per_seq;
+  int group, num_kv_heads, grid, prefill_weight;
+  int max_atoms, max_items, max_slots;
+  int4* atoms;            // prefill tiles: {r, g, tile, pages}
+  long long* atom_start;  // cost offset of each tile
+  long long* req_dec0;    // decode-unit offset of each request
+  int* req_declen;        // key pages of a decode-class request (0 if none)
+  int* req_rows;          // query rows (q_len * group) of each request
+  int2* seg_cut;          // per (request, KV head): first partial slot, first CTA
+  int4* items;
+  int* cta_begin;
+  float* ws_ml;           // partial (m, l), initialised here
+  int4* split_list;       // segments cut by CTA boundaries: {r, g, parts, first}
+  int* n_split;
 };
 
-__device__ __forceinline__ Counts block_exclusive_scan(Counts v, Counts* total,
-                                                       Counts* warp_sums) {
+template <typename T>
+__device__ __forceinline__ T block_scan_excl(T v, T* total, T* warp_sums) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  Counts inc = v;
+  T inc = v;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    int a = __shfl_up_sync(~0u, inc.pre, d);
-    int b = __shfl_up_sync(~0u, inc.full, d);
-    int c = __shfl_up_sync(~0u, inc.last, d);
-    if (lane >= d) {
-      inc.pre += a;
-      inc.full += b;
-      inc.last += c;
-    }
+    const T o = __shfl_up_sync(~0u, inc, d);
+    if (lane >= d) inc += o;
   }
   if (lane == 31) warp_sums[warp] = inc;
   __syncthreads();
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
-    Counts w = lane < nw ? warp_sums[lane] : Counts{0, 0, 0};
+    T w = lane < nw ? warp_sums[lane] : T(0);
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      int a = __shfl_up_sync(~0u, w.pre, d);
-      int b = __shfl_up_sync(~0u, w.full, d);
-      int c = __shfl_up_sync(~0u, w.last, d);
-      if (lane >= d) {
-        w.pre += a;
-        w.full += b;
-        w.last += c;
-      }
+      const T o = __shfl_up_sync(~0u, w, d);
+      if (lane >= d) w += o;
     }
-    if (lane < nw) warp_sums[lane] = w;  // inclusive warp prefix
+    if (lane < nw) warp_sums[lane] = w;
     if (lane == nw - 1) *total = w;
   }
   __syncthreads();
-  Counts base = warp == 0 ? Counts{0, 0, 0} : warp_sums[warp - 1];
-  Counts ex;
-  ex.pre = base.pre + inc.pre - v.pre;
-  ex.full = base.full + inc.full - v.full;
-  ex.last = base.last + inc.last - v.last;
-  __syncthreads();  // warp_sums / total reused by the next chunk
+  const T ex = (warp == 0 ? T(0) : warp_sums[warp - 1]) + inc - v;
+  __syncthreads();
   return ex;
 }
 
-__global__ void __launch_bounds__(kPlanThreads)
-plan_kernel(FastParams p, int4* items, int* num_items, int* req_nsplit) {
-  __shared__ Counts warp_sums[32];
-  __shared__ Counts chunk_total;
-  const int G = p.group, H = p.num_kv_heads;
-  // pass 1: totals of the three item classes (prefill tiles, full decode
-  // splits, last decode splits)
-  Counts run{0, 0, 0};
-  int total_pre = 0, total_full = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    run = Counts{0, 0, 0};
-    for (int base = 0; base < p.num_seqs; base += blockDim.x) {
-      const int r = base + threadIdx.x;
-      Counts c{0, 0, 0};
-      int tiles = 0, splits = 0;
-      ReqMeta m{0, 0, 0, 0, false};
-      if (r < p.num_seqs) {
-        m = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
-                     p.max_seq_len, p.max_blocks_per_seq);
-        if (!m.ok) {
-          if (pass == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
-        } else if (m.n > 0) {
-          if (m.n * G <= kDecodeMaxRows) {
-            splits = (m.nb + p.blocks_per_split - 1) / p.blocks_per_split;
-            c.full = (splits - 1) * H;
-            c.last = H;
+// key pages seen by prefill tile tt of a request (its last row's limit)
+__device__ __forceinline__ int tile_pages(const ReqMeta& m, int G, int tt) {
+  const int last_row = min(m.n * G, (tt + 1) * kPrefillTileRows) - 1;
+  return (m.L - m.n + last_row / G) / kBS + 1;
+}
+
+__device__ __forceinline__ long long cta_lo(int b, long long C, int grid) {
+  return (long long)b * C / grid;
+}
+
+// last CTA whose range starts at or before cost c (los[b] = start of CTA b)
+__device__ __forceinline__ int cta_of(long long c, const long long* los,
+                                      int grid) {
+  int lo = 0, hi = grid - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (los[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// first index in [0, n) with a[i] >= x (n if none)
+__device__ __forceinline__ int lower_bound_ll(const long long* a, int n,
+                                              long long x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+constexpr int kPlanCacheBytes = 40 * 1024;  // dynamic shared memory of the planner
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
+  extern __shared__ long long plan_cache[];
+  // the attention kernel may start its prologue now; it waits for this
+  // grid to finish before it reads the plan
+  pdl_launch_dependents();
+  __shared__ long long ws_ll[32];
+  __shared__ int ws_i[32];
+  __shared__ long long tot_ll;
+  __shared__ int tot_i;
+  __shared__ long long s_atoms, s_cost_pre, s_dec_total;
+  const int G = pa.group, H = pa.num_kv_heads, W = pa.prefill_weight;
+  // ---- 1: per request: prefill tiles (with their costs) and decode pages
+  long long run_atoms = 0, run_pcost = 0, run_dec = 0;
+  for (int base = 0; base < pa.num_seqs; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    ReqMeta m{0, 0, 0, 0, false};
+    int tiles = 0, declen = 0;
+    long long pcost = 0;
+    if (r < pa.num_seqs) {
+      m = load_req(pa.qsl, pa.seq_lens, r, pa.num_tokens, pa.max_query_len,
+                   pa.max_seq_len, pa.max_blocks_per_seq);
+      if (!m.ok) {
+        flag_error(pa.err, PA_DEV_ERR_METADATA);
+      } else if (m.n > 0) {
+        if (m.n * G <= kDecodeMaxRows) {
+          declen = m.nb;
+        } else {
+          tiles = (m.n * G + kPrefillTileRows - 1) / kPrefillTileRows;
+          for (int tt = 0; tt < tiles; ++tt) pcost += (long long)tile_pages(m, G, tt) * W;
+        }
+      }
+    }
+    const long long atoms_r = (long long)tiles * H;
+    const long long pcost_r = pcost * H;
+    const long long dec_r = (long long)declen * H;
+    const long long ex_atoms = block_scan_excl<long long>(atoms_r, &tot_ll, ws_ll);
+    const long long t_atoms = tot_ll;
+    __syncthreads();
+    const long long ex_pcost = block_scan_excl<long long>(pcost_r, &tot_ll, ws_ll);
+    const long long t_pcost = tot_ll;
+    __syncthreads();
+    const long long ex_dec = block_scan_excl<long long>(dec_r, &tot_ll, ws_ll);
+    const long long t_dec = tot_ll;
+    __syncthreads();
+    if (r < pa.num_seqs) {
+      pa.req_dec0[r] = run_dec + ex_dec;
+      pa.req_declen[r] = declen;
+      pa.req_rows[r] = m.ok ? m.n * G : 0;
+      long long a0 = run_atoms + ex_atoms;
+      long long c0 = run_pcost + ex_pcost;
+      for (int tt = 0; tt < tiles; ++tt) {
+        const int pg = tile_pages(m, G, tt);
+        const long long c = (long long)pg * W;
+        for (int g = 0; g < H; ++g) {
+          const long long ai = a0 + (long long)tt * H + g;
+          if (ai < pa.max_atoms) {
+            pa.atoms[ai] = make_int4(r, g, tt, pg);
+            pa.atom_start[ai] = c0 + g * c;
           } else {
-            tiles = (m.n * G + kPrefillTileRows - 1) / kPrefillTileRows;
-            c.pre = tiles * H;
+            flag_error(pa.err, PA_DEV_ERR_METADATA);
           }
         }
-        if (pass == 0) req_nsplit[r] = splits;
+        c0 += c * H;
       }
-      Counts ex = block_exclusive_scan(c, &chunk_total, warp_sums);
-      if (pass == 1 && r < p.num_seqs) {
-        // prefill tiles, last tile (most keys) first
-        int o = run.pre + ex.pre;
-        for (int tt = tiles - 1; tt >= 0; --tt)
-          for (int g = 0; g < H; ++g)
-            if (o < p.max_items) items[o++] = make_int4(r, g, kItemPrefill, tt);
-        o = total_pre + run.full + ex.full;
-        for (int s = 0; s < splits - 1; ++s)
-          for (int g = 0; g < H; ++g)
-            if (o < p.max_items) items[o++] = make_int4(r, g, kItemDecode, s);
-        o = total_pre + total_full + run.last + ex.last;
-        if (splits > 0)
-          for (int g = 0; g < H; ++g)
-            if (o < p.max_items)
-              items[o++] = make_int4(r, g, kItemDecode, splits - 1);
-      }
-      run.pre += chunk_total.pre;
-      run.full += chunk_total.full;
-      run.last += chunk_total.last;
-      __syncthreads();
     }
-    total_pre = run.pre;
-    total_full = run.full;
+    run_atoms += t_atoms;
+    run_pcost += t_pcost;
+    run_dec += t_dec;
   }
   if (threadIdx.x == 0) {
-    int64_t n = (int64_t)run.pre + run.full + run.last;
-    if (n > p.max_items) {
-      flag_error(p.err, PA_DEV_ERR_METADATA);
-      n = p.max_items;
+    s_atoms = run_atoms < pa.max_atoms ? run_atoms : pa.max_atoms;
+    s_cost_pre = run_pcost;
+    s_dec_total = run_dec;
+  }
+  __syncthreads();
+  const int n_atoms = (int)s_atoms;
+  const long long cost_pre = s_cost_pre, dec_total = s_dec_total;
+  const long long C = cost_pre + dec_total;
+  // CTAs that get work: every cost range at least kMinUnitsPerCta long, so
+  // no range is empty; the others find an empty item list
+  long long g_eff = C / kMinUnitsPerCta;
+  if (g_eff > pa.grid) g_eff = pa.grid;
+  if (g_eff < 1) g_eff = 1;
+  const int grid = (int)g_eff;
+  // Everything the per-CTA walks below read goes to shared memory when it
+  // fits (in 8-byte words): range starts, per-request decode offsets /
+  // lengths / rows, per-segment cut info, tile starts; else it stays global.
+  long long* los = plan_cache;
+  for (int b = threadIdx.x; b <= grid; b += blockDim.x)
+    los[b] = C > 0 ? cta_lo(b, C, grid) : 0;
+  long long free_ll = kPlanCacheBytes / 8 - (grid + 1);
+  long long* next = los + grid + 1;
+  const int B = pa.num_seqs;
+  const bool req_sm = 2ll * B <= free_ll;  // dec0 + (declen, rows)
+  long long* dec0 = req_sm ? next : pa.req_dec0;
+  int* declen_a = req_sm ? reinterpret_cast<int*>(next + B) : pa.req_declen;
+  int* rows_a = req_sm ? declen_a + B : pa.req_rows;
+  if (req_sm) {
+    for (int r = threadIdx.x; r < B; r += blockDim.x) {
+      dec0[r] = pa.req_dec0[r];
+      declen_a[r] = pa.req_declen[r];
+      rows_a[r] = pa.req_rows[r];
     }
-    *num_items = (int)n;
-    *p.work_counter = 0;
+    next += 2ll * B;
+    free_ll -= 2ll * B;
+  }
+  const long long nseg = (long long)B * H;
+  const bool seg_sm = nseg <= free_ll;
+  int2* seg_cut = seg_sm ? reinterpret_cast<int2*>(next) : pa.seg_cut;
+  if (seg_sm) {
+    next += nseg;
+    free_ll -= nseg;
+  }
+  const bool atoms_sm = n_atoms <= free_ll;
+  long long* astart = atoms_sm ? next : pa.atom_start;
+  if (atoms_sm)
+    for (int i = threadIdx.x; i < n_atoms; i += blockDim.x) astart[i] = pa.atom_start[i];
+  __syncthreads();
+  __syncthreads();
+  // ---- 2: decode segments, one thread each: the CTAs that cut it, its
+  // first partial slot and its place in the list of split segments.  (Every
+  // CTA in a split segment's span owns a non-empty piece of it, so every
+  // partial slot is written before the merge reads it.)
+  int run_slots = 0, run_split = 0;
+  for (long long base = 0; base < nseg; base += blockDim.x) {
+    const long long sg = base + threadIdx.x;
+    int parts = 0, bf = 0;
+    if (sg < nseg) {
+      const int r = (int)(sg / H), g = (int)(sg - (long long)r * H);
+      const int declen = declen_a[r];
+      if (declen > 0) {
+        const long long s0 = cost_pre + dec0[r] + (long long)g * declen;
+        bf = cta_of(s0, los, grid);
+        parts = cta_of(s0 + declen - 1, los, grid) - bf + 1;
+      }
+    }
+    const int nslots = parts > 1 ? parts : 0;
+    const int ex_slot = block_scan_excl<int>(nslots, &tot_i, ws_i);
+    const int t_slot = tot_i;
+    __syncthreads();
+    const int ex_split = block_scan_excl<int>(parts > 1 ? 1 : 0, &tot_i, ws_i);
+    const int t_split = tot_i;
+    __syncthreads();
+    if (sg < nseg) {
+      int first = -1;
+      if (parts > 1) {
+        const int slot = run_slots + ex_slot;
+        if (slot + parts <= pa.max_slots) {
+          first = slot;
+          const int k = run_split + ex_split;
+          pa.split_list[k] = make_int4((int)(sg / H), (int)(sg % H), parts, first);
+        } else {
+          flag_error(pa.err, PA_DEV_ERR_METADATA);
+        }
+      }
+      seg_cut[sg] = make_int2(first, bf);
+    }
+    run_slots += t_slot;
+    run_split += t_split;
+  }
+  if (threadIdx.x == 0) *pa.n_split = run_split;
+  __syncthreads();  // seg_cut complete before the walks read it
+
+  // ---- 3: items of every CTA (count, scan, emit)
+  int run_items = 0;
+  for (int base = 0; base < pa.grid; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    long long lo = 0, hi = 0;
+    int a0 = 0, a1 = 0;
+    if (b < grid && C > 0) {  // CTAs at or past the effective grid: no work
+      lo = los[b];
+      hi = los[b + 1];
+      a0 = lower_bound_ll(astart, n_atoms, lo);
+      a1 = lower_bound_ll(astart, n_atoms, hi);
+    }
+    // decode interval of this CTA, in decode units
+    const long long d0 = min(max(lo, cost_pre) - cost_pre, dec_total);
+    const long long d1 = min(max(hi, cost_pre) - cost_pre, dec_total);
+    int cnt = a1 - a0;
+    for (int pass = 0; pass < 2; ++pass) {
+      int o = 0;
+      if (pass == 1) {
+        const int ex = block_scan_excl<int>(cnt, &tot_i, ws_i);
+        o = run_items + ex;
+        if (b < pa.grid) pa.cta_begin[b] = min(o, pa.max_items);
+        for (int a = a0; a < a1; ++a, ++o) {
+          if (o < pa.max_items) {
+            const int4 at = pa.atoms[a];
+            const ReqMeta m = load_req(pa.qsl, pa.seq_lens, at.x, pa.num_tokens,
+                                       pa.max_query_len, pa.max_seq_len,
+                                       pa.max_blocks_per_seq);
+            const int rows =
+                min(kPrefillTileRows, m.n * G - at.z * kPrefillTileRows);
+            pa.items[2 * o] = make_int4(at.x, at.y, kItemPrefill, at.z);
+            pa.items[2 * o + 1] = make_int4(0, at.w, rows, 0);
+          }
+        }
+      }
+      if (d0 < d1) {
+        // request holding decode unit d0: last r with req_dec0[r] <= d0
+        int lo_r = 0, hi_r = pa.num_seqs - 1;
+        while (lo_r < hi_r) {
+          const int mid = (lo_r + hi_r + 1) >> 1;
+          if (dec0[mid] <= d0) lo_r = mid; else hi_r = mid - 1;
+        }
+        int r = lo_r;
+        long long cur = d0;
+        int n_pieces = 0;
+        while (cur < d1 && r < pa.num_seqs) {
+          const int declen = declen_a[r];
+          if (declen == 0) { ++r; continue; }
+          const long long rs = dec0[r];
+          const int g = (int)((cur - rs) / declen);
+          const long long ss = rs + (long long)g * declen;
+          const long long se = ss + declen;
+          const long long pe = min(se, d1);
+          if (pass == 1 && o < pa.max_items) {
+            const int2 sc = seg_cut[(long long)r * H + g];
+            const int slot = sc.x >= 0 ? sc.x + (b - sc.y) : -1;
+            const int rows = rows_a[r];
+            pa.items[2 * o] = make_int4(r, g, kItemDecode, slot);
+            pa.items[2 * o + 1] = make_int4((int)(cur - ss), (int)(pe - ss), rows, 0);
+          }
+          ++o;
+          ++n_pieces;
+          cur = pe;
+          if (g + 1 == H) ++r;
+        }
+        if (pass == 0) cnt += n_pieces;
+      } else if (pass == 0) {
+        // no decode work for this CTA
+      }
+      if (pass == 1) {
+        const int t = tot_i;
+        __syncthreads();
+        run_items += t;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (run_items > pa.max_items) flag_error(pa.err, PA_DEV_ERR_METADATA);
+    pa.cta_begin[pa.grid] = min(run_items, pa.max_items);
   }
 }
 
@@ -388,22 +630,20 @@ __device__ __forceinline__ void load_q(const FastParams& p, int q0, int g,
   }
 }
 
-// Process one page (16 keys) held in shared memory at k_base / v_base.
+// S^T = Q.K^T for one page: rows are query rows, columns the 16 keys (two
+// 8-key tiles; column n of tile nt is key nt * 8 + perm(n)).  Two
+// accumulators per tile (even / odd k-steps) keep four MMA chains in flight.
 template <int kKind, bool kRows16>
-__device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
-                                             const uint32_t (&qa)[8][4],
-                                             WarpState& st, int key0,
-                                             int valid_keys, bool need_mask,
-                                             int lim0, int lim1,
-                                             float sscale0, float sscale1,
-                                             int lane) {
+__device__ __forceinline__ void qk_page(uint32_t k_base,
+                                        const uint32_t (&qa)[8][4],
+                                        float (&s)[2][4], int lane) {
   using Tr = Traits<kKind>;
   constexpr bool kB = Tr::kMmaBF16;
   constexpr uint32_t P = Tr::kPerm;
   const int r = lane >> 2, c = lane & 3;
   // Q.K^T: two accumulators per 8-key tile (even / odd k-steps) so that four
   // independent MMA chains are in flight
-  float s[2][4], s2[2][4];
+  float s2[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
@@ -414,8 +654,8 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
       for (int j = 0; j < 4; ++j) {
         const int dhi = j >> 1;
         const int u = ((j & 1) << 2) | c;
-        const int phys = u ^ (((t << 1) | dhi) & 7);
-        const uint4 kv = lds128(k_base + t * 256 + dhi * 128 + phys * 16);
+        const uint4 kv = lds128(k_base + t * 256 + dhi * 128 +
+                                ((u ^ (((t << 1) | dhi) & 7)) << 4));
         mma_acc<kB, kRows16>(s[nt], qa[2 * j], kv.x, kv.y);
         mma_acc<kB, kRows16>(s2[nt], qa[2 * j + 1], kv.z, kv.w);
       }
@@ -439,6 +679,23 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
 #pragma unroll
     for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
   }
+}
+
+// Process one page (16 keys) held in shared memory at k_base / v_base.
+template <int kKind, bool kRows16>
+__device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
+                                             const uint32_t (&qa)[8][4],
+                                             WarpState& st, int key0,
+                                             int valid_keys, bool need_mask,
+                                             int lim0, int lim1,
+                                             float sscale0, float sscale1,
+                                             int lane) {
+  using Tr = Traits<kKind>;
+  constexpr bool kB = Tr::kMmaBF16;
+  constexpr uint32_t P = Tr::kPerm;
+  const int r = lane >> 2, c = lane & 3;
+  float s[2][4];
+  qk_page<kKind, kRows16>(k_base, qa, s, lane);
   // scale, mask
   const int tA = perm_of(P, 2 * c), tB = perm_of(P, 2 * c + 1);
 #pragma unroll
@@ -520,8 +777,8 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int t = tk[k];
-        const int phys = r ^ (((t << 1) | h) & 7);
-        v[k] = lds128(v_base + t * 256 + h * 128 + phys * 16);
+        v[k] = lds128(v_base + t * 256 + h * 128 +
+                      ((r ^ (((t << 1) | h) & 7)) << 4));
       }
       if (valid_keys < kBS) {  // last page: slots past the sequence end
 #pragma unroll
@@ -583,6 +840,150 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
   }
 }
 
+// ---------------------------------------------------------------------------
+// decode items with at most 8 query rows: S^T = Q.K^T as above, then
+// O^T = V^T.P^T -- the accumulator fragment of S^T is, element for element,
+// the B operand of P^T, and V^T comes from transposing matrix loads, so P.V
+// needs 8 MMAs per page (M = 16 head-dim rows, N = 8 query rows, K = 16 keys)
+// and no register shuffles.
+// ---------------------------------------------------------------------------
+struct NarrowState {
+  float o[8][4];  // O^T: tile mt holds 16 head-dim rows x query rows 2c, 2c+1
+  float m, l;     // softmax state of query row lane / 4
+};
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&a)[4], uint32_t addr) {
+  asm volatile(
+      "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+      : "r"(addr));
+}
+
+// head-dim index of O^T element e of tile mt for thread (r, c)
+template <int kKind>
+__device__ __forceinline__ int narrow_col(int mt, int e, int r) {
+  if constexpr (Traits<kKind>::kFp8) {
+    return 16 * r + 2 * mt + (e >> 1);
+  } else {
+    return 16 * mt + r + 8 * (e >> 1);
+  }
+}
+
+template <int kKind>
+__device__ __forceinline__ void process_page_narrow(
+    uint32_t k_base, uint32_t v_base, const uint32_t (&qa)[8][4],
+    NarrowState& st, int key0, int valid_keys, bool need_mask, int lim,
+    float sscale, int lane) {
+  using Tr = Traits<kKind>;
+  constexpr bool kB = Tr::kMmaBF16;
+  constexpr uint32_t P = Tr::kPerm;
+  const int r = lane >> 2, c = lane & 3;
+  float s[2][4];
+  qk_page<kKind, false>(k_base, qa, s, lane);
+  const int tA = perm_of(P, 2 * c), tB = perm_of(P, 2 * c + 1);
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = s[nt][e] * sscale;
+      if (need_mask && key0 + nt * 8 + (e ? tB : tA) > lim) v = -INFINITY;
+      s[nt][e] = v;
+    }
+  // online softmax (base 2) of query row r
+  float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
+  const float mnew = fmaxf(st.m, mx);
+  const float muse = mnew == -INFINITY ? 0.f : mnew;
+  const float alpha = exp2f(st.m - muse);
+  st.m = mnew;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) s[nt][e] = exp2f(s[nt][e] - muse);
+  st.l = st.l * alpha + ((s[0][0] + s[0][1]) + (s[1][0] + s[1][1]));
+  // this thread's O^T columns are query rows 2c and 2c + 1
+  const float a_lo = __shfl_sync(~0u, alpha, 8 * c);
+  const float a_hi = __shfl_sync(~0u, alpha, 8 * c + 4);
+  if (__any_sync(~0u, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      st.o[mt][0] *= a_lo;
+      st.o[mt][1] *= a_hi;
+      st.o[mt][2] *= a_lo;
+      st.o[mt][3] *= a_hi;
+    }
+  }
+  // P^T as the B operand: b0 = keys (tA, tB), b1 = keys (8 + tA, 8 + tB) of
+  // query row r; with bf16 operands a bf16 head and tail of P
+  const uint32_t b0 = pack2<kB>(s[0][0], s[0][1]);
+  const uint32_t b1 = pack2<kB>(s[1][0], s[1][1]);
+  uint32_t b0l = 0, b1l = 0;
+  if constexpr (kB) {
+    b0l = pack2<true>(s[0][0] - bf16_lo(b0), s[0][1] - bf16_hi(b0));
+    b1l = pack2<true>(s[1][0] - bf16_lo(b1), s[1][1] - bf16_hi(b1));
+  }
+  // keys past the sequence end (last page only) hold NaN: clear them in V
+  uint32_t m01 = ~0u, m23 = ~0u;
+  if (valid_keys < kBS) {
+    m01 = (tA < valid_keys ? 0x0000FFFFu : 0u) | (tB < valid_keys ? 0xFFFF0000u : 0u);
+    m23 = (8 + tA < valid_keys ? 0x0000FFFFu : 0u) |
+          (8 + tB < valid_keys ? 0xFFFF0000u : 0u);
+  }
+  if constexpr (!Tr::kFp8) {
+    // matrix g (lanes 8g..8g+7) row i: key (g >> 1) * 8 + perm(i), head-dim
+    // chunk 2 * (mt & 3) + (g & 1) of segment mt >> 2
+    const int g8 = lane >> 3, i8 = lane & 7;
+    const int tok = ((g8 >> 1) << 3) + perm_of(P, i8);
+    const uint32_t row = v_base + tok * 256;
+    const int tx = (tok << 1) & 7, gb = g8 & 1;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t a[4];
+      const int ch = 2 * (mt & 3) + gb;
+      const int dhi = mt >> 2;
+      ldsm_x4_trans(a, row + dhi * 128 + ((ch ^ (tx | dhi)) << 4));
+      a[0] &= m01;
+      a[1] &= m01;
+      a[2] &= m23;
+      a[3] &= m23;
+      mma16816<kB>(st.o[mt], a, b0, b1);
+      if constexpr (kB) mma16816<true>(st.o[mt], a, b0l, b1l);
+    }
+  } else {
+    // thread (r, c) reads head-dim bytes 16r .. 16r+15 of keys tA, tB, 8+tA,
+    // 8+tB; tile mt row r is head-dim 16r + 2mt, row r + 8 is 16r + 2mt + 1
+    const int tk[4] = {tA, tB, 8 + tA, 8 + tB};
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = tk[k];
+      v[k] = lds128(v_base + t * 128 + ((r ^ (t & 7)) << 4));
+    }
+    if (valid_keys < kBS) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (tk[k] >= valid_keys) v[k] = make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t va[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+    const uint32_t vb[4] = {v[1].x, v[1].y, v[1].z, v[1].w};
+    const uint32_t vc[4] = {v[2].x, v[2].y, v[2].z, v[2].w};
+    const uint32_t vd[4] = {v[3].x, v[3].y, v[3].z, v[3].w};
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+      const uint32_t ab = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);
+      const uint32_t cd = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2(ab);
+      a[1] = e4m3x2_to_f16x2(ab >> 16);
+      a[2] = e4m3x2_to_f16x2(cd);
+      a[3] = e4m3x2_to_f16x2(cd >> 16);
+      mma16816<false>(st.o[mt], a, b0, b1);
+    }
+  }
+}
+
 template <typename TOut>
 __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
   static_cast<TOut*>(out)[idx] = from_f32<TOut>(v);
@@ -592,22 +993,21 @@ template <int kKind>
 using OutT = typename std::conditional<Traits<kKind>::kQBF16, __nv_bfloat16,
                                        __half>::type;
 
-constexpr int kItemQueue = 4;  // work items the producer may run ahead
-
 // Shared-memory carve-up of one CTA (offsets from a 1024-aligned base).
 template <int kKind, bool kWide>
 struct Layout {
   using Tr = Traits<kKind>;
   static constexpr int kE = kWide ? 4 : 2;  // accumulator rows kept per lane
+  // (the narrow state, 8 tiles x 4 per lane, has the size of 16 x 2)
   static constexpr int kRing = 0;
   static constexpr int kScratch = Tr::kRingBytes;                 // partial O
   static constexpr int kScratchBytes = kConsumerWarps * 16 * kE * 32 * 4;
   static constexpr int kML = kScratch + kScratchBytes;            // m, l
   static constexpr int kMLBytes = kConsumerWarps * 16 * 2 * 4;
   static constexpr int kBars = kML + kMLBytes;                    // 8 B each
-  static constexpr int kNumBars = 2 * Tr::kStages + 2 * kItemQueue;
-  static constexpr int kItems = kBars + 8 * kNumBars;             // int4 each
-  static constexpr int kAbort = kItems + 16 * kItemQueue;
+  static constexpr int kNumBars = 2 * Tr::kStages;
+  static constexpr int kIds = kBars + 8 * kNumBars;               // int [2][32]
+  static constexpr int kAbort = kIds + 2 * 32 * 4;
   static constexpr int kBytes = kAbort + 16;
   static constexpr int kSmemBytes = 1024 + kBytes;  // + alignment slack
 };
@@ -618,12 +1018,8 @@ struct Smem {
   int stages;
   __device__ uint32_t full(int s) const { return bars + 8 * s; }
   __device__ uint32_t empty(int s) const { return bars + 8 * (stages + s); }
-  __device__ uint32_t item_full(int q) const { return bars + 8 * (2 * stages + q); }
-  __device__ uint32_t item_empty(int q) const {
-    return bars + 8 * (2 * stages + kItemQueue + q);
-  }
   uint32_t bars;
-  int4* items;
+  int* ids;
   volatile int* abort_flag;
   float* scratch;
   float* ml;
@@ -660,27 +1056,24 @@ struct ItemGeom {
   int page0, npages, row0, rows;
 };
 
-__device__ __forceinline__ ItemGeom item_geom(const FastParams& p, int kind,
-                                              int x, const ReqMeta& rm) {
+// rec0 = {request, KV head, kind, tile (prefill) or partial slot (decode,
+// -1: write the output)}, rec1 = {first page, end page, query rows}
+__device__ __forceinline__ ItemGeom item_geom(const FastParams& p,
+                                              const int4& rec0,
+                                              const int4& rec1,
+                                              const ReqMeta& rm) {
   ItemGeom ig;
-  if (kind == kItemDecode) {
-    ig.page0 = x * p.blocks_per_split;
-    ig.npages = min(p.blocks_per_split, rm.nb - ig.page0);
-    ig.row0 = 0;
-    ig.rows = rm.n * p.group;
-  } else {
-    ig.row0 = x * kPrefillTileRows;
-    ig.rows = min(kPrefillTileRows, rm.n * p.group - ig.row0);
-    const int lim_last = rm.L - rm.n + (ig.row0 + ig.rows - 1) / p.group;
-    ig.page0 = 0;
-    ig.npages = lim_last / kBS + 1;
-  }
+  ig.page0 = rec1.x;
+  ig.npages = rec1.y - rec1.x;
+  (void)rm;
+  ig.rows = rec1.z;
+  ig.row0 = rec0.z == kItemDecode ? 0 : rec0.w * kPrefillTileRows;
   return ig;
 }
 
 // One consumer warp's share of one work item.  Pages are numbered by the
-// CTA-wide counter c0 + j; in a decode item page c goes to warp c % 4 (the
-// same warp for a given ring slot, since the ring depth is a multiple of 4),
+// CTA-wide counter c0 + j; in a decode item page c goes to warp c % W (the
+// same warp for a given ring slot, since the ring depth is a multiple of W),
 // in a prefill tile every warp reads every page for its own 16 rows.
 template <int kKind, bool kRows16, bool kWide>
 __device__ void consume_item(const FastParams& p, const Smem& sm,
@@ -723,7 +1116,10 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.f;
 
-  const int first = decode ? (int)((warp - (int)(c0 & 3u)) & 3) : 0;
+  const int first =
+      decode ? (int)((warp - (int)(c0 % kConsumerWarps) + kConsumerWarps) %
+                     kConsumerWarps)
+             : 0;
   const int stride = decode ? kConsumerWarps : 1;
   bool alive = *sm.abort_flag == 0;
   for (int j = first; j < ig.npages && alive; j += stride) {
@@ -792,10 +1188,10 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
     }
   }
   consumers_sync();
-  const int nsplit = __ldg(p.req_nsplit + r);
+  const int slot = x;  // partial slot, -1: this item covers the whole segment
 #pragma unroll
-  for (int Tq = 0; Tq < 4; ++Tq) {
-    const int T = warp * 4 + Tq;
+  for (int Tq = 0; Tq < 16 / kConsumerWarps; ++Tq) {
+    const int T = warp * (16 / kConsumerWarps) + Tq;
 #pragma unroll
     for (int e = 0; e < kE; ++e) {
       const int rr = rq + (e >> 1) * 8;
@@ -817,14 +1213,125 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
       const int h = g * G + (rr - i * G);
       const int64_t row = (int64_t)(rm.q0 + i) * Hq + h;
       const int col = out_col<kKind>(T, e, c);
-      if (nsplit <= 1) {
+      if (slot < 0) {
         store_out<OutT<kKind>>(p.out, row * 128 + col, num / den * p.out_scale);
       } else {
-        const int64_t slotp = row * p.max_splits + x;
-        p.ws_acc[slotp * 128 + col] = num;
+        const int64_t pr = (int64_t)slot * 16 + rr;
+        p.ws_acc[pr * 128 + col] = num;
         if (T == 0 && (e & 1) == 0 && c == 0) {
-          p.ws_ml[slotp * 2 + 0] = M;
-          p.ws_ml[slotp * 2 + 1] = den;
+          p.ws_ml[pr * 2 + 0] = M;
+          p.ws_ml[pr * 2 + 1] = den;
+        }
+      }
+    }
+  }
+}
+
+// One consumer warp's share of a decode item with at most 8 query rows
+// (pages c0 + j with (c0 + j) % W == warp), merged across the W warps in
+// shared memory at the end.
+template <int kKind, bool kWide>
+__device__ void consume_item_narrow(const FastParams& p, const Smem& sm,
+                                    const ReqMeta& rm, int r, int g, int x,
+                                    const ItemGeom& ig, uint32_t c0, int warp,
+                                    int lane) {
+  using Tr = Traits<kKind>;
+  using Ly = Layout<kKind, kWide>;
+  constexpr int S = Tr::kStages;
+  const int rq = lane >> 2, c = lane & 3;
+  const int G = p.group;
+  const int rows = ig.rows;
+  uint32_t qa[8][4];
+  float rscale[2];
+  load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
+  const int lim = rq < rows ? rm.L - rm.n + rq / G : rm.L - 1;
+  int min_lim = rq < rows ? lim : INT_MAX;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1)
+    min_lim = min(min_lim, __shfl_xor_sync(~0u, min_lim, d));
+  min_lim = min(min_lim, rm.L - 1);
+  const float ss = p.score_scale * rscale[0];
+
+  NarrowState st;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+    st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
+  st.m = -INFINITY;
+  st.l = 0.f;
+
+  const int first = (int)((warp - (int)(c0 % kConsumerWarps) + kConsumerWarps) %
+                          kConsumerWarps);
+  bool alive = *sm.abort_flag == 0;
+  for (int j = first; j < ig.npages && alive; j += kConsumerWarps) {
+    const uint32_t cc = c0 + j;
+    const int slot = cc % S;
+    if (!__all_sync(~0u, mbar_wait_bounded(sm.full(slot), (cc / S) & 1))) {
+      if (lane == 0) {
+        flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+        *sm.abort_flag = 1;
+      }
+      alive = false;
+      break;
+    }
+    const int key0 = (ig.page0 + j) * kBS;
+    const int valid = min(kBS, rm.L - key0);
+    const bool need_mask = key0 + kBS - 1 > min_lim;
+    const uint32_t kb = sm.base + Ly::kRing + slot * Tr::kStageBytes;
+    process_page_narrow<kKind>(kb, kb + Tr::kPageBytes, qa, st, key0, valid,
+                               need_mask, lim, ss, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cnt(sm.empty(slot), kConsumerWarps);
+  }
+  st.l += __shfl_xor_sync(~0u, st.l, 1);
+  st.l += __shfl_xor_sync(~0u, st.l, 2);
+
+  // merge the four warps' states (scratch free since the item-start barrier)
+  float* of = sm.scratch;  // [warp][mt][e][lane]
+  float* ml = sm.ml;       // [warp][16 rows][m, l]
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      of[((warp * 8 + mt) * 4 + e) * 32 + lane] = st.o[mt][e];
+  if (c == 0) {
+    ml[(warp * 16 + rq) * 2 + 0] = st.m;
+    ml[(warp * 16 + rq) * 2 + 1] = st.l;
+  }
+  consumers_sync();
+  const int slot = x;  // partial slot, -1: this item covers the whole segment
+  const int Hq = p.num_q_heads;
+#pragma unroll
+  for (int k = 0; k < 8 / kConsumerWarps; ++k) {
+    const int mt = warp * (8 / kConsumerWarps) + k;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int qrow = 2 * c + (e & 1);
+      if (qrow >= rows) continue;
+      float mw[kConsumerWarps], M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        mw[w] = ml[(w * 16 + qrow) * 2];
+        M = fmaxf(M, mw[w]);
+      }
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float a = mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M);
+        num += a * of[((w * 8 + mt) * 4 + e) * 32 + lane];
+        den += a * ml[(w * 16 + qrow) * 2 + 1];
+      }
+      const int i = qrow / G;
+      const int h = g * G + (qrow - i * G);
+      const int64_t orow = (int64_t)(rm.q0 + i) * Hq + h;
+      const int col = narrow_col<kKind>(mt, e, rq);
+      if (slot < 0) {
+        store_out<OutT<kKind>>(p.out, orow * 128 + col, num / den * p.out_scale);
+      } else {
+        const int64_t pr = (int64_t)slot * 16 + qrow;
+        p.ws_acc[pr * 128 + col] = num;
+        if (mt == 0 && (e >> 1) == 0 && rq == 0) {
+          p.ws_ml[pr * 2 + 0] = M;
+          p.ws_ml[pr * 2 + 1] = den;
         }
       }
     }
@@ -840,7 +1347,7 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
 // small shared-memory queue and streams their pages into the ring; warps 0-3
 // consume.  The ring keeps streaming across item boundaries.
 template <int kKind, bool kWide>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, PA_CTAS_PER_SM)
 attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v,
                  const __grid_constant__ FastParams p) {
@@ -854,7 +1361,7 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
   sm.ptr = smem_raw + (sm.base - raw);
   sm.stages = S;
   sm.bars = sm.base + Ly::kBars;
-  sm.items = reinterpret_cast<int4*>(sm.ptr + Ly::kItems);
+  sm.ids = reinterpret_cast<int*>(sm.ptr + Ly::kIds);
   sm.abort_flag = reinterpret_cast<volatile int*>(sm.ptr + Ly::kAbort);
   sm.scratch = reinterpret_cast<float*>(sm.ptr + Ly::kScratch);
   sm.ml = reinterpret_cast<float*>(sm.ptr + Ly::kML);
@@ -865,15 +1372,14 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
       mbar_init(sm.full(i), 1);
       mbar_init(sm.empty(i), kConsumerWarps);
     }
-    for (int q = 0; q < kItemQueue; ++q) {
-      mbar_init(sm.item_full(q), 1);
-      mbar_init(sm.item_empty(q), kConsumerWarps);
-    }
     *sm.abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
-  const int num_items = __ldg(p.num_items);
+  pdl_launch_dependents();  // the merge may be scheduled behind this grid
+  pdl_wait();               // the planner (and everything before it) is done
+  const int it_begin = __ldg(p.cta_begin + blockIdx.x);
+  const int it_end = __ldg(p.cta_begin + blockIdx.x + 1);
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -882,157 +1388,102 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
       tma_prefetch_desc(&tmap_v);
     }
     uint32_t c = 0;     // pages issued
-    for (int k = 0;; ++k) {
-      const int q = k % kItemQueue;
-      int4 it = make_int4(-1, 0, 0, 0);
-      if (lane == 0) {
-        bool ok = k < kItemQueue ||
-                  mbar_wait_bounded(sm.item_empty(q), ((k / kItemQueue) - 1) & 1);
-        if (!ok) {
-          flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-          *sm.abort_flag = 1;
-        }
-        if (ok && *sm.abort_flag == 0) {
-          const int idx = atomicAdd(p.work_counter, 1);
-          if (idx < num_items) it = __ldg(p.items + idx);
-        }
-        if (ok) {
-          sm.items[q] = it;
-          mbar_arrive(sm.item_full(q));
-        }
-      }
-      it.x = __shfl_sync(~0u, it.x, 0);
-      it.y = __shfl_sync(~0u, it.y, 0);
-      it.z = __shfl_sync(~0u, it.z, 0);
-      it.w = __shfl_sync(~0u, it.w, 0);
-      if (it.x < 0) break;
-      const ReqMeta rm = load_req(p.qsl, p.seq_lens, it.x, p.num_tokens,
-                                  p.max_query_len, p.max_seq_len,
-                                  p.max_blocks_per_seq);
-      const ItemGeom ig = item_geom(p, it.z, it.w, rm);
-      if (!kWide && (it.z == kItemPrefill || ig.rows > 8)) continue;
+    int go = 1;
+    for (int k = it_begin; k < it_end && go; ++k) {
+      const int4 rec0 = __ldg(p.items + 2 * k);
+      const int4 rec1 = __ldg(p.items + 2 * k + 1);
+      // the narrow kernel never gets prefill tiles or items over 8 rows (the
+      // host guarantees it); both sides skip them the same way
+      if (!kWide && (rec0.z == kItemPrefill || rec1.z > 8)) continue;
       const int32_t* bt =
-          p.block_tables + (int64_t)it.x * p.max_blocks_per_seq + ig.page0;
-      // block ids of this item, 32 per register, loaded two chunks ahead
-      const int n = ig.npages;
-      int ids0 = lane < n ? __ldg(bt + lane) : 0;
-      int ids1 = 32 + lane < n ? __ldg(bt + 32 + lane) : 0;
-      int ids2 = 64 + lane < n ? __ldg(bt + 64 + lane) : 0;
-      constexpr int PF = PA_L2_PREFETCH_PAGES;
-      static_assert(PF >= 0 && PF <= 32, "prefetch window must fit one id chunk");
-      auto page_row = [&](int blk) {
-        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-          flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
-          blk = 0;
-        }
-        return (blk * p.num_kv_heads + it.y) * kBS;
-      };
-      auto prefetch = [&](int row) {
-        if constexpr (Tr::kFp8) {
-          tma_prefetch_2d(&tmap_k, 0, row);
-          tma_prefetch_2d(&tmap_v, 0, row);
-        } else {
-          tma_prefetch_3d(&tmap_k, 0, 0, row);
-          tma_prefetch_3d(&tmap_v, 0, 0, row);
-        }
-      };
-      // the first window goes to L2 at once
-      if (PF > 0 && lane < min(PF, n)) prefetch(page_row(ids0));
-      int go = 1;
-      for (int j = 0; j < n && go; ++j, ++c) {
-        if (j > 0 && (j & 31) == 0) {
-          ids0 = ids1;
-          ids1 = ids2;
-          const int idx = j + 64 + lane;
-          ids2 = idx < n ? __ldg(bt + idx) : 0;
-        }
-        int blk = __shfl_sync(~0u, ids0, j & 31);
-        const int jp = j + PF;
-        const int blk_pf = __shfl_sync(~0u, (jp >> 5) == (j >> 5) ? ids0 : ids1,
-                                       jp & 31);
-        if (lane == 0) {
-          if (PF > 0 && jp < n) prefetch(page_row(blk_pf));
-          const int slot = c % S;
-          if (c >= (uint32_t)S &&
-              !mbar_wait_bounded(sm.empty(slot), ((c / S) - 1) & 1)) {
-            flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-            *sm.abort_flag = 1;
-          }
-          if (*sm.abort_flag) {
-            go = 0;
-          } else {
-            const int row = page_row(blk);
-            const uint32_t dst = sm.base + Ly::kRing + slot * Tr::kStageBytes;
-            mbar_arrive_expect_tx(sm.full(slot), Tr::kStageBytes);
-            if constexpr (Tr::kFp8) {
-              tma_load_2d(dst, &tmap_k, sm.full(slot), 0, row);
-              tma_load_2d(dst + Tr::kPageBytes, &tmap_v, sm.full(slot), 0, row);
-            } else {
-              tma_load_3d(dst, &tmap_k, sm.full(slot), 0, 0, row);
-              tma_load_3d(dst + Tr::kPageBytes, &tmap_v, sm.full(slot), 0, 0, row);
+          p.block_tables + (int64_t)rec0.x * p.max_blocks_per_seq + rec1.x;
+      // Block ids go through shared memory 32 at a time (the next chunk is
+      // loaded while the current one is issued).  Lanes 0 and 1 issue each
+      // page together: lane 0 its K page and the expected byte count, lane
+      // 1 its V page.
+      const int n = rec1.y - rec1.x;
+      sm.ids[lane] = lane < n ? __ldg(bt + lane) : 0;
+      __syncwarp();
+      for (int j0 = 0; j0 < n && go; j0 += 32) {
+        const int buf = (j0 >> 5) & 1;
+        const int nidx = j0 + 32 + lane;
+        const int nreg = nidx < n ? __ldg(bt + nidx) : 0;
+        if (lane < 2) {
+          const int* cur = sm.ids + buf * 32;
+          const int cnt = min(32, n - j0);
+          const CUtensorMap* map = lane ? &tmap_v : &tmap_k;
+          for (int jj = 0; jj < cnt; ++jj) {
+            const int slot = c % S;
+            const bool ok = c < (uint32_t)S ||
+                            mbar_wait_bounded(sm.empty(slot), ((c / S) - 1) & 1);
+            if (__any_sync(0x3u, !ok)) {
+              if (lane == 0) {
+                flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+                *sm.abort_flag = 1;
+              }
+              go = 0;
+              break;
             }
+            int blk = cur[jj];
+            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+              if (lane == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+              blk = 0;
+            }
+            const int row = (blk * p.num_kv_heads + rec0.y) * kBS;
+            const uint32_t dst =
+                sm.base + Ly::kRing + slot * Tr::kStageBytes + lane * Tr::kPageBytes;
+            if (lane == 0) mbar_arrive_expect_tx(sm.full(slot), Tr::kStageBytes);
+            __syncwarp(0x3u);
+            if constexpr (Tr::kFp8)
+              tma_load_2d(dst, map, sm.full(slot), 0, row);
+            else
+              tma_load_3d(dst, map, sm.full(slot), 0, 0, row);
+            ++c;
           }
         }
+        __syncwarp();
         go = __shfl_sync(~0u, go, 0);
+        c = __shfl_sync(~0u, c, 0);
+        sm.ids[(buf ^ 1) * 32 + lane] = nreg;
+        __syncwarp();
       }
-      if (!go) {
-        // stop claiming; hand the consumers an end marker if a queue slot
-        // frees up, then let the copies already in flight land
-        if (lane == 0) {
-          const int q2 = (k + 1) % kItemQueue;
-          if (k + 1 < kItemQueue ||
-              mbar_wait_bounded(sm.item_empty(q2), (((k + 1) / kItemQueue) - 1) & 1)) {
-            sm.items[q2] = make_int4(-1, 0, 0, 0);
-            mbar_arrive(sm.item_full(q2));
-          }
-          const uint32_t from = c > (uint32_t)S ? c - S : 0;
-          for (uint32_t i = from; i < c; ++i)
-            mbar_wait_bounded(sm.full(i % S), (i / S) & 1);
-        }
-        break;
-      }
+    }
+    // after an abort, let the copies already in flight land before exiting
+    if (!go && lane == 0) {
+      const uint32_t from = c > (uint32_t)S ? c - S : 0;
+      for (uint32_t i = from; i < c; ++i)
+        mbar_wait_bounded(sm.full(i % S), (i / S) & 1);
     }
     return;
   }
 
   // ------------------------------ consumers -------------------------------
   uint32_t c = 0;  // pages consumed (CTA-wide numbering, as issued)
-  for (int k = 0;; ++k) {
-    const int q = k % kItemQueue;
-    const bool got =
-        __all_sync(~0u, mbar_wait_bounded(sm.item_full(q), (k / kItemQueue) & 1));
-    int4 it = make_int4(-1, 0, 0, 0);
-    if (got) {
-      it = sm.items[q];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sm.item_empty(q));
-    } else if (lane == 0) {
-      flag_error(p.err, PA_DEV_ERR_TIMEOUT);
-      *sm.abort_flag = 1;
-    }
+  for (int k = it_begin; k < it_end; ++k) {
+    const int4 rec0 = __ldg(p.items + 2 * k);
+    const int4 rec1 = __ldg(p.items + 2 * k + 1);
     // every consumer warp meets here once per item: decisions below are
     // uniform, the previous item's shared scratch is no longer read, and all
     // earlier pages have been consumed by their owners
-    if (consumers_sync_any(it.x < 0 || *sm.abort_flag != 0)) break;
-    const ReqMeta rm = load_req(p.qsl, p.seq_lens, it.x, p.num_tokens,
+    if (consumers_sync_any(*sm.abort_flag != 0)) break;
+    const ReqMeta rm = load_req(p.qsl, p.seq_lens, rec0.x, p.num_tokens,
                                 p.max_query_len, p.max_seq_len,
                                 p.max_blocks_per_seq);
-    const ItemGeom ig = item_geom(p, it.z, it.w, rm);
-    if constexpr (kWide) {
-      if (it.z == kItemPrefill || ig.rows > 8)
-        consume_item<kKind, true, true>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
+    const ItemGeom ig = item_geom(p, rec0, rec1, rm);
+    if (!kWide && (rec0.z == kItemPrefill || rec1.z > 8)) {
+      if (threadIdx.x == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
+      continue;
+    }
+    if (rec0.z == kItemDecode && ig.rows <= 8) {
+      consume_item_narrow<kKind, kWide>(p, sm, rm, rec0.x, rec0.y, rec0.w, ig,
                                         c, warp, lane);
-      else
-        consume_item<kKind, false, true>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
-                                         c, warp, lane);
+    } else if constexpr (kWide) {
+      consume_item<kKind, true, true>(p, sm, rm, rec0.x, rec0.y, rec0.z,
+                                      rec0.w, ig, c, warp, lane);
     } else {
-      if (it.z == kItemPrefill || ig.rows > 8) {
-        // the host never sends such an item to the narrow kernel
-        if (threadIdx.x == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
-        continue;
-      }
-      consume_item<kKind, false, false>(p, sm, rm, it.x, it.y, it.z, it.w, ig,
-                                        c, warp, lane);
+      // the host never sends such an item to the narrow kernel
+      if (threadIdx.x == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
+      continue;
     }
     c += ig.npages;
   }
@@ -1041,48 +1492,47 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // ---------------------------------------------------------------------------
 // split-K merge: one warp per (token, q head) row of a split decode request
 // ---------------------------------------------------------------------------
+// split-K merge: CTA k finishes split segment k (request r, KV head g): one
+// warp per query row, parts combined in slot order (deterministic)
 template <typename TOut>
 __global__ void __launch_bounds__(128)
 merge_kernel(FastParams p) {
-  const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  pdl_wait();  // the attention grid has finished writing the parts
+  if ((int)blockIdx.x >= min(*p.n_split, p.max_slots)) return;
+  const int4 sg = p.split_list[blockIdx.x];
+  const int r = sg.x, g = sg.y, parts = sg.z, first = sg.w;
   const int lane = threadIdx.x & 31;
-  if (row >= p.num_tokens * p.num_q_heads) return;
-  const int64_t t = row / p.num_q_heads;
-  // request owning token t: last r with qsl[r] <= t
-  int lo = 0, hi = p.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.qsl + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  const int r = lo;
   const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
                               p.max_seq_len, p.max_blocks_per_seq);
-  if (!rm.ok || t < rm.q0 || t >= rm.q0 + rm.n) return;
-  if (rm.n * p.group > kDecodeMaxRows) return;
-  const int ns = __ldg(p.req_nsplit + r);
-  if (ns <= 1) return;
-  const float* ml = p.ws_ml + row * p.max_splits * 2;
-  float M = -INFINITY;
-  for (int s = lane; s < ns; s += 32) M = fmaxf(M, ml[2 * s]);
+  const int rows = rm.n * p.group;
+  for (int rr = threadIdx.x >> 5; rr < rows; rr += blockDim.x >> 5) {
+    const int i = rr / p.group;
+    const int h = g * p.group + (rr - i * p.group);
+    const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
+    float M = -INFINITY;
+    for (int s = lane; s < parts; s += 32)
+      M = fmaxf(M, p.ws_ml[((int64_t)(first + s) * 16 + rr) * 2]);
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float den = 0.f;
-  const float* a = p.ws_acc + row * p.max_splits * 128;
-  for (int s = 0; s < ns; ++s) {
-    const float ms = ml[2 * s];
-    const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
-    den += w * ml[2 * s + 1];
-    const float4 v = *reinterpret_cast<const float4*>(a + s * 128 + 4 * lane);
-    acc[0] += w * v.x;
-    acc[1] += w * v.y;
-    acc[2] += w * v.z;
-    acc[3] += w * v.w;
+    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    for (int s = 0; s < parts; ++s) {
+      const int64_t pr = (int64_t)(first + s) * 16 + rr;
+      const float ms = p.ws_ml[pr * 2];
+      if (ms == -INFINITY) continue;  // a part with no keys
+      const float w = exp2f(ms - M);
+      den += w * p.ws_ml[pr * 2 + 1];
+      const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + pr * 128 + 4 * lane);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    }
+    const float inv = p.out_scale / den;
+    TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
   }
-  const float inv = p.out_scale / den;
-  TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
 }
 
 template <int kKind, bool kWide>
@@ -1118,38 +1568,50 @@ cudaError_t prepare_kernel(int* grid) {
 }
 
 template <int kKind>
-cudaError_t launch_kind(const FastParams& fp, const AttnPlan& plan,
+cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
                         const CUtensorMap& tk, const CUtensorMap& tv,
-                        int4* items, int* count, int* nsplit,
                         cudaStream_t stream) {
-  using Tr = Traits<kKind>;
-  (void)Tr::kStages;
   // the narrow kernel covers steps whose every item has <= 8 rows
   const bool wide = (int64_t)fp.max_query_len * fp.group > 8;
   int grid = 0;
   cudaError_t e = wide ? prepare_kernel<kKind, true>(&grid)
                        : prepare_kernel<kKind, false>(&grid);
   if (e != cudaSuccess) return e;
-  if ((int64_t)grid > plan.max_items) grid = (int)plan.max_items;
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(fp, items, count, nsplit);
+  if (grid > plan.grid_max) grid = plan.grid_max;
+  pa.grid = grid;
+  plan_kernel<<<1, kPlanThreads, kPlanCacheBytes, stream>>>(pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // The attention kernel and the merge are launched as programmatic
+  // dependents: each may start while its predecessor runs and waits (on the
+  // device) for it to finish before touching its results.  With the
+  // profiling hook on, plain launches keep the events around the kernel.
   const ProfileEvents& pe = profile_events();
+  const bool pdl = pe.start == nullptr;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (pe.start) cudaEventRecord(pe.start, stream);
-  if (wide)
-    attn_fast_kernel<kKind, true>
-        <<<grid, kThreads, Layout<kKind, true>::kSmemBytes, stream>>>(tk, tv, fp);
-  else
-    attn_fast_kernel<kKind, false>
-        <<<grid, kThreads, Layout<kKind, false>::kSmemBytes, stream>>>(tk, tv, fp);
-  e = cudaGetLastError();
+  if (wide) {
+    cfg.dynamicSmemBytes = Layout<kKind, true>::kSmemBytes;
+    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, true>, tk, tv, fp);
+  } else {
+    cfg.dynamicSmemBytes = Layout<kKind, false>::kSmemBytes;
+    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, false>, tk, tv, fp);
+  }
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
-  if (plan.max_splits > 1) {
-    const int64_t rows = fp.num_tokens * fp.num_q_heads;
-    const unsigned mgrid = (unsigned)((rows + 3) / 4);
-    merge_kernel<OutT<kKind>><<<mgrid, 128, 0, stream>>>(fp);
-    e = cudaGetLastError();
+  if (plan.has_decode) {
+    // split segments: at most one fewer than the CTAs that got work
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<OutT<kKind>>, fp);
   }
   return e;
 }
@@ -1171,49 +1633,33 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                    int max_seq_len, int num_sms) {
   AttnPlan pl{};
   pl.group = num_q_heads / num_kv_heads;
-  const int64_t mb = ((int64_t)max_seq_len + kBS - 1) / kBS;
-  // Split size: aim for several waves of CTAs (two resident per SM) so that
-  // the tail of the step is short, but keep every split long enough to hide
-  // its pipeline start-up and bound the number of partial results.
-  const int64_t target = (int64_t)num_sms * PA_SPLIT_WAVES;
-  const int64_t units = (int64_t)num_seqs * num_kv_heads;
-  int64_t bps = mb;
-  if (units > 0) {
-    const int64_t want_splits = (target + units - 1) / units;
-    bps = (mb + want_splits - 1) / want_splits;
-  }
-  if (bps < PA_SPLIT_MIN_BLOCKS) bps = PA_SPLIT_MIN_BLOCKS;
-  if (bps > mb) bps = mb;
-  if (bps < 1) bps = 1;
-  int64_t ms = (mb + bps - 1) / bps;
-  if (ms > 64) {  // bound the partial-result storage
-    bps = (mb + 63) / 64;
-    ms = (mb + bps - 1) / bps;
-  }
-  pl.blocks_per_split = (int)bps;
-  pl.max_splits = (int)(ms < 1 ? 1 : ms);
   pl.has_prefill = (int64_t)max_query_len * pl.group > kDecodeMaxRows;
-  int64_t items = 0;
-  if (pl.group <= kDecodeMaxRows)
-    items += (int64_t)num_seqs * num_kv_heads * pl.max_splits;
-  if (pl.has_prefill)
-    items += (int64_t)num_kv_heads *
-             ((num_tokens * pl.group + kPrefillTileRows - 1) / kPrefillTileRows +
-              num_seqs);
-  pl.max_items = items;
+  pl.has_decode = pl.group <= kDecodeMaxRows;
+  pl.grid_max = num_sms * kMaxCtasPerSm;
+  pl.max_atoms =
+      pl.has_prefill
+          ? (int64_t)num_kv_heads *
+                ((num_tokens * pl.group + kPrefillTileRows - 1) / kPrefillTileRows +
+                 num_seqs)
+          : 0;
+  pl.max_items = pl.max_atoms + (pl.has_decode ? (int64_t)num_seqs * num_kv_heads : 0) +
+                 pl.grid_max;
+  pl.max_slots = 2 * (int64_t)pl.grid_max;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   size_t off = 0;
-  pl.off_items = off;
-  off = up(off + (size_t)items * 16);
-  pl.off_count = off;
-  off = up(off + 16);
-  pl.off_nsplit = off;
-  off = up(off + (size_t)num_seqs * 4);
+  pl.off_atoms = off;       off = up(off + (size_t)pl.max_atoms * 16);
+  pl.off_atom_start = off;  off = up(off + (size_t)pl.max_atoms * 8);
+  pl.off_req_dec0 = off;    off = up(off + (size_t)num_seqs * 8);
+  pl.off_req_declen = off;  off = up(off + (size_t)num_seqs * 4);
+  pl.off_req_rows = off;    off = up(off + (size_t)num_seqs * 4);
+  pl.off_items = off;       off = up(off + (size_t)pl.max_items * 32);
+  pl.off_cta_begin = off;   off = up(off + (size_t)(pl.grid_max + 1) * 4);
+  pl.off_seg_info = off;    off = up(off + (size_t)num_seqs * num_kv_heads * 8);
+  pl.off_split = off;       off = up(off + (size_t)pl.max_slots * 16 + 16);
   pl.off_acc = off;
-  const size_t rows = (size_t)num_tokens * num_q_heads;
-  if (pl.max_splits > 1) off = up(off + rows * pl.max_splits * head_dim * 4);
+  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * 16 * head_dim * 4);
   pl.off_ml = off;
-  if (pl.max_splits > 1) off = up(off + rows * pl.max_splits * 2 * 4);
+  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * 16 * 2 * 4);
   pl.total_bytes = off;
   return pl;
 }
@@ -1222,7 +1668,6 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
                                   const CUtensorMap& tmap_k,
                                   const CUtensorMap& tmap_v,
                                   cudaStream_t stream) {
-  if (plan.max_items == 0) return cudaSuccess;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   FastParams fp{};
   fp.q = a.q;
@@ -1231,9 +1676,10 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.seq_lens = a.seq_lens;
   fp.qsl = a.query_start_loc;
   fp.items = reinterpret_cast<const int4*>(ws + plan.off_items);
-  fp.num_items = reinterpret_cast<const int*>(ws + plan.off_count);
-  fp.work_counter = reinterpret_cast<int*>(ws + plan.off_count + 4);
-  fp.req_nsplit = reinterpret_cast<const int*>(ws + plan.off_nsplit);
+  fp.cta_begin = reinterpret_cast<const int*>(ws + plan.off_cta_begin);
+  fp.split_list = reinterpret_cast<const int4*>(ws + plan.off_split + 16);
+  fp.n_split = reinterpret_cast<const int*>(ws + plan.off_split);
+  fp.max_slots = (int)plan.max_slots;
   fp.ws_acc = reinterpret_cast<float*>(ws + plan.off_acc);
   fp.ws_ml = reinterpret_cast<float*>(ws + plan.off_ml);
   fp.err = a.err;
@@ -1246,22 +1692,43 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.group = plan.group;
   fp.max_query_len = a.max_query_len;
   fp.max_seq_len = a.max_seq_len;
-  fp.blocks_per_split = plan.blocks_per_split;
-  fp.max_splits = plan.max_splits;
-  fp.max_items = plan.max_items;
   const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
   fp.score_scale = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.0f);
   fp.out_scale = fp8 ? a.v_scale : 1.0f;
-  int4* items = reinterpret_cast<int4*>(ws + plan.off_items);
-  int* count = reinterpret_cast<int*>(ws + plan.off_count);
-  int* nsplit = reinterpret_cast<int*>(ws + plan.off_nsplit);
+
+  PlanArgs pa{};
+  pa.qsl = a.query_start_loc;
+  pa.seq_lens = a.seq_lens;
+  pa.err = a.err;
+  pa.num_tokens = a.num_tokens;
+  pa.num_seqs = a.num_seqs;
+  pa.max_query_len = a.max_query_len;
+  pa.max_seq_len = a.max_seq_len;
+  pa.max_blocks_per_seq = a.max_blocks_per_seq;
+  pa.group = plan.group;
+  pa.num_kv_heads = a.num_kv_heads;
+  pa.prefill_weight = PA_PREFILL_WEIGHT;
+  pa.max_atoms = (int)plan.max_atoms;
+  pa.max_items = (int)plan.max_items;
+  pa.max_slots = (int)plan.max_slots;
+  pa.atoms = reinterpret_cast<int4*>(ws + plan.off_atoms);
+  pa.atom_start = reinterpret_cast<long long*>(ws + plan.off_atom_start);
+  pa.req_dec0 = reinterpret_cast<long long*>(ws + plan.off_req_dec0);
+  pa.req_declen = reinterpret_cast<int*>(ws + plan.off_req_declen);
+  pa.items = reinterpret_cast<int4*>(ws + plan.off_items);
+  pa.cta_begin = reinterpret_cast<int*>(ws + plan.off_cta_begin);
+  pa.seg_cut = reinterpret_cast<int2*>(ws + plan.off_seg_info);
+  pa.req_rows = reinterpret_cast<int*>(ws + plan.off_req_rows);
+  pa.ws_ml = fp.ws_ml;
+  pa.split_list = reinterpret_cast<int4*>(ws + plan.off_split + 16);
+  pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
   if (a.cache_dtype == PA_BF16)
-    return launch_kind<kKindBF16>(fp, plan, tmap_k, tmap_v, items, count, nsplit, stream);
+    return launch_kind<kKindBF16>(fp, pa, plan, tmap_k, tmap_v, stream);
   if (a.cache_dtype == PA_F16)
-    return launch_kind<kKindF16>(fp, plan, tmap_k, tmap_v, items, count, nsplit, stream);
+    return launch_kind<kKindF16>(fp, pa, plan, tmap_k, tmap_v, stream);
   if (a.q_dtype == PA_BF16)
-    return launch_kind<kKindFp8BF16>(fp, plan, tmap_k, tmap_v, items, count, nsplit, stream);
-  return launch_kind<kKindFp8F16>(fp, plan, tmap_k, tmap_v, items, count, nsplit, stream);
+    return launch_kind<kKindFp8BF16>(fp, pa, plan, tmap_k, tmap_v, stream);
+  return launch_kind<kKindFp8F16>(fp, pa, plan, tmap_k, tmap_v, stream);
 }
 
 }  // namespace pa

@@ -166,25 +166,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Bring a tile into L2 ahead of its load (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x,
-                                                int y) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x,
-                                                int y, int z) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map,
                                             uint32_t bar, int x, int y, int z) {
   asm volatile(

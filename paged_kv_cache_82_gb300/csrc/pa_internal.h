@@ -32,16 +32,26 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
 enum : int { kItemDecode = 0, kItemPrefill = 1 };
 
 constexpr int kDecodeMaxRows = 16;   // q_len * group rows handled by one warp
-constexpr int kPrefillTileRows = 64; // rows of a prefill tile (4 warps x 16)
+#ifndef PA_CONSUMER_WARPS
+#define PA_CONSUMER_WARPS 4
+#endif
+// rows of a prefill tile: 16 per consumer warp
+constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
+
+constexpr int kMaxCtasPerSm = 4;     // bound used to size the workspace
 
 struct AttnPlan {
   int group;            // Hq / Hkv
-  int blocks_per_split; // decode split size in blocks
-  int max_splits;       // ceil(max_blocks / blocks_per_split)
-  int has_prefill;      // max_query_len * group > kDecodeMaxRows
-  int64_t max_items;    // grid bound of the main kernel
+  int has_prefill;      // some request may have > 16 query rows
+  int has_decode;       // some request may have <= 16 query rows
+  int grid_max;         // CTAs of the attention kernel, at most
+  int64_t max_atoms;    // prefill tiles, at most
+  int64_t max_items;    // work items, at most
+  int64_t max_slots;    // partial results, at most (2 per CTA)
   // workspace carve-up (byte offsets, 256-aligned)
-  size_t off_items, off_count, off_nsplit, off_acc, off_ml, total_bytes;
+  size_t off_atoms, off_atom_start, off_req_dec0, off_req_declen, off_req_rows,
+      off_items,
+      off_cta_begin, off_seg_info, off_split, off_acc, off_ml, total_bytes;
 };
 
 // Host planning from host-known sizes only (no device read-back).

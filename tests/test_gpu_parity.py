@@ -369,7 +369,8 @@ def test_host_validation_rejects_before_launch():
     bt, sl, qsl = (torch.zeros(2, 4, **i32), torch.ones(2, **i32),
                    torch.tensor([0, 1, 2], **i32))
     s = torch.cuda.current_stream().cuda_stream
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(pa.pa_attention_workspace_size(2, 8, 2, 128, 2, 1, 1),
+                     dtype=torch.uint8, device="cuda")
 
     def call(**kw):
         a = dict(q=q.data_ptr(), qdt=pa.PA_BF16, kc=kc.data_ptr(),
