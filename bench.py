@@ -286,7 +286,7 @@ def _traffic_record(kernel_src_hash):
 def _kernel_hash():
     import hashlib
     h = hashlib.sha256()
-    for f in ("attn_fast.cu", "pa_common.cuh"):
+    for f in ("attn_fast.cu", "pa_common.cuh", "pa_internal.h"):
         with open(os.path.join(ROOT, "paged_kv_cache_82_gb300", "csrc", f),
                   "rb") as fh:
             h.update(fh.read())

@@ -44,7 +44,7 @@ namespace {
 constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
 
 #ifndef PA_PREFILL_WEIGHT
-#define PA_PREFILL_WEIGHT 4     // cost of a prefill tile page vs a decode page
+#define PA_PREFILL_WEIGHT 2     // cost of a prefill tile page vs a decode page
 #endif
 #ifndef PA_CONSUMER_WARPS
 #define PA_CONSUMER_WARPS 4     // consumer warps per CTA (one producer warp)
