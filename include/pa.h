@@ -227,6 +227,44 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
 pa_status pa_get_device_error(pa_stream_t stream, uint32_t* flags);
 
 /*
+ * pa_attention_noalloc -- pa_attention without a caller-provided workspace.
+ * No counterpart on the pages: it exists for callers that cannot allocate
+ * device memory per step -- for instance an engine that gives all free HBM
+ * to its KV-cache pool at start-up, or code that must not call cudaMalloc /
+ * cudaFree because they can synchronise the device.
+ *
+ * Same arguments and results as pa_attention, minus the workspace.  The
+ * scratch is one fixed array of PA_NOALLOC_SCRATCH_BYTES in device memory
+ * that the library image carries: every GPU that loads the library holds it
+ * until the process exits.  The function allocates nothing and calls no
+ * allocating routine.
+ *
+ *  - Sizes whose workspace (pa_attention_workspace_size) exceeds
+ *    PA_NOALLOC_SCRATCH_BYTES are rejected with PA_ERR_INVALID_ARG before
+ *    anything runs.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's
+ *    contents (nothing in it needs to start at zero).  Calls whose work
+ *    overlaps on the GPU -- on different streams, or from different host
+ *    threads without ordering -- race on it: order them.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+pa_status pa_attention_noalloc(const void* q, pa_dtype q_dtype,
+                               const void* k_cache, const void* v_cache,
+                               pa_dtype cache_dtype, int64_t num_blocks,
+                               int block_size, int num_q_heads,
+                               int num_kv_heads, int head_dim,
+                               const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, int num_seqs,
+                               int64_t num_tokens, int max_query_len,
+                               int max_seq_len, float scale, float k_scale,
+                               float v_scale, void* out, pa_stream_t stream);
+
+/*
  * pa_set_profile_events -- measurement hook (no counterpart on the pages).
  * When both events are non-NULL, every later pa_attention call on this
  * thread records `start` on its stream immediately before the launch of the

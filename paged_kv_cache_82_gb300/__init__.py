@@ -237,3 +237,37 @@ def pa_set_profile_events(start: Optional[torch.cuda.Event],
         return ev.cuda_event
     _check(_load().pa_set_profile_events(handle(start), handle(stop)),
            "pa_set_profile_events")
+
+
+def pa_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                         max_query_len: int, max_seq_len: int, scale: float,
+                         k_scale: float = 1.0, v_scale: float = 1.0,
+                         out: Optional[torch.Tensor] = None,
+                         cache_dtype: Optional[str] = None,
+                         stream=None) -> torch.Tensor:
+    """pa_attention with the library's fixed device scratch instead of a
+    workspace, for callers that cannot allocate device memory per step (the
+    output tensor is still the caller's)."""
+    lib = _load()
+    f = lib.pa_attention_noalloc
+    P, i64, i32, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                        ctypes.c_float)
+    f.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32, i32, P, i32, P, P,
+                  i32, i64, i32, i32, f32, f32, f32, P, P]
+    f.restype = i32
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    B = seq_lens.numel()
+    if out is None:
+        raise ValueError("pa_attention_noalloc needs a caller-provided out")
+    st = f(_dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
+           _dev(v_cache, "v_cache"), _dtype_code(k_cache, cache_dtype), NB, bs,
+           Hq, Hkv, D, _dev(block_tables, "block_tables"),
+           block_tables.shape[1], _dev(seq_lens, "seq_lens"),
+           _dev(query_start_loc, "query_start_loc"), B, T, int(max_query_len),
+           int(max_seq_len), float(scale), float(k_scale), float(v_scale),
+           _dev(out, "out"), _stream(stream))
+    _check(st, "pa_attention_noalloc")
+    return out
