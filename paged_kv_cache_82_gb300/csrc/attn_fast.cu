@@ -43,6 +43,9 @@ namespace {
 #endif
 constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
 
+#ifndef PA_PRODUCER_PAGES
+#define PA_PRODUCER_PAGES 4     // pages the producer issues per step (2 lanes each)
+#endif
 #ifndef PA_PREFILL_WEIGHT
 #define PA_PREFILL_WEIGHT 2     // cost of a prefill tile page vs a decode page
 #endif
@@ -1408,15 +1411,22 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int buf = (j0 >> 5) & 1;
         const int nidx = j0 + 32 + lane;
         const int nreg = nidx < n ? __ldg(bt + nidx) : 0;
-        if (lane < 2) {
+        // lanes 2k and 2k+1 issue page j + k of each group of PP pages
+        constexpr int PP = PA_PRODUCER_PAGES;
+        constexpr unsigned kMask = (PP >= 16) ? 0xFFFFFFFFu : ((1u << (2 * PP)) - 1u);
+        if (lane < 2 * PP) {
           const int* cur = sm.ids + buf * 32;
           const int cnt = min(32, n - j0);
-          const CUtensorMap* map = lane ? &tmap_v : &tmap_k;
-          for (int jj = 0; jj < cnt; ++jj) {
-            const int slot = c % S;
-            const bool ok = c < (uint32_t)S ||
-                            mbar_wait_bounded(sm.empty(slot), ((c / S) - 1) & 1);
-            if (__any_sync(0x3u, !ok)) {
+          const int kk = lane >> 1;        // page within the group
+          const int kv = lane & 1;         // 0: K page, 1: V page
+          const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+          for (int jj = 0; jj < cnt; jj += PP) {
+            const bool mine = jj + kk < cnt;
+            const uint32_t cc = c + kk;
+            const int slot = cc % S;
+            const bool ok = !mine || cc < (uint32_t)S ||
+                            mbar_wait_bounded(sm.empty(slot), ((cc / S) - 1) & 1);
+            if (__any_sync(kMask, !ok)) {
               if (lane == 0) {
                 flag_error(p.err, PA_DEV_ERR_TIMEOUT);
                 *sm.abort_flag = 1;
@@ -1424,21 +1434,23 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
               go = 0;
               break;
             }
-            int blk = cur[jj];
-            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-              if (lane == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
-              blk = 0;
+            if (mine) {
+              int blk = cur[jj + kk];
+              if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                if (kv == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+                blk = 0;
+              }
+              const int row = (blk * p.num_kv_heads + rec0.y) * kBS;
+              const uint32_t dst =
+                  sm.base + Ly::kRing + slot * Tr::kStageBytes + kv * Tr::kPageBytes;
+              if (kv == 0) mbar_arrive_expect_tx(sm.full(slot), Tr::kStageBytes);
+              __syncwarp(__activemask());
+              if constexpr (Tr::kFp8)
+                tma_load_2d(dst, map, sm.full(slot), 0, row);
+              else
+                tma_load_3d(dst, map, sm.full(slot), 0, 0, row);
             }
-            const int row = (blk * p.num_kv_heads + rec0.y) * kBS;
-            const uint32_t dst =
-                sm.base + Ly::kRing + slot * Tr::kStageBytes + lane * Tr::kPageBytes;
-            if (lane == 0) mbar_arrive_expect_tx(sm.full(slot), Tr::kStageBytes);
-            __syncwarp(0x3u);
-            if constexpr (Tr::kFp8)
-              tma_load_2d(dst, map, sm.full(slot), 0, row);
-            else
-              tma_load_3d(dst, map, sm.full(slot), 0, 0, row);
-            ++c;
+            c += min(PP, cnt - jj);
           }
         }
         __syncwarp();
