@@ -42,6 +42,7 @@ namespace {
 #define PA_NARROW_MIN_BLOCKS 3  // resident CTAs per SM, <= 8-row kernel
 #endif
 constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
+constexpr int kSelfPlanMaxSeqs = 1024;  // decode steps the kernel plans itself
 
 #ifndef PA_PRODUCER_PAGES
 #define PA_PRODUCER_PAGES 4     // pages the producer issues per step (2 lanes each)
@@ -133,6 +134,7 @@ struct FastParams {
   int max_query_len, max_seq_len;
   float score_scale;  // softmax scale * log2(e) (* k_scale for FP8)
   float out_scale;    // 1, or v_scale for FP8
+  int self_plan;      // 1: every CTA plans its own range (decode-only steps)
 };
 
 // ---------------------------------------------------------------------------
@@ -1011,7 +1013,13 @@ struct Layout {
   static constexpr int kNumBars = 2 * Tr::kStages;
   static constexpr int kIds = kBars + 8 * kNumBars;               // int [2][32]
   static constexpr int kAbort = kIds + 2 * 32 * 4;
-  static constexpr int kBytes = kAbort + 16;
+  // narrow kernel: the CTA's own plan (per-request decode offset, pages,
+  // rows) and scan scratch
+  static constexpr int kPlan = kAbort + 16;
+  static constexpr int kPlanBytes = kWide ? 0 : kSelfPlanMaxSeqs * 16;
+  static constexpr int kScan = kPlan + kPlanBytes;
+  static constexpr int kScanBytes = kWide ? 0 : 34 * 8;
+  static constexpr int kBytes = kScan + kScanBytes;
   static constexpr int kSmemBytes = 1024 + kBytes;  // + alignment slack
 };
 
@@ -1341,6 +1349,106 @@ __device__ void consume_item_narrow(const FastParams& p, const Smem& sm,
   }
 }
 
+// Where a CTA's work items come from: the planner's list, or (decode-only
+// steps, self_plan) the CTA's own stream-K range over the per-request page
+// prefix it computed in its prologue.  Every warp of the CTA keeps its own
+// copy and draws the same sequence.
+struct ItemSource {
+  // planner list
+  const int4* items;
+  int k, end;
+  // own range
+  bool self;
+  const long long* dec0;
+  const int* declen;
+  const int* rows;
+  long long cur, lo, hi;
+  int r, B, H, b;
+
+  __device__ bool next(int4& rec0, int4& rec1) {
+    if (!self) {
+      if (k >= end) return false;
+      rec0 = __ldg(items + 2 * k);
+      rec1 = __ldg(items + 2 * k + 1);
+      ++k;
+      return true;
+    }
+    if (cur >= hi) return false;
+    while (r < B && declen[r] == 0) ++r;
+    if (r >= B) return false;
+    const long long rs = dec0[r];
+    const int dl = declen[r];
+    const int g = (int)((cur - rs) / dl);
+    const long long ss = rs + (long long)g * dl, se = ss + dl;
+    const long long pe = se < hi ? se : hi;
+    // a piece that continues a segment begun in an earlier range is this
+    // CTA's "head" part (slot 2b); one that continues into a later range is
+    // its "tail" part (slot 2b + 1)
+    const bool before = cur == lo && ss < lo;
+    const bool after = pe == hi && se > hi;
+    const int slot = before ? 2 * b : (after ? 2 * b + 1 : -1);
+    rec0 = make_int4(r, g, kItemDecode, slot);
+    rec1 = make_int4((int)(cur - ss), (int)(pe - ss), rows[r], 0);
+    cur = pe;
+    if (pe == se && g + 1 == H) ++r;
+    return true;
+  }
+};
+
+// Per-request decode pages of the step and their prefix (units of pages x
+// KV heads) into shared memory; all threads of the block take part.
+// Returns the total.  Requests with invalid metadata contribute nothing.
+__device__ long long plan_prefix(const FastParams& p, long long* dec0,
+                                 int* declen, int* rows, long long* scan_tot,
+                                 long long* scan_ws) {
+  long long run = 0;
+  for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    int dl = 0, rw = 0;
+    if (r < p.num_seqs) {
+      const ReqMeta m = load_req(p.qsl, p.seq_lens, r, p.num_tokens,
+                                 p.max_query_len, p.max_seq_len,
+                                 p.max_blocks_per_seq);
+      if (m.ok && m.n > 0 && m.n * p.group <= 8) {
+        dl = m.nb;
+        rw = m.n * p.group;
+      } else if (!m.ok && blockIdx.x == 0) {
+        flag_error(p.err, PA_DEV_ERR_METADATA);
+      }
+    }
+    const long long ex =
+        block_scan_excl<long long>((long long)dl * p.num_kv_heads, scan_tot, scan_ws);
+    const long long tot = *scan_tot;
+    __syncthreads();
+    if (r < p.num_seqs) {
+      dec0[r] = run + ex;
+      declen[r] = dl;
+      rows[r] = rw;
+    }
+    run += tot;
+  }
+  __syncthreads();
+  return run;
+}
+
+__device__ __forceinline__ int self_plan_grid(long long C, int grid) {
+  long long g = C / kMinUnitsPerCta;
+  if (g > grid) g = grid;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+// first request whose decode range holds unit u (skipping empty requests)
+__device__ __forceinline__ int request_of(const long long* dec0, int B,
+                                          long long u) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (dec0[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // kWide = false: every work item has at most 8 query rows (decode steps with
 // q_len * group <= 8) -- half the accumulators.
 // kWide = true: any item (up to 16 rows per warp, prefill tiles).
@@ -1381,8 +1489,37 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
   __syncthreads();
   pdl_launch_dependents();  // the merge may be scheduled behind this grid
   pdl_wait();               // the planner (and everything before it) is done
-  const int it_begin = __ldg(p.cta_begin + blockIdx.x);
-  const int it_end = __ldg(p.cta_begin + blockIdx.x + 1);
+  ItemSource src{};
+  src.self = false;
+  if constexpr (!kWide) {
+    if (p.self_plan) {
+      long long* dec0 = reinterpret_cast<long long*>(sm.ptr + Ly::kPlan);
+      int* declen = reinterpret_cast<int*>(dec0 + kSelfPlanMaxSeqs);
+      int* rows = declen + kSelfPlanMaxSeqs;
+      long long* scan = reinterpret_cast<long long*>(sm.ptr + Ly::kScan);
+      const long long C = plan_prefix(p, dec0, declen, rows, scan + 32, scan);
+      const int g_eff = self_plan_grid(C, gridDim.x);
+      src.self = true;
+      src.dec0 = dec0;
+      src.declen = declen;
+      src.rows = rows;
+      src.B = p.num_seqs;
+      src.H = p.num_kv_heads;
+      src.b = blockIdx.x;
+      src.lo = src.hi = 0;
+      if ((int)blockIdx.x < g_eff && C > 0) {
+        src.lo = (long long)blockIdx.x * C / g_eff;
+        src.hi = (long long)(blockIdx.x + 1) * C / g_eff;
+      }
+      src.cur = src.lo;
+      src.r = p.num_seqs > 0 ? request_of(dec0, p.num_seqs, src.lo) : 0;
+    }
+  }
+  if (!src.self) {
+    src.items = p.items;
+    src.k = __ldg(p.cta_begin + blockIdx.x);
+    src.end = __ldg(p.cta_begin + blockIdx.x + 1);
+  }
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -1392,9 +1529,8 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     uint32_t c = 0;     // pages issued
     int go = 1;
-    for (int k = it_begin; k < it_end && go; ++k) {
-      const int4 rec0 = __ldg(p.items + 2 * k);
-      const int4 rec1 = __ldg(p.items + 2 * k + 1);
+    int4 rec0, rec1;
+    while (go && src.next(rec0, rec1)) {
       // the narrow kernel never gets prefill tiles or items over 8 rows (the
       // host guarantees it); both sides skip them the same way
       if (!kWide && (rec0.z == kItemPrefill || rec1.z > 8)) continue;
@@ -1471,9 +1607,8 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   // ------------------------------ consumers -------------------------------
   uint32_t c = 0;  // pages consumed (CTA-wide numbering, as issued)
-  for (int k = it_begin; k < it_end; ++k) {
-    const int4 rec0 = __ldg(p.items + 2 * k);
-    const int4 rec1 = __ldg(p.items + 2 * k + 1);
+  int4 rec0, rec1;
+  while (src.next(rec0, rec1)) {
     // every consumer warp meets here once per item: decisions below are
     // uniform, the previous item's shared scratch is no longer read, and all
     // earlier pages have been consumed by their owners
@@ -1501,8 +1636,6 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
 }
 
-// ---------------------------------------------------------------------------
-// split-K merge: one warp per (token, q head) row of a split decode request
 // ---------------------------------------------------------------------------
 // split-K merge: CTA k finishes split segment k (request r, KV head g): one
 // warp per query row, parts combined in slot order (deterministic)
@@ -1532,6 +1665,73 @@ merge_kernel(FastParams p) {
       const int64_t pr = (int64_t)(first + s) * 16 + rr;
       const float ms = p.ws_ml[pr * 2];
       if (ms == -INFINITY) continue;  // a part with no keys
+      const float w = exp2f(ms - M);
+      den += w * p.ws_ml[pr * 2 + 1];
+      const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + pr * 128 + 4 * lane);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    }
+    const float inv = p.out_scale / den;
+    TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+  }
+}
+
+// Split-K merge of a self-planned decode step: CTA b looks at the range
+// boundary b; if it is the first boundary inside a segment it combines that
+// segment's parts -- the tail of range b-1 (slot 2(b-1)+1) and the heads of
+// ranges b, b+1, ... (slots 2k) -- in that order.
+template <typename TOut>
+__global__ void __launch_bounds__(128)
+merge_self_kernel(FastParams p) {
+  extern __shared__ long long mplan[];
+  __shared__ long long scan[34];
+  pdl_wait();
+  long long* dec0 = mplan;
+  int* declen = reinterpret_cast<int*>(dec0 + p.num_seqs);
+  int* rows = declen + p.num_seqs;
+  const long long C = plan_prefix(p, dec0, declen, rows, scan + 32, scan);
+  const int g_eff = self_plan_grid(C, gridDim.x);
+  const int b = blockIdx.x;
+  if (b == 0 || b >= g_eff || C <= 0) return;
+  const long long lo_b = (long long)b * C / g_eff;
+  const long long lo_p = (long long)(b - 1) * C / g_eff;
+  int r = request_of(dec0, p.num_seqs, lo_b);
+  while (r < p.num_seqs && declen[r] == 0) ++r;
+  if (r >= p.num_seqs) return;
+  const int dl = declen[r];
+  const int g = (int)((lo_b - dec0[r]) / dl);
+  const long long ss = dec0[r] + (long long)g * dl, se = ss + dl;
+  if (ss >= lo_b || ss < lo_p) return;  // not cut here, or cut earlier
+  // parts in order: slot 2(b-1)+1, then 2k for the ranges b..k_end-1 that
+  // begin inside the segment
+  int k_end = b + 1;
+  while (k_end < g_eff && (long long)k_end * C / g_eff < se) ++k_end;
+  const int np = 1 + (k_end - b);
+  const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
+                              p.max_seq_len, p.max_blocks_per_seq);
+  const int lane = threadIdx.x & 31;
+  for (int rr = threadIdx.x >> 5; rr < rows[r]; rr += blockDim.x >> 5) {
+    const int i = rr / p.group;
+    const int h = g * p.group + (rr - i * p.group);
+    const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
+    float M = -INFINITY;
+    for (int s = lane; s < np; s += 32) {
+      const int slot = s == 0 ? 2 * (b - 1) + 1 : 2 * (b + s - 1);
+      M = fmaxf(M, p.ws_ml[((int64_t)slot * 16 + rr) * 2]);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float den = 0.f;
+    for (int s = 0; s < np; ++s) {
+      const int slot = s == 0 ? 2 * (b - 1) + 1 : 2 * (b + s - 1);
+      const int64_t pr = (int64_t)slot * 16 + rr;
+      const float ms = p.ws_ml[pr * 2];
+      if (ms == -INFINITY) continue;  // a part with no visible key
       const float w = exp2f(ms - M);
       den += w * p.ws_ml[pr * 2 + 1];
       const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + pr * 128 + 4 * lane);
@@ -1591,9 +1791,15 @@ cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
   if (e != cudaSuccess) return e;
   if (grid > plan.grid_max) grid = plan.grid_max;
   pa.grid = grid;
-  plan_kernel<<<1, kPlanThreads, kPlanCacheBytes, stream>>>(pa);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  // decode-only steps of up to kSelfPlanMaxSeqs requests plan inside the
+  // attention kernel (no planner launch)
+  FastParams f = fp;
+  f.self_plan = !wide && fp.num_seqs <= kSelfPlanMaxSeqs;
+  if (!f.self_plan) {
+    plan_kernel<<<1, kPlanThreads, kPlanCacheBytes, stream>>>(pa);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   // The attention kernel and the merge are launched as programmatic
   // dependents: each may start while its predecessor runs and waits (on the
   // device) for it to finish before touching its results.  With the
@@ -1612,18 +1818,23 @@ cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
   if (pe.start) cudaEventRecord(pe.start, stream);
   if (wide) {
     cfg.dynamicSmemBytes = Layout<kKind, true>::kSmemBytes;
-    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, true>, tk, tv, fp);
+    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, true>, tk, tv, f);
   } else {
     cfg.dynamicSmemBytes = Layout<kKind, false>::kSmemBytes;
-    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, false>, tk, tv, fp);
+    e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, false>, tk, tv, f);
   }
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
   if (plan.has_decode) {
     // split segments: at most one fewer than the CTAs that got work
     cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<OutT<kKind>>, fp);
+    if (f.self_plan) {
+      cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
+      e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
+    } else {
+      cfg.dynamicSmemBytes = 0;
+      e = cudaLaunchKernelEx(&cfg, merge_kernel<OutT<kKind>>, f);
+    }
   }
   return e;
 }
@@ -1632,7 +1843,6 @@ cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
 
 bool fast_path_supported(const AttnArgs& a) {
   if (a.head_dim != 128) return false;
-  if (a.num_q_heads / a.num_kv_heads > kDecodeMaxRows && false) return false;
   if (a.cache_dtype == PA_BF16 && a.q_dtype == PA_BF16) return true;
   if (a.cache_dtype == PA_F16 && a.q_dtype == PA_F16) return true;
   if (a.cache_dtype == PA_FP8_E4M3 && (a.q_dtype == PA_BF16 || a.q_dtype == PA_F16))

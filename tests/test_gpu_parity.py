@@ -154,6 +154,22 @@ def test_ragged_lengths(cache_dtype):
                         write_new=cache_dtype == "e4m3"))
 
 
+@pytest.mark.parametrize("batch", [1024, 1100])
+def test_decode_batch_around_in_kernel_plan_limit(batch):
+    # up to 1024 decode requests the attention kernel plans its own split-K
+    # ranges; beyond that the planner kernel does
+    rng = np.random.default_rng(batch)
+    seq_q = [(int(L), 1) for L in rng.integers(1, 120, size=batch)]
+    _check_step(_custom(seq_q, 32, 8, write_new=True))
+
+
+@pytest.mark.parametrize("cache_dtype", ["bf16", "e4m3"])
+def test_one_long_sequence_split_over_many_ctas(cache_dtype):
+    # every KV head's segment is cut by dozens of CTA boundaries
+    _check_step(_custom([(40000, 1)], 32, 8, cache_dtype=cache_dtype,
+                        write_new=True))
+
+
 @pytest.mark.parametrize("Hq,Hkv,seq_q", [
     (32, 8, [(300, 4), (40, 3), (17, 2)]),      # 16, 12, 8 rows: decode class
     (32, 8, [(300, 5), (100, 64)]),             # 20 / 256 rows: prefill tiles
