@@ -16,7 +16,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpa.so")
 
-SOURCES = ["pa_api.cu", "cache_kernels.cu", "attn_fast.cu", "attn_generic.cu",
+SOURCES = ["pa_api.cu", "cache_kernels.cu", "attn_fast.cu", "attn_prefill_tc.cu",
+           "attn_generic.cu",
            "pa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

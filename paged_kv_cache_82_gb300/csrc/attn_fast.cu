@@ -158,6 +158,9 @@ struct PlanArgs {
   int64_t num_tokens;
   int num_seqs, max_query_len, max_seq_len, max_blocks_per_seq;
   int group, num_kv_heads, grid, prefill_weight;
+  int tile_rows;          // query rows of a prefill tile
+  int prefill_tc;         // 1: prefill tiles go to the tensor-core kernel
+  int* n_atoms_out;       // prefill tiles of the step (for that kernel)
   int max_atoms, max_items, max_slots;
   int4* atoms;            // prefill tiles: {r, g, tile, pages}
   long long* atom_start;  // cost offset of each tile
@@ -201,8 +204,9 @@ __device__ __forceinline__ T block_scan_excl(T v, T* total, T* warp_sums) {
 }
 
 // key pages seen by prefill tile tt of a request (its last row's limit)
-__device__ __forceinline__ int tile_pages(const ReqMeta& m, int G, int tt) {
-  const int last_row = min(m.n * G, (tt + 1) * kPrefillTileRows) - 1;
+__device__ __forceinline__ int tile_pages(const ReqMeta& m, int G, int tt,
+                                          int tile_rows) {
+  const int last_row = min(m.n * G, (tt + 1) * tile_rows) - 1;
   return (m.L - m.n + last_row / G) / kBS + 1;
 }
 
@@ -234,13 +238,6 @@ __device__ __forceinline__ int lower_bound_ll(const long long* a, int n,
 
 constexpr int kPlanCacheBytes = 40 * 1024;  // dynamic shared memory of the planner
 
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
   extern __shared__ long long plan_cache[];
   // the attention kernel may start its prologue now; it waits for this
@@ -268,8 +265,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
         if (m.n * G <= kDecodeMaxRows) {
           declen = m.nb;
         } else {
-          tiles = (m.n * G + kPrefillTileRows - 1) / kPrefillTileRows;
-          for (int tt = 0; tt < tiles; ++tt) pcost += (long long)tile_pages(m, G, tt) * W;
+          tiles = (m.n * G + pa.tile_rows - 1) / pa.tile_rows;
+          // tiles run by the tensor-core kernel are not on the cost line
+          if (!pa.prefill_tc)
+            for (int tt = 0; tt < tiles; ++tt)
+              pcost += (long long)tile_pages(m, G, tt, pa.tile_rows) * W;
         }
       }
     }
@@ -292,8 +292,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
       long long a0 = run_atoms + ex_atoms;
       long long c0 = run_pcost + ex_pcost;
       for (int tt = 0; tt < tiles; ++tt) {
-        const int pg = tile_pages(m, G, tt);
-        const long long c = (long long)pg * W;
+        const int pg = tile_pages(m, G, tt, pa.tile_rows);
+        const long long c = pa.prefill_tc ? 0 : (long long)pg * W;
         for (int g = 0; g < H; ++g) {
           const long long ai = a0 + (long long)tt * H + g;
           if (ai < pa.max_atoms) {
@@ -312,11 +312,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
   }
   if (threadIdx.x == 0) {
     s_atoms = run_atoms < pa.max_atoms ? run_atoms : pa.max_atoms;
+    if (pa.prefill_tc) *pa.n_atoms_out = (int)s_atoms;
     s_cost_pre = run_pcost;
     s_dec_total = run_dec;
   }
   __syncthreads();
-  const int n_atoms = (int)s_atoms;
+  // prefill tiles the attention kernel runs (none when the tensor-core
+  // kernel takes them)
+  const int n_atoms = pa.prefill_tc ? 0 : (int)s_atoms;
   const long long cost_pre = s_cost_pre, dec_total = s_dec_total;
   const long long C = cost_pre + dec_total;
   // CTAs that get work: every cost range at least kMinUnitsPerCta long, so
@@ -433,7 +436,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
                                        pa.max_query_len, pa.max_seq_len,
                                        pa.max_blocks_per_seq);
             const int rows =
-                min(kPrefillTileRows, m.n * G - at.z * kPrefillTileRows);
+                min(pa.tile_rows, m.n * G - at.z * pa.tile_rows);
             pa.items[2 * o] = make_int4(at.x, at.y, kItemPrefill, at.z);
             pa.items[2 * o + 1] = make_int4(0, at.w, rows, 0);
           }
@@ -1780,8 +1783,9 @@ cudaError_t prepare_kernel(int* grid) {
 }
 
 template <int kKind>
-cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
-                        const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
+                        const AttnPlan& plan, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const TcMaps* tc, int num_sms,
                         cudaStream_t stream) {
   // the narrow kernel covers steps whose every item has <= 8 rows
   const bool wide = (int64_t)fp.max_query_len * fp.group > 8;
@@ -1816,6 +1820,12 @@ cudaError_t launch_kind(const FastParams& fp, PlanArgs pa, const AttnPlan& plan,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (pe.start) cudaEventRecord(pe.start, stream);
+  if (tc) {
+    // prefill tiles on the tensor cores, ahead of the decode work
+    e = launch_prefill_tc(a, *tc, pa.atoms, pa.n_atoms_out, pa.max_atoms,
+                          num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
   if (wide) {
     cfg.dynamicSmemBytes = Layout<kKind, true>::kSmemBytes;
     e = cudaLaunchKernelEx(&cfg, attn_fast_kernel<kKind, true>, tk, tv, f);
@@ -1878,6 +1888,7 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
   pl.off_cta_begin = off;   off = up(off + (size_t)(pl.grid_max + 1) * 4);
   pl.off_seg_info = off;    off = up(off + (size_t)num_seqs * num_kv_heads * 8);
   pl.off_split = off;       off = up(off + (size_t)pl.max_slots * 16 + 16);
+  pl.off_pref = off;        off = up(off + 16);
   pl.off_acc = off;
   if (pl.has_decode) off = up(off + (size_t)pl.max_slots * 16 * head_dim * 4);
   pl.off_ml = off;
@@ -1888,8 +1899,8 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
 
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
                                   const CUtensorMap& tmap_k,
-                                  const CUtensorMap& tmap_v,
-                                  cudaStream_t stream) {
+                                  const CUtensorMap& tmap_v, const TcMaps* tc,
+                                  int num_sms, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   FastParams fp{};
   fp.q = a.q;
@@ -1930,6 +1941,9 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.group = plan.group;
   pa.num_kv_heads = a.num_kv_heads;
   pa.prefill_weight = PA_PREFILL_WEIGHT;
+  pa.prefill_tc = tc != nullptr;
+  pa.tile_rows = tc ? tc_prefill_tile_rows(plan.group) : kPrefillTileRows;
+  pa.n_atoms_out = reinterpret_cast<int*>(ws + plan.off_pref);
   pa.max_atoms = (int)plan.max_atoms;
   pa.max_items = (int)plan.max_items;
   pa.max_slots = (int)plan.max_slots;
@@ -1945,12 +1959,16 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.split_list = reinterpret_cast<int4*>(ws + plan.off_split + 16);
   pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
   if (a.cache_dtype == PA_BF16)
-    return launch_kind<kKindBF16>(fp, pa, plan, tmap_k, tmap_v, stream);
+    return launch_kind<kKindBF16>(a, fp, pa, plan, tmap_k, tmap_v, tc, num_sms,
+                                  stream);
   if (a.cache_dtype == PA_F16)
-    return launch_kind<kKindF16>(fp, pa, plan, tmap_k, tmap_v, stream);
+    return launch_kind<kKindF16>(a, fp, pa, plan, tmap_k, tmap_v, tc, num_sms,
+                                 stream);
   if (a.q_dtype == PA_BF16)
-    return launch_kind<kKindFp8BF16>(fp, pa, plan, tmap_k, tmap_v, stream);
-  return launch_kind<kKindFp8F16>(fp, pa, plan, tmap_k, tmap_v, stream);
+    return launch_kind<kKindFp8BF16>(a, fp, pa, plan, tmap_k, tmap_v, nullptr,
+                                     num_sms, stream);
+  return launch_kind<kKindFp8F16>(a, fp, pa, plan, tmap_k, tmap_v, nullptr,
+                                  num_sms, stream);
 }
 
 }  // namespace pa

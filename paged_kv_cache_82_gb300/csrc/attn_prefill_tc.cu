@@ -1,0 +1,548 @@
+// attn_prefill_tc.cu -- the prefill tiles of a unified step on the
+// 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// What it computes ("vLLM engine anatomy": PagedAttention section and Figure
+// 2 for the paging, Table 1 for GQA; "vLLM V1 engine architecture" for
+// chunked prefill; "Boundaries: FlashAttention ..." for exact attention with
+// an online softmax): for every query row of a prefill-class request (query
+// token i of n, q head h of KV head g = h / G), softmax attention over the
+// request's keys 0 .. L - n + i, read through the block table from 16-token
+// pages.  Decode-class requests are left to the attention kernel of
+// attn_fast.cu.
+//
+// How (one CTA per SM, persistent over the step's prefill tiles):
+//  * A tile is 128 query rows of one (request, KV head): 128 / G consecutive
+//    tokens times the G q heads of the group, row = token * G + head.  Keys
+//    go in chunks of 128 (8 pages).
+//  * warp 4 (TMA producer): the Q tile through a 3-D map over q
+//    [token][head][dim], and for every chunk its pages of K and of V through
+//    a 2-D map over the cache rows, each page as two 64-column halves under
+//    the 128-byte swizzle, into a two-deep ring.  The same shared-memory
+//    layout serves as the K-major B operand of Q.K^T and as the MN-major B
+//    operand of P.V.
+//  * warp 5 (MMA): allocates tensor memory (512 columns: two S buffers, O,
+//    P) and issues, from one lane, S = Q.K^T (M 128, N = 16 x pages of the
+//    chunk, K 128) into the S buffer of the chunk, and O += P.V with P read
+//    from tensor memory.  P goes in two bf16 (or f16) parts, P = hi + lo, so
+//    that the rounding of the probabilities to 16 bits costs no accuracy.
+//    Completion is tracked with tcgen05.commit on mbarriers.
+//  * warps 0-3 (softmax): one thread per query row.  Each chunk: S from
+//    tensor memory, scale and causal mask, online softmax against a
+//    reference max that only moves when the row max has grown by more than
+//    2^8 (O is then rescaled in tensor memory; otherwise the exponentials
+//    stay below 2^8), P into tensor memory.  At the end of the tile: O / l in
+//    the output type.
+//  * V rows of the request's last page that lie past the sequence end are
+//    cleared in shared memory before P.V (their P is 0, but 0 x NaN is not).
+//
+// Every wait is bounded; on a timeout the CTA records PA_DEV_ERR_TIMEOUT,
+// lets its copies and MMAs in flight finish, frees its tensor memory and
+// returns.
+#include <float.h>
+
+#include <type_traits>
+
+#include "pa_common.cuh"
+#include "pa_internal.h"
+#include "tcgen05.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTcRows = 128;               // query rows of a tile (MMA M)
+constexpr int kTcKeys = 128;               // keys of a chunk
+constexpr int kTcPages = kTcKeys / kBS;    // pages of a chunk
+constexpr int kTcThreads = 192;            // 4 softmax warps, producer, MMA
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kHalf = 128 * 128;           // 128 rows x 128 B: one column half
+constexpr int kTileBytes = 2 * kHalf;      // 128 rows x 128 columns, 16-bit
+constexpr int kPageHalf = kBS * 128;       // one page, one column half
+constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (log2)
+
+// tensor-memory columns
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;      // S buffers at 0 and 128
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColPHi = 384;
+constexpr uint32_t kColPLo = 448;
+
+// barriers
+enum : int {
+  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
+  kSFull = 10, kSFree = 12, kPFull = 14, kODone = 15, kMmaDone = 16,
+  kNumBars = 17
+};
+
+struct TcLayout {
+  static constexpr int kK = 0;                       // 2 K stages
+  static constexpr int kV = kK + 2 * kTileBytes;     // 2 V stages
+  static constexpr int kQ = kV + 2 * kTileBytes;     // Q tile
+  static constexpr int kBars = kQ + kTileBytes;
+  static constexpr int kTmemSlot = kBars + 8 * kNumBars;
+  static constexpr int kAbort = kTmemSlot + 4;
+  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
+};
+
+struct TcParams {
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int4* atoms;     // prefill tiles {r, g, tile, pages} from the planner
+  const int* n_atoms;
+  int max_atoms;
+  unsigned* err;
+  int64_t num_tokens;
+  int64_t num_blocks;
+  int max_blocks_per_seq, num_seqs;
+  int num_q_heads, num_kv_heads, group;
+  int max_query_len, max_seq_len;
+  int tokens_per_tile;   // 128 / group
+  float score_scale;     // softmax scale * log2(e)
+};
+
+// one tile, as every role of the CTA sees it
+struct TcTile {
+  int r, g, q0, n, L, i0, ntok, pages, nc;
+  bool ok;
+};
+
+__device__ __forceinline__ TcTile tc_tile(const TcParams& p, int a) {
+  const int4 at = __ldg(p.atoms + a);
+  TcTile t{};
+  t.r = at.x;
+  t.g = at.y;
+  t.ok = at.x >= 0 && at.x < p.num_seqs && at.y >= 0 && at.y < p.num_kv_heads;
+  if (!t.ok) return t;
+  const ReqMeta m = load_req(p.qsl, p.seq_lens, t.r, p.num_tokens,
+                             p.max_query_len, p.max_seq_len,
+                             p.max_blocks_per_seq);
+  t.q0 = m.q0;
+  t.n = m.n;
+  t.L = m.L;
+  t.i0 = at.z * p.tokens_per_tile;
+  t.ntok = min(p.tokens_per_tile, m.n - t.i0);
+  t.ok = m.ok && at.z >= 0 && t.ntok > 0;
+  // keys up to the last token's limit L - n + i0 + ntok - 1
+  t.pages = t.ok ? (t.L - t.n + t.i0 + t.ntok - 1) / kBS + 1 : 0;
+  t.nc = (t.pages + kTcPages - 1) / kTcPages;
+  return t;
+}
+
+// Bounded wait by a whole warp; false (and the CTA aborts) on a timeout.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned* err) {
+  const bool ok = __all_sync(~0u, mbar_wait_bounded(bar, parity));
+  if (!ok && (threadIdx.x & 31) == 0) {
+    flag_error(err, PA_DEV_ERR_TIMEOUT);
+    *abort_flag = 1;
+  }
+  return ok;
+}
+
+__device__ __forceinline__ bool aborted(volatile int* abort_flag) {
+  return __any_sync(~0u, *abort_flag != 0);
+}
+
+// two fp32 -> a 16-bit pair (hi) and the pair of what it left out (lo)
+template <bool kBF16>
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi,
+                                           uint32_t& lo) {
+  hi = pack2<kBF16>(a, b);
+  float ah, bh;
+  if constexpr (kBF16) {
+    ah = __uint_as_float(hi << 16);
+    bh = __uint_as_float(hi & 0xFFFF0000u);
+  } else {
+    const __half2 h = *reinterpret_cast<const __half2*>(&hi);
+    const float2 f = __half22float2(h);
+    ah = f.x;
+    bh = f.y;
+  }
+  lo = pack2<kBF16>(a - ah, b - bh);
+}
+
+template <bool kBF16>
+__global__ void __launch_bounds__(kTcThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ TcParams p) {
+  using TOut = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sp = smem_raw + (base - raw);
+  const uint32_t bars = base + TcLayout::kBars;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + TcLayout::kAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.group;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) {
+      const bool softmax_side = i == kSFree || i == kSFree + 1 || i == kPFull;
+      mbar_init(bars + 8 * i, softmax_side ? kTcRows : 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) tc_alloc<kTmemCols>(base + TcLayout::kTmemSlot);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem =
+      *reinterpret_cast<volatile uint32_t*>(sp + TcLayout::kTmemSlot);
+  pdl_launch_dependents();
+  pdl_wait();  // the planner's tile list is complete
+  const int n_atoms = min(*p.n_atoms, p.max_atoms);
+
+  if (warp == kProducerWarp) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_q);
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+    }
+    const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
+    uint32_t u = 0, qt = 0;
+    uint32_t used[2][2] = {{0, 0}, {0, 0}};  // loads issued: [K/V][stage]
+    bool go = true;
+    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+      const TcTile t = tc_tile(p, a);
+      if (!t.ok) continue;
+      if (aborted(abort_flag)) break;
+      if (qt > 0 && !warp_wait(bars + 8 * kQEmpty, (qt - 1) & 1, abort_flag, p.err))
+        break;
+      if (lane == 0) {
+        const uint32_t fb = bars + 8 * kQFull;
+        mbar_arrive_expect_tx(fb, q_bytes);
+        tma_load_3d(base + TcLayout::kQ, &tmap_q, fb, 0, t.g * G, t.q0 + t.i0);
+        tma_load_3d(base + TcLayout::kQ + kHalf, &tmap_q, fb, 64, t.g * G,
+                    t.q0 + t.i0);
+      }
+      ++qt;
+      const int32_t* bt = p.block_tables + (int64_t)t.r * p.max_blocks_per_seq;
+      for (int c = 0; c < t.nc; ++c, ++u) {
+        const int st = u & 1;
+        const uint32_t ph = (u >> 1) & 1;
+        const int pg0 = c * kTcPages;
+        const int np = min(kTcPages, t.pages - pg0);
+        int row = 0;
+        if (lane < np) {
+          int blk = __ldg(bt + pg0 + lane);
+          if (blk < 0 || blk >= p.num_blocks) {
+            flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+            blk = 0;
+          }
+          row = (blk * p.num_kv_heads + t.g) * kBS;
+        }
+        for (int kv = 0; kv < 2; ++kv) {
+          const int full = (kv ? kVFull : kKFull) + st;
+          const int empty = (kv ? kVEmpty : kKEmpty) + st;
+          if (u >= 2 && !warp_wait(bars + 8 * empty, ph ^ 1, abort_flag, p.err)) {
+            go = false;
+            break;
+          }
+          if (lane == 0)
+            mbar_arrive_expect_tx(bars + 8 * full, (uint32_t)np * 2u * kPageHalf);
+          __syncwarp();
+          if (lane < np) {
+            const uint32_t dst = base + (kv ? TcLayout::kV : TcLayout::kK) +
+                                 st * kTileBytes + lane * kPageHalf;
+            const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+            tma_load_2d(dst, map, bars + 8 * full, 0, row);
+            tma_load_2d(dst + kHalf, map, bars + 8 * full, 64, row);
+          }
+          ++used[kv][st];
+        }
+        if (!go) break;
+      }
+    }
+    // let every copy this warp issued land before the CTA may exit
+    for (int kv = 0; kv < 2; ++kv)
+      for (int st = 0; st < 2; ++st)
+        if (used[kv][st] > 0)
+          mbar_wait_bounded(bars + 8 * ((kv ? kVFull : kKFull) + st),
+                            (used[kv][st] - 1) & 1);
+    if (qt > 0) mbar_wait_bounded(bars + 8 * kQFull, (qt - 1) & 1);
+  } else if (warp == kMmaWarp) {
+    // -------------------------------- MMA ---------------------------------
+    const uint32_t q_s = base + TcLayout::kQ;
+    const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
+    auto issue_qk = [&](uint32_t uu, int c, const TcTile& t) -> bool {
+      const int st = uu & 1;
+      const uint32_t ph = (uu >> 1) & 1;
+      if (!warp_wait(bars + 8 * (kKFull + st), ph, abort_flag, p.err)) return false;
+      if (uu >= 2 &&
+          !warp_wait(bars + 8 * (kSFree + st), ph ^ 1, abort_flag, p.err))
+        return false;
+      tc_fence_after();
+      if (lane == 0) {
+        const int np = min(kTcPages, t.pages - c * kTcPages);
+        const uint32_t idesc = tc_idesc_f16(kBF16, false, kTcRows, np * kBS);
+        const uint32_t k_s = base + TcLayout::kK + st * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          tc_mma_ss(tmem + kColS + st * 128, tc_desc_sw128(q_s + off, 16, 1024),
+                    tc_desc_sw128(k_s + off, 16, 1024), idesc, kk > 0);
+        }
+        tc_commit(bars + 8 * (kSFull + st));
+        tc_commit(bars + 8 * (kKEmpty + st));
+      }
+      __syncwarp();
+      return true;
+    };
+    uint32_t u = 0, qt = 0;
+    bool go = true;
+    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+      const TcTile t = tc_tile(p, a);
+      if (!t.ok) continue;
+      if (aborted(abort_flag)) break;
+      if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
+      ++qt;
+      if (!issue_qk(u, 0, t)) break;
+      const int last = (t.L - 1) / kBS;  // page holding the last key
+      const int tail = t.L % kBS;        // its keys (0: a full page)
+      for (int c = 0; c < t.nc; ++c) {
+        const uint32_t uu = u + c;
+        const int st = uu & 1;
+        if (c + 1 < t.nc) {
+          if (!issue_qk(uu + 1, c + 1, t)) { go = false; break; }
+        } else if (lane == 0) {
+          tc_commit(bars + 8 * kQEmpty);  // Q is free once the last S is done
+        }
+        if (!warp_wait(bars + 8 * kPFull, uu & 1, abort_flag, p.err) ||
+            !warp_wait(bars + 8 * (kVFull + st), (uu >> 1) & 1, abort_flag, p.err)) {
+          go = false;
+          break;
+        }
+        tc_fence_after();
+        const int pg0 = c * kTcPages;
+        const int np = min(kTcPages, t.pages - pg0);
+        if (tail != 0 && last >= pg0 && last < pg0 + np) {
+          // V rows past the sequence end (whatever the cache holds there)
+          uint8_t* vp = sp + TcLayout::kV + st * kTileBytes + (last - pg0) * kPageHalf;
+          const int nrow = kBS - tail;
+          for (int i = lane; i < nrow * 16; i += 32) {
+            const int rr = tail + (i >> 4), ch = i & 15;
+            *reinterpret_cast<uint4*>(vp + (ch >> 3) * kHalf + rr * 128 +
+                                      (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t v_s = base + TcLayout::kV + st * kTileBytes;
+          for (int pp = 0; pp < np; ++pp) {
+            const uint64_t bv = tc_desc_sw128(v_s + pp * kPageHalf, kHalf, 1024);
+            tc_mma_ts(tmem + kColO, tmem + kColPHi + pp * 8, bv, idesc_pv,
+                      (c > 0 || pp > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + kColO, tmem + kColPLo + pp * 8, bv, idesc_pv, 1u);
+          }
+          tc_commit(bars + 8 * (kVEmpty + st));
+          tc_commit(bars + 8 * kODone);
+        }
+        __syncwarp();
+      }
+      u += t.nc;
+    }
+    // every MMA issued has completed before tensor memory is freed
+    if (lane == 0) tc_commit(bars + 8 * kMmaDone);
+    __syncwarp();
+    mbar_wait_bounded(bars + 8 * kMmaDone, 0);
+  } else {
+    // ------------------------------ softmax -------------------------------
+    const int row = threadIdx.x;  // tensor-memory lane
+    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+    const uint32_t t_s = tmem + lrow + kColS;
+    const uint32_t t_o = tmem + lrow + kColO;
+    const uint32_t t_hi = tmem + lrow + kColPHi;
+    const uint32_t t_lo = tmem + lrow + kColPLo;
+    const int it = row / G, jh = row - it * G;
+    uint32_t u = 0;
+    bool go = true;
+    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+      const TcTile t = tc_tile(p, a);
+      if (!t.ok) continue;
+      if (aborted(abort_flag)) break;
+      // rows past the tile's tokens compute on the tile's last limit and are
+      // never stored
+      const bool valid = it < t.ntok;
+      const int lim = t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
+      float m_ref = -INFINITY, l = 0.f;
+      for (int c = 0; c < t.nc; ++c) {
+        const uint32_t uu = u + c;
+        const int st = uu & 1;
+        if (!warp_wait(bars + 8 * (kSFull + st), (uu >> 1) & 1, abort_flag, p.err)) {
+          go = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tc_ld32(t_s + st * 128 + j * 32, sr[j]);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bars + 8 * (kSFree + st));
+        const int vis = lim - c * kTcKeys;  // columns 0 .. vis are visible
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const float x = j <= vis ? __uint_as_float(sr[j >> 5][j & 31]) * p.score_scale
+                                   : -INFINITY;
+          sr[j >> 5][j & 31] = __float_as_uint(x);
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_ref, mx);
+        if (c > 0) {
+          // the previous P.V is done: P may be overwritten, O is stable
+          if (!warp_wait(bars + 8 * kODone, (uu - 1) & 1, abort_flag, p.err)) {
+            go = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const bool grow = m_new > m_ref + kRescaleLog2;
+        const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
+        if (c > 0 && __any_sync(~0u, grow)) {
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint32_t o[32];
+            tc_ld32(t_o + j * 32, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tc_st32(t_o + j * 32, o);
+          }
+          tc_wait_st();
+        }
+        if (grow) {
+          l *= alpha;
+          m_ref = m_new;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float p0 = exp2f(__uint_as_float(sr[j][2 * k]) - m_ref);
+            const float p1 = exp2f(__uint_as_float(sr[j][2 * k + 1]) - m_ref);
+            l += p0 + p1;
+            split_pair<kBF16>(p0, p1, hi[k], lo[k]);
+          }
+          tc_st16(t_hi + j * 16, hi);
+          tc_st16(t_lo + j * 16, lo);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(bars + 8 * kPFull);
+      }
+      if (!go) break;
+      if (!warp_wait(bars + 8 * kODone, (u + t.nc - 1) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const float inv = 1.f / l;
+      TOut* o = static_cast<TOut*>(p.out) +
+                ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128;
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[32];
+        tc_ld32(t_o + j * 32, v);
+        tc_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            pk[k] = pack2<kBF16>(__uint_as_float(v[2 * k]) * inv,
+                                 __uint_as_float(v[2 * k + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(o + j * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      tc_fence_before();
+      u += t.nc;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tc_dealloc<kTmemCols>(tmem);
+  }
+}
+
+template <bool kBF16>
+cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
+                      cudaStream_t stream) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             TcLayout::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcLayout::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kBF16>, m.q, m.k, m.v, p);
+}
+
+}  // namespace
+
+bool tc_prefill_supported(const AttnArgs& a) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  return a.head_dim == 128 && G >= 1 && G <= kTcRows &&
+         (a.cache_dtype == PA_BF16 || a.cache_dtype == PA_F16) &&
+         a.q_dtype == a.cache_dtype;
+}
+
+int tc_prefill_tile_rows(int group) { return (kTcRows / group) * group; }
+
+cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
+                              const int4* atoms, const int* n_atoms,
+                              int max_atoms, int num_sms, cudaStream_t stream) {
+  TcParams p{};
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.query_start_loc;
+  p.atoms = atoms;
+  p.n_atoms = n_atoms;
+  p.max_atoms = max_atoms;
+  p.err = a.err;
+  p.num_tokens = a.num_tokens;
+  p.num_blocks = a.num_blocks;
+  p.max_blocks_per_seq = a.max_blocks_per_seq;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.group = a.num_q_heads / a.num_kv_heads;
+  p.max_query_len = a.max_query_len;
+  p.max_seq_len = a.max_seq_len;
+  p.tokens_per_tile = kTcRows / p.group;
+  p.score_scale = a.scale * 1.4426950408889634f;
+  int grid = max_atoms < num_sms ? max_atoms : num_sms;
+  if (grid < 1) grid = 1;
+  return a.cache_dtype == PA_BF16 ? launch_tc<true>(p, maps, grid, stream)
+                                  : launch_tc<false>(p, maps, grid, stream);
+}
+
+}  // namespace pa

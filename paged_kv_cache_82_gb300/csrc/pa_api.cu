@@ -150,6 +150,41 @@ bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
   return true;
 }
 
+bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* m) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || a.head_dim != 128) return false;
+  const int G = a.num_q_heads / a.num_kv_heads;
+  const cuuint32_t tp = (cuuint32_t)(128 / G);
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const cuuint32_t es[3] = {1, 1, 1};
+  // q [token][head][128]: a box is 64 columns of G heads of 128/G tokens
+  {
+    cuuint64_t dims[3] = {128, (cuuint64_t)a.num_q_heads, (cuuint64_t)a.num_tokens};
+    cuuint64_t strides[2] = {256, (cuuint64_t)a.num_q_heads * 256};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, tp};
+    if (fn(&m->q, dt, 3, const_cast<void*>(a.q), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  // caches [row][128]: a box is 64 columns of one 16-row page
+  const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.num_kv_heads * PA_BLOCK_SIZE;
+  const void* ptrs[2] = {a.k_cache, a.v_cache};
+  CUtensorMap* maps[2] = {&m->k, &m->v};
+  for (int k = 0; k < 2; ++k) {
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {64, PA_BLOCK_SIZE};
+    if (fn(maps[k], dt, 2, const_cast<void*>(ptrs[k]), dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -354,7 +389,13 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
   if (fast) {
     CUtensorMap tk, tv;
     if (!encode_cache_tensor_maps(a, &tk, &tv)) return PA_ERR_CUDA;
-    e = launch_attention_fast(a, plan, tk, tv, s);
+    // prefill tiles go to the tensor-core kernel where it takes the step's
+    // types (else the attention kernel runs them on the warp-level MMA)
+    TcMaps tc;
+    const bool use_tc = plan.has_prefill && tc_prefill_supported(a) &&
+                        encode_prefill_tensor_maps(a, &tc);
+    e = launch_attention_fast(a, plan, tk, tv, use_tc ? &tc : nullptr,
+                              di->num_sms, s);
   } else {
     e = launch_attention_generic(a, s);
   }

@@ -148,6 +148,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
 }
 
 // ----------------------------------------------------------------------------
+// programmatic dependent launch: let the next grid in the stream start its
+// prologue; wait until the previous grid has completed and its writes are
+// visible
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor) loads into shared memory, completing on an
 // mbarrier.  Coordinates are element indices, innermost first.
 // ----------------------------------------------------------------------------

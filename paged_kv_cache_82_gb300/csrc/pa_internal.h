@@ -51,7 +51,8 @@ struct AttnPlan {
   // workspace carve-up (byte offsets, 256-aligned)
   size_t off_atoms, off_atom_start, off_req_dec0, off_req_declen, off_req_rows,
       off_items,
-      off_cta_begin, off_seg_info, off_split, off_acc, off_ml, total_bytes;
+      off_cta_begin, off_seg_info, off_split, off_pref, off_acc, off_ml,
+      total_bytes;
 };
 
 // Host planning from host-known sizes only (no device read-back).
@@ -90,11 +91,27 @@ struct ProfileEvents {
 };
 ProfileEvents& profile_events();  // thread-local
 
-// plan kernel + main kernel + split merge (fast path)
+// tensor maps of the tensor-core prefill kernel: q as [token][head][dim],
+// each cache as [row][dim] with 64-column boxes of one page
+struct TcMaps {
+  CUtensorMap q, k, v;
+};
+
+// true if the tensor-core kernel can take the prefill tiles of such a step
+bool tc_prefill_supported(const AttnArgs& a);
+// query rows of one of its tiles (128 / group tokens x group heads)
+int tc_prefill_tile_rows(int group);
+bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
+// prefill tiles listed by the planner, one persistent CTA per SM
+cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
+                              const int4* atoms, const int* n_atoms,
+                              int max_atoms, int num_sms, cudaStream_t stream);
+
+// plan kernel + (tensor-core prefill kernel) + main kernel + split merge
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
                                   const CUtensorMap& tmap_k,
-                                  const CUtensorMap& tmap_v,
-                                  cudaStream_t stream);
+                                  const CUtensorMap& tmap_v, const TcMaps* tc,
+                                  int num_sms, cudaStream_t stream);
 
 // warp-per-row kernel for the remaining types / shapes
 cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream);

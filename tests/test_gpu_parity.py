@@ -181,6 +181,27 @@ def test_query_shapes(Hq, Hkv, seq_q):
     _check_step(_custom(seq_q, Hq, Hkv, write_new=True))
 
 
+@pytest.mark.parametrize("Hq,Hkv,seq_q,dtype", [
+    (12, 4, [(1500, 300), (200, 1)], "bf16"),   # group 3: 126-row tiles
+    (32, 8, [(3022, 1022), (90, 1)], "bf16"),   # a 1022-token chunk
+    (8, 8, [(900, 257)], "f16"),                # MHA: 128-token tiles, f16
+    (64, 4, [(650, 90), (77, 77)], "bf16"),     # group 16: 8-token tiles
+])
+def test_prefill_tiles(Hq, Hkv, seq_q, dtype):
+    # bf16 / f16 prefill tiles run on the tensor-core kernel: several tiles
+    # per request, several 128-key chunks, a partial last page (its free
+    # slots hold NaN) and a prefill next to decodes
+    _check_step(_custom(seq_q, Hq, Hkv, dtype=dtype, write_new=True))
+
+
+def test_prefill_row_max_growing_across_chunks():
+    # with scores 11x larger than 1/sqrt(D) gives, row maxima keep growing
+    # from chunk to chunk, so the running output is rescaled many times
+    wl = _custom([(2000, 700), (50, 1)], 32, 8, write_new=True)
+    wl.scale = 1.0
+    _check_step(wl)
+
+
 def test_f16_and_fp8_f16_query():
     _check_step(_custom([(333, 1), (64, 7)], 32, 8, dtype="f16",
                         write_new=True))
