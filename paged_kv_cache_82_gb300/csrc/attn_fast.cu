@@ -312,7 +312,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
   }
   if (threadIdx.x == 0) {
     s_atoms = run_atoms < pa.max_atoms ? run_atoms : pa.max_atoms;
-    if (pa.prefill_tc) *pa.n_atoms_out = (int)s_atoms;
+    if (pa.prefill_tc) {
+      pa.n_atoms_out[0] = (int)s_atoms;
+      pa.n_atoms_out[1] = 0;  // tiles handed out by the tensor-core kernel
+    }
     s_cost_pre = run_pcost;
     s_dec_total = run_dec;
   }
@@ -1822,8 +1825,8 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   if (pe.start) cudaEventRecord(pe.start, stream);
   if (tc) {
     // prefill tiles on the tensor cores, ahead of the decode work
-    e = launch_prefill_tc(a, *tc, pa.atoms, pa.n_atoms_out, pa.max_atoms,
-                          num_sms, stream);
+    e = launch_prefill_tc(a, *tc, pa.atoms, pa.n_atoms_out,
+                          pa.n_atoms_out + 1, pa.max_atoms, num_sms, stream);
     if (e != cudaSuccess) return e;
   }
   if (wide) {

@@ -13,19 +13,23 @@
 // How (one CTA per SM, persistent over the step's prefill tiles):
 //  * A tile is 128 query rows of one (request, KV head): 128 / G consecutive
 //    tokens times the G q heads of the group, row = token * G + head.  Keys
-//    go in chunks of 128 (8 pages).
+//    go in chunks of 128 (8 pages).  The producer warp draws tiles from a
+//    step-wide counter, longest first, and passes each tile's index to the
+//    other warps through a two-slot ring in shared memory.
 //  * warp 4 (TMA producer): the Q tile through a 3-D map over q
 //    [token][head][dim], and for every chunk its pages of K and of V through
 //    a 2-D map over the cache rows, each page as two 64-column halves under
 //    the 128-byte swizzle, into a two-deep ring.  The same shared-memory
 //    layout serves as the K-major B operand of Q.K^T and as the MN-major B
 //    operand of P.V.
-//  * warp 5 (MMA): allocates tensor memory (512 columns: two S buffers, O,
-//    P) and issues, from one lane, S = Q.K^T (M 128, N = 16 x pages of the
+//  * warp 5 (MMA): allocates tensor memory (512 columns: three S buffers and
+//    O) and issues, from one lane, S = Q.K^T (M 128, N = 16 x pages of the
 //    chunk, K 128) into the S buffer of the chunk, and O += P.V with P read
-//    from tensor memory.  P goes in two bf16 (or f16) parts, P = hi + lo, so
-//    that the rounding of the probabilities to 16 bits costs no accuracy.
-//    Completion is tracked with tcgen05.commit on mbarriers.
+//    from tensor memory, where the softmax wrote it over that chunk's S.  P
+//    goes in two 16-bit parts, P = hi + lo, so that the rounding of the
+//    probabilities to 16 bits costs no accuracy.  Completion is tracked with
+//    tcgen05.commit on mbarriers; with three buffers the softmax of one chunk
+//    overlaps the MMAs of its neighbours.
 //  * warps 0-3 (softmax): one thread per query row.  Each chunk: S from
 //    tensor memory, scale and causal mask, online softmax against a
 //    reference max that only moves when the row max has grown by more than
@@ -59,31 +63,47 @@ constexpr int kHalf = 128 * 128;           // 128 rows x 128 B: one column half
 constexpr int kTileBytes = 2 * kHalf;      // 128 rows x 128 columns, 16-bit
 constexpr int kPageHalf = kBS * 128;       // one page, one column half
 constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (log2)
+#ifndef PA_TC_KV_STAGES
+#define PA_TC_KV_STAGES 2
+#endif
+constexpr int kKvStages = PA_TC_KV_STAGES;  // ring depth, chunks of K and of V
+constexpr int kSBufs = 3;                   // S / P buffers in tensor memory
 
-// tensor-memory columns
+// Tensor memory: three S buffers of 128 columns; the softmax overwrites each
+// with its P (per 16-key MMA step, 8 columns of hi parts then 8 of lo parts),
+// which the P.V of the chunk then reads; O after them.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S buffers at 0 and 128
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColPHi = 384;
-constexpr uint32_t kColPLo = 448;
+constexpr uint32_t kColO = 384;
 
 // barriers
 enum : int {
-  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kVFull = 6, kVEmpty = 8,
-  kSFull = 10, kSFree = 12, kPFull = 14, kODone = 15, kMmaDone = 16,
-  kNumBars = 17
+  kQFull = 0,
+  kQEmpty = 1,
+  kKFull = 2,
+  kKEmpty = kKFull + kKvStages,
+  kVFull = kKEmpty + kKvStages,
+  kVEmpty = kVFull + kKvStages,
+  kSFull = kVEmpty + kKvStages,      // S of the buffer written
+  kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
+  kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
+  kTileFull = kPvDone + kSBufs,      // tile index slot filled
+  kTileEmpty = kTileFull + 2,        // tile index slot read (5 warps)
+  kMmaDone = kTileEmpty + 2,
+  kNumBars = kMmaDone + 1
 };
 
 struct TcLayout {
-  static constexpr int kK = 0;                       // 2 K stages
-  static constexpr int kV = kK + 2 * kTileBytes;     // 2 V stages
-  static constexpr int kQ = kV + 2 * kTileBytes;     // Q tile
+  static constexpr int kK = 0;                               // K stages
+  static constexpr int kV = kK + kKvStages * kTileBytes;     // V stages
+  static constexpr int kQ = kV + kKvStages * kTileBytes;     // Q tile
   static constexpr int kBars = kQ + kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kTileSlot = kAbort + 4;               // int[2]
+  static constexpr int kBytes = kTileSlot + 8;
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
+static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct TcParams {
   void* out;
@@ -92,6 +112,7 @@ struct TcParams {
   const int32_t* qsl;
   const int4* atoms;     // prefill tiles {r, g, tile, pages} from the planner
   const int* n_atoms;
+  int* tile_ctr;         // tiles handed out so far (zeroed by the planner)
   int max_atoms;
   unsigned* err;
   int64_t num_tokens;
@@ -143,26 +164,44 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
   return ok;
 }
 
-__device__ __forceinline__ bool aborted(volatile int* abort_flag) {
-  return __any_sync(~0u, *abort_flag != 0);
+// The next tile of a consumer warp: index slot q % 2 once the producer has
+// filled it; the warp then hands the slot back.  -1: no more tiles.
+__device__ __forceinline__ int next_tile(uint32_t bars, volatile int* slots,
+                                         uint32_t q, volatile int* abort_flag,
+                                         unsigned* err) {
+  const int s = q & 1;
+  if (!warp_wait(bars + 8 * (kTileFull + s), (q >> 1) & 1, abort_flag, err))
+    return -1;
+  const int a = slots[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
+  return a;
 }
 
-// two fp32 -> a 16-bit pair (hi) and the pair of what it left out (lo)
+// Probabilities as two 16-bit parts each, p = hi + lo + O(2^-16 p): for bf16
+// hi keeps the top half of the fp32 bits (truncation, exact) and lo is the
+// rest rounded to nearest; for f16 both parts are rounded to nearest.
 template <bool kBF16>
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi,
                                            uint32_t& lo) {
-  hi = pack2<kBF16>(a, b);
-  float ah, bh;
   if constexpr (kBF16) {
-    ah = __uint_as_float(hi << 16);
-    bh = __uint_as_float(hi & 0xFFFF0000u);
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    hi = __byte_perm(ua, ub, 0x7632);
+    lo = pack2<true>(a - __uint_as_float(ua & 0xFFFF0000u),
+                     b - __uint_as_float(ub & 0xFFFF0000u));
   } else {
-    const __half2 h = *reinterpret_cast<const __half2*>(&hi);
-    const float2 f = __half22float2(h);
-    ah = f.x;
-    bh = f.y;
+    hi = pack2<false>(a, b);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+    lo = pack2<false>(a - f.x, b - f.y);
   }
-  lo = pack2<kBF16>(a - ah, b - bh);
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; results
+// below 2^-126 flush to zero, which a softmax weight next to l >= 1 is)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <bool kBF16>
@@ -178,13 +217,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* const sp = smem_raw + (base - raw);
   const uint32_t bars = base + TcLayout::kBars;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + TcLayout::kAbort);
+  volatile int* slots = reinterpret_cast<volatile int*>(sp + TcLayout::kTileSlot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool softmax_side = i == kSFree || i == kSFree + 1 || i == kPFull;
-      mbar_init(bars + 8 * i, softmax_side ? kTcRows : 1);
+      uint32_t count = 1;
+      if (i >= kPFull && i < kPFull + kSBufs) count = kTcRows;
+      if (i == kTileEmpty || i == kTileEmpty + 1) count = 5;
+      mbar_init(bars + 8 * i, count);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -207,13 +249,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tma_prefetch_desc(&tmap_v);
     }
     const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
-    uint32_t u = 0, qt = 0;
-    uint32_t used[2][2] = {{0, 0}, {0, 0}};  // loads issued: [K/V][stage]
+    uint32_t u = 0, qt = 0, q = 0;
+    uint32_t used[2][kKvStages] = {};  // loads issued: [K/V][stage]
     bool go = true;
-    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+    while (go) {
+      // hand out the next tile, longest first (the planner lists a request's
+      // tiles in causal order)
+      const int s = q & 1;
+      if (q >= 2 &&
+          !warp_wait(bars + 8 * (kTileEmpty + s), ((q >> 1) - 1) & 1, abort_flag, p.err))
+        break;
+      int a = -1;
+      if (lane == 0) {
+        const int ticket = *abort_flag ? n_atoms : atomicAdd(p.tile_ctr, 1);
+        a = ticket < n_atoms ? n_atoms - 1 - ticket : -1;
+        slots[s] = a;
+        mbar_arrive(bars + 8 * (kTileFull + s));
+      }
+      a = __shfl_sync(~0u, a, 0);
+      ++q;
+      if (a < 0) break;
       const TcTile t = tc_tile(p, a);
       if (!t.ok) continue;
-      if (aborted(abort_flag)) break;
       if (qt > 0 && !warp_wait(bars + 8 * kQEmpty, (qt - 1) & 1, abort_flag, p.err))
         break;
       if (lane == 0) {
@@ -225,9 +282,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       ++qt;
       const int32_t* bt = p.block_tables + (int64_t)t.r * p.max_blocks_per_seq;
-      for (int c = 0; c < t.nc; ++c, ++u) {
-        const int st = u & 1;
-        const uint32_t ph = (u >> 1) & 1;
+      for (int c = 0; c < t.nc && go; ++c, ++u) {
+        const int st = u % kKvStages;
+        const uint32_t ph = (u / kKvStages) & 1;
         const int pg0 = c * kTcPages;
         const int np = min(kTcPages, t.pages - pg0);
         int row = 0;
@@ -242,7 +299,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         for (int kv = 0; kv < 2; ++kv) {
           const int full = (kv ? kVFull : kKFull) + st;
           const int empty = (kv ? kVEmpty : kKEmpty) + st;
-          if (u >= 2 && !warp_wait(bars + 8 * empty, ph ^ 1, abort_flag, p.err)) {
+          if (u >= kKvStages &&
+              !warp_wait(bars + 8 * empty, ph ^ 1, abort_flag, p.err)) {
             go = false;
             break;
           }
@@ -258,12 +316,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           ++used[kv][st];
         }
-        if (!go) break;
       }
     }
     // let every copy this warp issued land before the CTA may exit
     for (int kv = 0; kv < 2; ++kv)
-      for (int st = 0; st < 2; ++st)
+      for (int st = 0; st < kKvStages; ++st)
         if (used[kv][st] > 0)
           mbar_wait_bounded(bars + 8 * ((kv ? kVFull : kKFull) + st),
                             (used[kv][st] - 1) & 1);
@@ -272,12 +329,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // -------------------------------- MMA ---------------------------------
     const uint32_t q_s = base + TcLayout::kQ;
     const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
+    // S of chunk uu (chunk c of tile t) into buffer uu % 3, once the P.V
+    // that last read that buffer has completed
     auto issue_qk = [&](uint32_t uu, int c, const TcTile& t) -> bool {
-      const int st = uu & 1;
-      const uint32_t ph = (uu >> 1) & 1;
-      if (!warp_wait(bars + 8 * (kKFull + st), ph, abort_flag, p.err)) return false;
-      if (uu >= 2 &&
-          !warp_wait(bars + 8 * (kSFree + st), ph ^ 1, abort_flag, p.err))
+      const int st = uu % kKvStages;
+      const int b = uu % kSBufs;
+      if (!warp_wait(bars + 8 * (kKFull + st), (uu / kKvStages) & 1, abort_flag, p.err))
+        return false;
+      if (uu >= kSBufs &&
+          !warp_wait(bars + 8 * (kPvDone + b), ((uu / kSBufs) - 1) & 1, abort_flag, p.err))
         return false;
       tc_fence_after();
       if (lane == 0) {
@@ -287,36 +347,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc_mma_ss(tmem + kColS + st * 128, tc_desc_sw128(q_s + off, 16, 1024),
+          tc_mma_ss(tmem + b * 128, tc_desc_sw128(q_s + off, 16, 1024),
                     tc_desc_sw128(k_s + off, 16, 1024), idesc, kk > 0);
         }
-        tc_commit(bars + 8 * (kSFull + st));
+        tc_commit(bars + 8 * (kSFull + b));
         tc_commit(bars + 8 * (kKEmpty + st));
       }
       __syncwarp();
       return true;
     };
     uint32_t u = 0, qt = 0;
-    bool go = true;
-    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+    for (uint32_t q = 0;; ++q) {
+      const int a = next_tile(bars, slots, q, abort_flag, p.err);
+      if (a < 0) break;
       const TcTile t = tc_tile(p, a);
       if (!t.ok) continue;
-      if (aborted(abort_flag)) break;
       if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
       ++qt;
       if (!issue_qk(u, 0, t)) break;
       const int last = (t.L - 1) / kBS;  // page holding the last key
       const int tail = t.L % kBS;        // its keys (0: a full page)
+      bool go = true;
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
-        const int st = uu & 1;
+        const int st = uu % kKvStages;
+        const int b = uu % kSBufs;
         if (c + 1 < t.nc) {
           if (!issue_qk(uu + 1, c + 1, t)) { go = false; break; }
         } else if (lane == 0) {
           tc_commit(bars + 8 * kQEmpty);  // Q is free once the last S is done
         }
-        if (!warp_wait(bars + 8 * kPFull, uu & 1, abort_flag, p.err) ||
-            !warp_wait(bars + 8 * (kVFull + st), (uu >> 1) & 1, abort_flag, p.err)) {
+        if (!warp_wait(bars + 8 * (kPFull + b), (uu / kSBufs) & 1, abort_flag, p.err) ||
+            !warp_wait(bars + 8 * (kVFull + st), (uu / kKvStages) & 1, abort_flag, p.err)) {
           go = false;
           break;
         }
@@ -337,17 +399,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         __syncwarp();
         if (lane == 0) {
           const uint32_t v_s = base + TcLayout::kV + st * kTileBytes;
+          const uint32_t t_p = tmem + b * 128;
           for (int pp = 0; pp < np; ++pp) {
             const uint64_t bv = tc_desc_sw128(v_s + pp * kPageHalf, kHalf, 1024);
-            tc_mma_ts(tmem + kColO, tmem + kColPHi + pp * 8, bv, idesc_pv,
+            tc_mma_ts(tmem + kColO, t_p + pp * 16, bv, idesc_pv,
                       (c > 0 || pp > 0) ? 1u : 0u);
-            tc_mma_ts(tmem + kColO, tmem + kColPLo + pp * 8, bv, idesc_pv, 1u);
+            tc_mma_ts(tmem + kColO, t_p + pp * 16 + 8, bv, idesc_pv, 1u);
           }
           tc_commit(bars + 8 * (kVEmpty + st));
-          tc_commit(bars + 8 * kODone);
+          tc_commit(bars + 8 * (kPvDone + b));
         }
         __syncwarp();
       }
+      if (!go) break;
       u += t.nc;
     }
     // every MMA issued has completed before tensor memory is freed
@@ -358,62 +422,67 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // ------------------------------ softmax -------------------------------
     const int row = threadIdx.x;  // tensor-memory lane
     const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_s = tmem + lrow + kColS;
     const uint32_t t_o = tmem + lrow + kColO;
-    const uint32_t t_hi = tmem + lrow + kColPHi;
-    const uint32_t t_lo = tmem + lrow + kColPLo;
     const int it = row / G, jh = row - it * G;
     uint32_t u = 0;
-    bool go = true;
-    for (int a = blockIdx.x; a < n_atoms && go; a += gridDim.x) {
+    for (uint32_t q = 0;; ++q) {
+      const int a = next_tile(bars, slots, q, abort_flag, p.err);
+      if (a < 0) break;
       const TcTile t = tc_tile(p, a);
       if (!t.ok) continue;
-      if (aborted(abort_flag)) break;
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
       const bool valid = it < t.ntok;
       const int lim = t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
       float m_ref = -INFINITY, l = 0.f;
+      bool go = true;
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
-        const int st = uu & 1;
-        if (!warp_wait(bars + 8 * (kSFull + st), (uu >> 1) & 1, abort_flag, p.err)) {
+        const int b = uu % kSBufs;
+        const uint32_t t_b = tmem + lrow + b * 128;
+        if (!warp_wait(bars + 8 * (kSFull + b), (uu / kSBufs) & 1, abort_flag, p.err)) {
           go = false;
           break;
         }
         tc_fence_after();
         uint32_t sr[4][32];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tc_ld32(t_s + st * 128 + j * 32, sr[j]);
-        tc_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bars + 8 * (kSFree + st));
+        for (int j = 0; j < 4; ++j) tc_ld32(t_b + j * 32, sr[j]);
+        tc_wait_ld_dep(sr);
+        // row max of the raw scores (the scale is positive); keys past the
+        // row's limit (only in chunks that reach the diagonal) become -inf
         const int vis = lim - c * kTcKeys;  // columns 0 .. vis are visible
-        float mx = -INFINITY;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (__any_sync(~0u, vis < kTcKeys - 1)) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float x = j <= vis ? __uint_as_float(sr[j >> 5][j & 31]) * p.score_scale
-                                   : -INFINITY;
-          sr[j >> 5][j & 31] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          for (int j = 0; j < 128; ++j) {
+            const float x = j <= vis ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
+            sr[j >> 5][j & 31] = __float_as_uint(x);
+            mx4[j & 3] = fmaxf(mx4[j & 3], x);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 128; ++j)
+            mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
         }
-        const float m_new = fmaxf(m_ref, mx);
-        if (c > 0) {
-          // the previous P.V is done: P may be overwritten, O is stable
-          if (!warp_wait(bars + 8 * kODone, (uu - 1) & 1, abort_flag, p.err)) {
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float m_new = fmaxf(m_ref, mx * p.score_scale);
+        const bool grow = m_new > m_ref + kRescaleLog2;
+        const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
+        if (c > 0 && __any_sync(~0u, grow)) {
+          // O is stable once the previous chunk's P.V has completed
+          const uint32_t up = uu - 1;
+          if (!warp_wait(bars + 8 * (kPvDone + up % kSBufs), (up / kSBufs) & 1,
+                         abort_flag, p.err)) {
             go = false;
             break;
           }
           tc_fence_after();
-        }
-        const bool grow = m_new > m_ref + kRescaleLog2;
-        const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
-        if (c > 0 && __any_sync(~0u, grow)) {
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
             uint32_t o[32];
             tc_ld32(t_o + j * 32, o);
-            tc_wait_ld();
+            tc_wait_ld_dep(o);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
@@ -425,25 +494,34 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           l *= alpha;
           m_ref = m_new;
         }
+        // P = 2^(s * scale - m_ref) over the S just read, in place: the 16
+        // keys of MMA step k take columns 16k .. 16k+7 (hi parts) and
+        // 16k+8 .. 16k+15 (lo parts), key pairs packed low key first
+        const float neg_m = -m_ref;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t hi[16], lo[16];
+          uint32_t w[32];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = exp2f(__uint_as_float(sr[j][2 * k]) - m_ref);
-            const float p1 = exp2f(__uint_as_float(sr[j][2 * k + 1]) - m_ref);
-            l += p0 + p1;
-            split_pair<kBF16>(p0, p1, hi[k], lo[k]);
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j][2 * k]), p.score_scale, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j][2 * k + 1]), p.score_scale, neg_m));
+            l4[k & 3] += p0 + p1;
+            const int slot = (k >> 3) * 16 + (k & 7);  // hi at slot, lo at slot + 8
+            split_pair<kBF16>(p0, p1, w[slot], w[slot + 8]);
           }
-          tc_st16(t_hi + j * 16, hi);
-          tc_st16(t_lo + j * 16, lo);
+          tc_st32(t_b + j * 32, w);
         }
+        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         tc_wait_st();
         tc_fence_before();
-        mbar_arrive(bars + 8 * kPFull);
+        mbar_arrive(bars + 8 * (kPFull + b));
       }
       if (!go) break;
-      if (!warp_wait(bars + 8 * kODone, (u + t.nc - 1) & 1, abort_flag, p.err)) break;
+      const uint32_t ul = u + t.nc - 1;
+      if (!warp_wait(bars + 8 * (kPvDone + ul % kSBufs), (ul / kSBufs) & 1,
+                     abort_flag, p.err))
+        break;
       tc_fence_after();
       const float inv = 1.f / l;
       TOut* o = static_cast<TOut*>(p.out) +
@@ -452,7 +530,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
         tc_ld32(t_o + j * 32, v);
-        tc_wait_ld();
+        tc_wait_ld_dep(v);
         if (valid) {
           uint32_t pk[16];
 #pragma unroll
@@ -509,7 +587,8 @@ cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
 
 bool tc_prefill_supported(const AttnArgs& a) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  return a.head_dim == 128 && G >= 1 && G <= kTcRows &&
+  // (the row max is taken on raw scores: the scale must be positive)
+  return a.head_dim == 128 && G >= 1 && G <= kTcRows && a.scale > 0.f &&
          (a.cache_dtype == PA_BF16 || a.cache_dtype == PA_F16) &&
          a.q_dtype == a.cache_dtype;
 }
@@ -518,7 +597,8 @@ int tc_prefill_tile_rows(int group) { return (kTcRows / group) * group; }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               const int4* atoms, const int* n_atoms,
-                              int max_atoms, int num_sms, cudaStream_t stream) {
+                              int* tile_ctr, int max_atoms, int num_sms,
+                              cudaStream_t stream) {
   TcParams p{};
   p.out = a.out;
   p.block_tables = a.block_tables;
@@ -526,6 +606,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
   p.qsl = a.query_start_loc;
   p.atoms = atoms;
   p.n_atoms = n_atoms;
+  p.tile_ctr = tile_ctr;
   p.max_atoms = max_atoms;
   p.err = a.err;
   p.num_tokens = a.num_tokens;

@@ -102,10 +102,12 @@ bool tc_prefill_supported(const AttnArgs& a);
 // query rows of one of its tiles (128 / group tokens x group heads)
 int tc_prefill_tile_rows(int group);
 bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
-// prefill tiles listed by the planner, one persistent CTA per SM
+// prefill tiles listed by the planner (n_atoms of them; tile_ctr zeroed),
+// one persistent CTA per SM
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               const int4* atoms, const int* n_atoms,
-                              int max_atoms, int num_sms, cudaStream_t stream);
+                              int* tile_ctr, int max_atoms, int num_sms,
+                              cudaStream_t stream);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
