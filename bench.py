@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 METRIC = "paged-attn decode HBM TB/s (fraction of peak); mixed-step tokens/s"
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def _peaks():
@@ -43,6 +44,18 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def _tensor_peak():
+    """Dense bf16 tensor peak (burst figure: the prefill kernel is timed in
+    isolation), measured on this machine, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def _dist():
@@ -140,21 +153,20 @@ def _device_inputs(wl, dev):
 
 def _step(pa, wl, d):
     """One pass of the hot path over the step: copy-on-write copies, K/V
-    writes, attention.  Returns the number of our kernel launches."""
-    launches = 0
+    writes, attention.  Returns the number of our kernel launches (the
+    library's own count)."""
+    n0 = pa.pa_launch_count()
     if wl.copy_pairs:
         pa.pa_copy_blocks(d["kc"], d["vc"], d["pairs"])
-        launches += 1
     if wl.write_new:
         pa.pa_reshape_and_cache(d["key"], d["value"], d["kc"], d["vc"],
                                 d["slots"], k_scale=wl.k_scale,
                                 v_scale=wl.v_scale)
-        launches += 1
     md = d["md"]
     pa.pa_attention(d["q"], d["kc"], d["vc"], d["bt"], d["sl"], d["qsl"],
                     md["max_query_len"], md["max_seq_len"], wl.scale,
                     wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"])
-    return launches + 3   # plan, main, split merge
+    return pa.pa_launch_count() - n0
 
 
 def _time_steps(pa, wl, d, steps, warmup, flush):
@@ -307,16 +319,18 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     if args.only != "all":
-        wl = workloads.config2() if args.only == "decode" else \
-            workloads.config4()
+        wl = {"decode": workloads.config2, "mixed": workloads.config4,
+              "prefill": workloads.prefill_chunk}[args.only]()
         d = _device_inputs(wl, dev)
         step_ms, kern_ms, _ = _time_steps(pa, wl, d, args.steps, args.warmup,
                                           flush)
         flags = pa.pa_get_device_error()
         byts = wl.kv_bytes() + wl.qo_bytes()
-        print(f"{args.only}: step {statistics.mean(step_ms):.4f} ms, main "
-              f"kernel {statistics.mean(kern_ms):.4f} ms, "
-              f"{byts / statistics.mean(kern_ms) / 1e9:.3f} TB/s kernel, "
+        km = statistics.mean(kern_ms)
+        print(f"{args.only}: step {statistics.mean(step_ms):.4f} ms, "
+              f"attention kernels {km:.4f} ms, "
+              f"{byts / km / 1e9:.3f} TB/s, "
+              f"{workloads.attention_flops(wl) / km / 1e9:.1f} TFLOP/s, "
               f"flags 0x{flags:x}")
         if flags:
             raise SystemExit(2)
@@ -384,9 +398,32 @@ def run_ours(args):
             wl4.kv_bytes(unique=False),
         "hbm_tbs": m_bytes / (m_ms * 1e-3) / 1e12,
         "frac_of_measured_hbm": m_bytes / (m_ms * 1e-3) / 1e9 / peak_gbs,
-        "attention_kernel_ms": statistics.mean(m_kern),
+        "attention_kernels_ms": statistics.mean(m_kern),
     }
     del d4
+
+    # ---- prefill tiles alone: one long chunked prefill (tensor cores)
+    wlp = workloads.prefill_chunk()
+    dp = _device_inputs(wlp, dev)
+    p_step, p_kern, _ = _time_steps(pa, wlp, dp, args.steps, args.warmup,
+                                    flush)
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x} (prefill step)")
+    p_km = statistics.mean(p_kern)
+    p_tflops = workloads.attention_flops(wlp) / (p_km * 1e-3) / 1e12
+    bf16_peak, bf16_kind = _tensor_peak()
+    prefill = {
+        "workload": ("Llama-3.1-8B shape, bf16: one request, 4096-token "
+                     "chunk after 4096 cached tokens (causal)"),
+        "kernel": "prefill_tc_kernel (bf16, tcgen05) + the empty decode launch",
+        "bound": "tensor", "achieved": p_tflops, "peak": bf16_peak,
+        "unit": "TFLOP/s", "frac": p_tflops / bf16_peak,
+        "peak_kind": bf16_kind, "kernels_ms": p_km,
+        "ms_per_step": statistics.mean(p_step),
+        "flops": workloads.attention_flops(wlp),
+    }
+    del dp
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -423,6 +460,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clocks,
         "mixed_step": mixed,
+        "prefill_step": prefill,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -479,7 +517,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "mixed"],
+    ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill"],
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
                          "line")

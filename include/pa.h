@@ -267,13 +267,24 @@ pa_status pa_attention_noalloc(const void* q, pa_dtype q_dtype,
 /*
  * pa_set_profile_events -- measurement hook (no counterpart on the pages).
  * When both events are non-NULL, every later pa_attention call on this
- * thread records `start` on its stream immediately before the launch of the
- * main attention kernel and `stop` immediately after it, so that
- * cudaEventElapsedTime gives that kernel's device time alone (the planning
- * and split-merge launches are outside the pair).  NULL, NULL turns it off.
- * The events are owned by the caller and must outlive the calls.
+ * thread records `start` on its stream immediately before the launch of its
+ * attention kernels (the tensor-core prefill kernel, when the step has
+ * prefill tiles for it, then the main attention kernel) and `stop`
+ * immediately after them, so that cudaEventElapsedTime gives their device
+ * time alone (the planning and split-merge launches are outside the pair).
+ * NULL, NULL turns it off.  The events are owned by the caller and must
+ * outlive the calls.
  */
 pa_status pa_set_profile_events(pa_event_t start, pa_event_t stop);
+
+/*
+ * pa_launch_count -- measurement aid (no counterpart on the pages): the
+ * number of kernels this library has launched from the calling host thread
+ * since it was loaded, through every entry point (launches captured into a
+ * CUDA graph count once, at capture).  count: host pointer.  Never fails
+ * except on a NULL pointer (PA_ERR_INVALID_ARG).
+ */
+pa_status pa_launch_count(uint64_t* count);
 
 #ifdef __cplusplus
 }

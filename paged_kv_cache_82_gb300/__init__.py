@@ -35,7 +35,8 @@ BLOCK_SIZE = 16
 
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_copy_blocks",
             "pa_attention_workspace_size", "pa_attention",
-            "pa_get_device_error", "pa_set_profile_events")
+            "pa_get_device_error", "pa_set_profile_events",
+            "pa_launch_count", "pa_attention_noalloc")
 
 _DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3}
 _lib = None
@@ -79,6 +80,8 @@ def load_library(path: str = LIB_PATH):
     lib.pa_get_device_error.restype = i32
     lib.pa_set_profile_events.argtypes = [P, P]
     lib.pa_set_profile_events.restype = i32
+    lib.pa_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    lib.pa_launch_count.restype = i32
     _lib = lib
     return lib
 
@@ -228,8 +231,9 @@ def pa_get_device_error(stream=None) -> int:
 
 def pa_set_profile_events(start: Optional[torch.cuda.Event],
                           stop: Optional[torch.cuda.Event]) -> None:
-    """Record `start` / `stop` around every later main attention launch of
-    this thread (measurement hook); None, None turns it off."""
+    """Record `start` / `stop` around the attention kernels of every later
+    pa_attention call of this thread (measurement hook); None, None turns it
+    off."""
     def handle(ev):
         if ev is None:
             return None
@@ -237,6 +241,13 @@ def pa_set_profile_events(start: Optional[torch.cuda.Event],
         return ev.cuda_event
     _check(_load().pa_set_profile_events(handle(start), handle(stop)),
            "pa_set_profile_events")
+
+
+def pa_launch_count() -> int:
+    """Kernels the library has launched from this thread so far."""
+    n = ctypes.c_uint64(0)
+    _check(_load().pa_launch_count(ctypes.byref(n)), "pa_launch_count")
+    return int(n.value)
 
 
 def pa_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,

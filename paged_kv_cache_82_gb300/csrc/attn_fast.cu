@@ -1806,6 +1806,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
     plan_kernel<<<1, kPlanThreads, kPlanCacheBytes, stream>>>(pa);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launch();
   }
   // The attention kernel and the merge are launched as programmatic
   // dependents: each may start while its predecessor runs and waits (on the
@@ -1838,6 +1839,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   }
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
+  count_launch();
   if (plan.has_decode) {
     // split segments: at most one fewer than the CTAs that got work
     cfg.blockDim = dim3(128);
@@ -1848,6 +1850,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
       cfg.dynamicSmemBytes = 0;
       e = cudaLaunchKernelEx(&cfg, merge_kernel<OutT<kKind>>, f);
     }
+    if (e == cudaSuccess) count_launch();
   }
   return e;
 }

@@ -109,7 +109,9 @@ cudaError_t launch_t(const GenericParams& gp, int head_dim, cudaStream_t stream)
     attn_generic_kernel<TQ, TC, 128><<<grid, 128, 0, stream>>>(gp);
   else
     attn_generic_kernel<TQ, TC, 64><<<grid, 128, 0, stream>>>(gp);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 }  // namespace

@@ -13,16 +13,18 @@
 // How (one CTA per SM, persistent over the step's prefill tiles):
 //  * A tile is 128 query rows of one (request, KV head): 128 / G consecutive
 //    tokens times the G q heads of the group, row = token * G + head.  Keys
-//    go in chunks of 128 (8 pages).  The producer warp draws tiles from a
+//    go in chunks of 128 (8 pages).  Warp 8 draws tiles from a
 //    step-wide counter, longest first, and passes each tile's index to the
 //    other warps through a two-slot ring in shared memory.
-//  * warp 4 (TMA producer): the Q tile through a 3-D map over q
-//    [token][head][dim], and for every chunk its pages of K and of V through
-//    a 2-D map over the cache rows, each page as two 64-column halves under
-//    the 128-byte swizzle, into a two-deep ring.  The same shared-memory
+//  * warps 8 and 9 (TMA producers): the Q tile through a 3-D map over q
+//    [token][head][dim] and, for every chunk, its pages of K (warp 8) and of
+//    V (warp 9) through 2-D maps over the cache rows, each page as two
+//    64-column halves under the 128-byte swizzle, into rings three (K) and
+//    two (V) chunks deep.  The two rings advance independently, so K runs
+//    ahead of the P.V that frees the V stages.  The same shared-memory
 //    layout serves as the K-major B operand of Q.K^T and as the MN-major B
 //    operand of P.V.
-//  * warp 5 (MMA): allocates tensor memory (512 columns: three S buffers and
+//  * warp 10 (MMA): allocates tensor memory (512 columns: three S buffers and
 //    O) and issues, from one lane, S = Q.K^T (M 128, N = 16 x pages of the
 //    chunk, K 128) into the S buffer of the chunk, and O += P.V with P read
 //    from tensor memory, where the softmax wrote it over that chunk's S.  P
@@ -30,12 +32,13 @@
 //    probabilities to 16 bits costs no accuracy.  Completion is tracked with
 //    tcgen05.commit on mbarriers; with three buffers the softmax of one chunk
 //    overlaps the MMAs of its neighbours.
-//  * warps 0-3 (softmax): one thread per query row.  Each chunk: S from
-//    tensor memory, scale and causal mask, online softmax against a
-//    reference max that only moves when the row max has grown by more than
-//    2^8 (O is then rescaled in tensor memory; otherwise the exponentials
-//    stay below 2^8), P into tensor memory.  At the end of the tile: O / l in
-//    the output type.
+//  * warps 0-7 (softmax): two threads per query row, one per half of the
+//    key columns (warps w and w + 4 share lane quarter w % 4 of tensor
+//    memory).  Each chunk: S from tensor memory, causal mask, online softmax
+//    against a reference max that only moves when the row max has grown by
+//    more than 2^8 (O is then rescaled in tensor memory; otherwise the
+//    exponentials stay below 2^8), P into tensor memory.  At the end of the
+//    tile: O / l in the output type.
 //  * V rows of the request's last page that lie past the sequence end are
 //    cleared in shared memory before P.V (their P is 0, but 0 x NaN is not).
 //
@@ -56,17 +59,23 @@ namespace {
 constexpr int kTcRows = 128;               // query rows of a tile (MMA M)
 constexpr int kTcKeys = 128;               // keys of a chunk
 constexpr int kTcPages = kTcKeys / kBS;    // pages of a chunk
-constexpr int kTcThreads = 192;            // 4 softmax warps, producer, MMA
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8;           // two per row quarter
+constexpr int kKWarp = kSoftmaxWarps;      // tiles, Q and K
+constexpr int kVWarp = kSoftmaxWarps + 1;  // V
+constexpr int kMmaWarp = kSoftmaxWarps + 2;
+constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;
 constexpr int kHalf = 128 * 128;           // 128 rows x 128 B: one column half
 constexpr int kTileBytes = 2 * kHalf;      // 128 rows x 128 columns, 16-bit
 constexpr int kPageHalf = kBS * 128;       // one page, one column half
 constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (log2)
-#ifndef PA_TC_KV_STAGES
-#define PA_TC_KV_STAGES 2
+#ifndef PA_TC_K_STAGES
+#define PA_TC_K_STAGES 3
 #endif
-constexpr int kKvStages = PA_TC_KV_STAGES;  // ring depth, chunks of K and of V
+#ifndef PA_TC_V_STAGES
+#define PA_TC_V_STAGES 2
+#endif
+constexpr int kKStages = PA_TC_K_STAGES;  // ring depth in chunks, K
+constexpr int kVStages = PA_TC_V_STAGES;  // ring depth in chunks, V
 constexpr int kSBufs = 3;                   // S / P buffers in tensor memory
 
 // Tensor memory: three S buffers of 128 columns; the softmax overwrites each
@@ -80,27 +89,29 @@ enum : int {
   kQFull = 0,
   kQEmpty = 1,
   kKFull = 2,
-  kKEmpty = kKFull + kKvStages,
-  kVFull = kKEmpty + kKvStages,
-  kVEmpty = kVFull + kKvStages,
-  kSFull = kVEmpty + kKvStages,      // S of the buffer written
+  kKEmpty = kKFull + kKStages,
+  kVFull = kKEmpty + kKStages,
+  kVEmpty = kVFull + kVStages,
+  kSFull = kVEmpty + kVStages,       // S of the buffer written
   kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
   kTileFull = kPvDone + kSBufs,      // tile index slot filled
-  kTileEmpty = kTileFull + 2,        // tile index slot read (5 warps)
-  kMmaDone = kTileEmpty + 2,
+  kTileEmpty = kTileFull + 2,        // tile index slot read (10 warps)
+  kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
+  kMmaDone = kXchg + 4,
   kNumBars = kMmaDone + 1
 };
 
 struct TcLayout {
   static constexpr int kK = 0;                               // K stages
-  static constexpr int kV = kK + kKvStages * kTileBytes;     // V stages
-  static constexpr int kQ = kV + kKvStages * kTileBytes;     // Q tile
+  static constexpr int kV = kK + kKStages * kTileBytes;      // V stages
+  static constexpr int kQ = kV + kVStages * kTileBytes;      // Q tile
   static constexpr int kBars = kQ + kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileSlot = kAbort + 4;               // int[2]
-  static constexpr int kBytes = kTileSlot + 8;
+  static constexpr int kXchgSlot = kTileSlot + 8;            // float[2][2][128]
+  static constexpr int kBytes = kXchgSlot + 2 * 2 * 128 * 4;
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
 static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -224,8 +235,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
-      if (i >= kPFull && i < kPFull + kSBufs) count = kTcRows;
-      if (i == kTileEmpty || i == kTileEmpty + 1) count = 5;
+      if (i >= kPFull && i < kPFull + kSBufs) count = kSoftmaxWarps * 32;
+      if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 2;
+      if (i >= kXchg && i < kXchg + 4) count = 64;
       mbar_init(bars + 8 * i, count);
     }
     *abort_flag = 0;
@@ -241,16 +253,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   pdl_wait();  // the planner's tile list is complete
   const int n_atoms = min(*p.n_atoms, p.max_atoms);
 
-  if (warp == kProducerWarp) {
-    // ------------------------------ producer ------------------------------
+  // page rows of chunk c (lanes < np), checked against the pool
+  auto chunk_rows = [&](const TcTile& t, int c, int np) -> int {
+    int row = 0;
+    if (lane < np) {
+      int blk = __ldg(p.block_tables + (int64_t)t.r * p.max_blocks_per_seq +
+                      c * kTcPages + lane);
+      if (blk < 0 || blk >= p.num_blocks) {
+        flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+        blk = 0;
+      }
+      row = (blk * p.num_kv_heads + t.g) * kBS;
+    }
+    return row;
+  };
+  // one chunk of K or V: np pages, two 64-column halves each
+  auto load_chunk = [&](const CUtensorMap* map, uint32_t dst, uint32_t full,
+                        int np, int row) {
+    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)np * 2u * kPageHalf);
+    __syncwarp();
+    if (lane < np) {
+      tma_load_2d(dst + lane * kPageHalf, map, full, 0, row);
+      tma_load_2d(dst + kHalf + lane * kPageHalf, map, full, 64, row);
+    }
+  };
+
+  if (warp == kKWarp) {
+    // ------------------------- producer: tiles, Q, K -------------------------
     if (lane == 0) {
       tma_prefetch_desc(&tmap_q);
       tma_prefetch_desc(&tmap_k);
-      tma_prefetch_desc(&tmap_v);
     }
     const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
     uint32_t u = 0, qt = 0, q = 0;
-    uint32_t used[2][kKvStages] = {};  // loads issued: [K/V][stage]
+    uint32_t used[kKStages] = {};  // loads issued into each stage
     bool go = true;
     while (go) {
       // hand out the next tile, longest first (the planner lists a request's
@@ -281,50 +317,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     t.q0 + t.i0);
       }
       ++qt;
-      const int32_t* bt = p.block_tables + (int64_t)t.r * p.max_blocks_per_seq;
-      for (int c = 0; c < t.nc && go; ++c, ++u) {
-        const int st = u % kKvStages;
-        const uint32_t ph = (u / kKvStages) & 1;
-        const int pg0 = c * kTcPages;
-        const int np = min(kTcPages, t.pages - pg0);
-        int row = 0;
-        if (lane < np) {
-          int blk = __ldg(bt + pg0 + lane);
-          if (blk < 0 || blk >= p.num_blocks) {
-            flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
-            blk = 0;
-          }
-          row = (blk * p.num_kv_heads + t.g) * kBS;
+      for (int c = 0; c < t.nc; ++c, ++u) {
+        const int st = u % kKStages;
+        const int np = min(kTcPages, t.pages - c * kTcPages);
+        const int row = chunk_rows(t, c, np);
+        if (u >= kKStages &&
+            !warp_wait(bars + 8 * (kKEmpty + st), ((u / kKStages) & 1) ^ 1,
+                       abort_flag, p.err)) {
+          go = false;
+          break;
         }
-        for (int kv = 0; kv < 2; ++kv) {
-          const int full = (kv ? kVFull : kKFull) + st;
-          const int empty = (kv ? kVEmpty : kKEmpty) + st;
-          if (u >= kKvStages &&
-              !warp_wait(bars + 8 * empty, ph ^ 1, abort_flag, p.err)) {
-            go = false;
-            break;
-          }
-          if (lane == 0)
-            mbar_arrive_expect_tx(bars + 8 * full, (uint32_t)np * 2u * kPageHalf);
-          __syncwarp();
-          if (lane < np) {
-            const uint32_t dst = base + (kv ? TcLayout::kV : TcLayout::kK) +
-                                 st * kTileBytes + lane * kPageHalf;
-            const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
-            tma_load_2d(dst, map, bars + 8 * full, 0, row);
-            tma_load_2d(dst + kHalf, map, bars + 8 * full, 64, row);
-          }
-          ++used[kv][st];
-        }
+        load_chunk(&tmap_k, base + TcLayout::kK + st * kTileBytes,
+                   bars + 8 * (kKFull + st), np, row);
+        ++used[st];
       }
     }
     // let every copy this warp issued land before the CTA may exit
-    for (int kv = 0; kv < 2; ++kv)
-      for (int st = 0; st < kKvStages; ++st)
-        if (used[kv][st] > 0)
-          mbar_wait_bounded(bars + 8 * ((kv ? kVFull : kKFull) + st),
-                            (used[kv][st] - 1) & 1);
+    for (int st = 0; st < kKStages; ++st)
+      if (used[st] > 0)
+        mbar_wait_bounded(bars + 8 * (kKFull + st), (used[st] - 1) & 1);
     if (qt > 0) mbar_wait_bounded(bars + 8 * kQFull, (qt - 1) & 1);
+  } else if (warp == kVWarp) {
+    // ----------------------------- producer: V ------------------------------
+    if (lane == 0) tma_prefetch_desc(&tmap_v);
+    uint32_t u = 0;
+    uint32_t used[kVStages] = {};
+    bool go = true;
+    for (uint32_t q = 0; go; ++q) {
+      const int a = next_tile(bars, slots, q, abort_flag, p.err);
+      if (a < 0) break;
+      const TcTile t = tc_tile(p, a);
+      if (!t.ok) continue;
+      for (int c = 0; c < t.nc; ++c, ++u) {
+        const int st = u % kVStages;
+        const int np = min(kTcPages, t.pages - c * kTcPages);
+        const int row = chunk_rows(t, c, np);
+        if (u >= kVStages &&
+            !warp_wait(bars + 8 * (kVEmpty + st), ((u / kVStages) & 1) ^ 1,
+                       abort_flag, p.err)) {
+          go = false;
+          break;
+        }
+        load_chunk(&tmap_v, base + TcLayout::kV + st * kTileBytes,
+                   bars + 8 * (kVFull + st), np, row);
+        ++used[st];
+      }
+    }
+    for (int st = 0; st < kVStages; ++st)
+      if (used[st] > 0)
+        mbar_wait_bounded(bars + 8 * (kVFull + st), (used[st] - 1) & 1);
   } else if (warp == kMmaWarp) {
     // -------------------------------- MMA ---------------------------------
     const uint32_t q_s = base + TcLayout::kQ;
@@ -332,9 +373,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // S of chunk uu (chunk c of tile t) into buffer uu % 3, once the P.V
     // that last read that buffer has completed
     auto issue_qk = [&](uint32_t uu, int c, const TcTile& t) -> bool {
-      const int st = uu % kKvStages;
+      const int st = uu % kKStages;
       const int b = uu % kSBufs;
-      if (!warp_wait(bars + 8 * (kKFull + st), (uu / kKvStages) & 1, abort_flag, p.err))
+      if (!warp_wait(bars + 8 * (kKFull + st), (uu / kKStages) & 1, abort_flag, p.err))
         return false;
       if (uu >= kSBufs &&
           !warp_wait(bars + 8 * (kPvDone + b), ((uu / kSBufs) - 1) & 1, abort_flag, p.err))
@@ -370,7 +411,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       bool go = true;
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
-        const int st = uu % kKvStages;
+        const int sv = uu % kVStages;
         const int b = uu % kSBufs;
         if (c + 1 < t.nc) {
           if (!issue_qk(uu + 1, c + 1, t)) { go = false; break; }
@@ -378,7 +419,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           tc_commit(bars + 8 * kQEmpty);  // Q is free once the last S is done
         }
         if (!warp_wait(bars + 8 * (kPFull + b), (uu / kSBufs) & 1, abort_flag, p.err) ||
-            !warp_wait(bars + 8 * (kVFull + st), (uu / kKvStages) & 1, abort_flag, p.err)) {
+            !warp_wait(bars + 8 * (kVFull + sv), (uu / kVStages) & 1, abort_flag, p.err)) {
           go = false;
           break;
         }
@@ -387,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const int np = min(kTcPages, t.pages - pg0);
         if (tail != 0 && last >= pg0 && last < pg0 + np) {
           // V rows past the sequence end (whatever the cache holds there)
-          uint8_t* vp = sp + TcLayout::kV + st * kTileBytes + (last - pg0) * kPageHalf;
+          uint8_t* vp = sp + TcLayout::kV + sv * kTileBytes + (last - pg0) * kPageHalf;
           const int nrow = kBS - tail;
           for (int i = lane; i < nrow * 16; i += 32) {
             const int rr = tail + (i >> 4), ch = i & 15;
@@ -398,7 +439,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         }
         __syncwarp();
         if (lane == 0) {
-          const uint32_t v_s = base + TcLayout::kV + st * kTileBytes;
+          const uint32_t v_s = base + TcLayout::kV + sv * kTileBytes;
           const uint32_t t_p = tmem + b * 128;
           for (int pp = 0; pp < np; ++pp) {
             const uint64_t bv = tc_desc_sw128(v_s + pp * kPageHalf, kHalf, 1024);
@@ -406,7 +447,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       (c > 0 || pp > 0) ? 1u : 0u);
             tc_mma_ts(tmem + kColO, t_p + pp * 16 + 8, bv, idesc_pv, 1u);
           }
-          tc_commit(bars + 8 * (kVEmpty + st));
+          tc_commit(bars + 8 * (kVEmpty + sv));
           tc_commit(bars + 8 * (kPvDone + b));
         }
         __syncwarp();
@@ -420,11 +461,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_wait_bounded(bars + 8 * kMmaDone, 0);
   } else {
     // ------------------------------ softmax -------------------------------
-    const int row = threadIdx.x;  // tensor-memory lane
-    const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-    const uint32_t t_o = tmem + lrow + kColO;
+    // Warps w and w + 4 share the rows of lane quarter w % 4: w takes key
+    // columns 0-63 of every chunk, w + 4 columns 64-127.  The two halves of
+    // a row trade their partial max every chunk (and their partial sums at
+    // the end of the tile) through shared memory, on a per-quarter mbarrier.
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;  // tensor-memory lane
+    const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_o = tmem + lrow + kColO + half * 64;
+    const uint32_t xbar = bars + 8 * (kXchg + quarter);
+    float* xslot = reinterpret_cast<float*>(sp + TcLayout::kXchgSlot);
     const int it = row / G, jh = row - it * G;
-    uint32_t u = 0;
+    uint32_t u = 0, xk = 0;  // chunks done, exchanges done
+    // partner's value of this exchange (bounded wait); false on a timeout
+    auto exchange = [&](float mine, float& theirs) -> bool {
+      float* sl = xslot + (xk & 1) * 256;
+      sl[half * 128 + row] = mine;
+      mbar_arrive(xbar);
+      const bool ok = warp_wait(xbar, xk & 1, abort_flag, p.err);
+      theirs = sl[(half ^ 1) * 128 + row];
+      ++xk;
+      return ok;
+    };
     for (uint32_t q = 0;; ++q) {
       const int a = next_tile(bars, slots, q, abort_flag, p.err);
       if (a < 0) break;
@@ -439,33 +497,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
         const int b = uu % kSBufs;
-        const uint32_t t_b = tmem + lrow + b * 128;
+        const uint32_t t_b = tmem + lrow + b * 128 + half * 64;
         if (!warp_wait(bars + 8 * (kSFull + b), (uu / kSBufs) & 1, abort_flag, p.err)) {
           go = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tc_ld32(t_b + j * 32, sr[j]);
+        uint32_t sr[2][32];
+        tc_ld32(t_b, sr[0]);
+        tc_ld32(t_b + 32, sr[1]);
         tc_wait_ld_dep(sr);
-        // row max of the raw scores (the scale is positive); keys past the
-        // row's limit (only in chunks that reach the diagonal) become -inf
-        const int vis = lim - c * kTcKeys;  // columns 0 .. vis are visible
+        // partial row max of the raw scores (the scale is positive); keys
+        // past the row's limit (only in chunks that reach the diagonal)
+        // become -inf
+        const int vis = lim - c * kTcKeys - half * 64;  // columns 0 .. vis
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (__any_sync(~0u, vis < kTcKeys - 1)) {
+        if (__any_sync(~0u, vis < 63)) {
 #pragma unroll
-          for (int j = 0; j < 128; ++j) {
+          for (int j = 0; j < 64; ++j) {
             const float x = j <= vis ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
             sr[j >> 5][j & 31] = __float_as_uint(x);
             mx4[j & 3] = fmaxf(mx4[j & 3], x);
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 128; ++j)
+          for (int j = 0; j < 64; ++j)
             mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        float mx_other;
+        if (!exchange(mx, mx_other)) {
+          go = false;
+          break;
+        }
+        mx = fmaxf(mx, mx_other);  // the same value in both halves
         const float m_new = fmaxf(m_ref, mx * p.score_scale);
         const bool grow = m_new > m_ref + kRescaleLog2;
         const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
@@ -479,7 +544,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 2; ++j) {
             uint32_t o[32];
             tc_ld32(t_o + j * 32, o);
             tc_wait_ld_dep(o);
@@ -500,7 +565,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float neg_m = -m_ref;
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
           uint32_t w[32];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -518,16 +583,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         mbar_arrive(bars + 8 * (kPFull + b));
       }
       if (!go) break;
+      // the row sum: both halves add the two partial sums in the same order
+      float l_other;
+      if (!exchange(l, l_other)) break;
+      const float l_tot = half == 0 ? l + l_other : l_other + l;
       const uint32_t ul = u + t.nc - 1;
       if (!warp_wait(bars + 8 * (kPvDone + ul % kSBufs), (ul / kSBufs) & 1,
                      abort_flag, p.err))
         break;
       tc_fence_after();
-      const float inv = 1.f / l;
+      const float inv = 1.f / l_tot;
       TOut* o = static_cast<TOut*>(p.out) +
-                ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128;
+                ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128 +
+                half * 64;
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 2; ++j) {
         uint32_t v[32];
         tc_ld32(t_o + j * 32, v);
         tc_wait_ld_dep(v);
@@ -580,7 +650,9 @@ cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kBF16>, m.q, m.k, m.v, p);
+  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kBF16>, m.q, m.k, m.v, p);
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 }  // namespace

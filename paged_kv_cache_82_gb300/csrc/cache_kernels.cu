@@ -140,7 +140,9 @@ cudaError_t launch_reshape_t(const void* key, const void* value,
         num_blocks * kBS, num_kv_heads, head_dim, slot_mapping, k_scale,
         v_scale, err);
   }
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 // Copy whole blocks: blockIdx.y walks the pairs, x-threads stripe the
@@ -216,7 +218,9 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
   copy_blocks_kernel<<<dim3((unsigned)gx, (unsigned)gy), kThreads, 0, stream>>>(
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), num_blocks,
       vecs, block_mapping, num_pairs, err);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 }  // namespace pa

@@ -103,10 +103,13 @@ EncodeTiledFn encode_fn() {
 }
 
 thread_local ProfileEvents t_profile;
+thread_local uint64_t t_launches = 0;
 
 }  // namespace
 
 ProfileEvents& profile_events() { return t_profile; }
+
+void count_launch() { ++t_launches; }
 
 bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
                               CUtensorMap* tv) {
@@ -400,6 +403,12 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
     e = launch_attention_generic(a, s);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_launch_count(uint64_t* count) {
+  if (!count) return PA_ERR_INVALID_ARG;
+  *count = t_launches;
+  return PA_OK;
 }
 
 pa_status pa_set_profile_events(pa_event_t start, pa_event_t stop) {

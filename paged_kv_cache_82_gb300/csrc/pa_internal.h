@@ -10,6 +10,10 @@
 
 namespace pa {
 
+// Kernels launched from the calling host thread (pa_launch_count); every
+// launch site calls count_launch() once its launch has been accepted.
+void count_launch();
+
 // ---- cache kernels (cache_kernels.cu) --------------------------------------
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      pa_dtype kv_dtype, int64_t num_tokens,

@@ -102,3 +102,21 @@ def test_workspace_plan_is_pure_host_logic():
     # exercised through the C ABI on GPU machines; here only the formula's
     # inputs are validated by the header (no device to query the SM count)
     assert "pa_attention_workspace_size" in _declared()
+
+
+def test_launch_count_without_a_gpu(lib):
+    n = ctypes.c_uint64(123)
+    lib.pa_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+    assert lib.pa_launch_count(ctypes.byref(n)) == 0
+    assert n.value == 0  # nothing launched from this thread
+    lib.pa_launch_count.argtypes = [ctypes.c_void_p]
+    assert lib.pa_launch_count(None) == 1  # PA_ERR_INVALID_ARG
+
+
+def test_attention_flops_counts_visible_pairs():
+    # two requests: 3 new tokens after 5 cached (keys 6, 7, 8 visible) and a
+    # 1-token decode over 4 keys
+    wl = workloads.decode_step("f", 1, seq_lens=[8, 4], q_lens=[3, 1],
+                               num_q_heads=2, num_kv_heads=1, head_dim=8,
+                               num_blocks=4, dtype="bf16", cache_dtype="bf16")
+    assert workloads.attention_flops(wl) == (6 + 7 + 8 + 4) * 2 * 8 * 4

@@ -236,11 +236,25 @@ def test_empty_step_launches_nothing():
     kc = torch.zeros(4, 2, 16, 128, dtype=torch.bfloat16, device="cuda")
     q = torch.zeros(0, 8, 128, dtype=torch.bfloat16, device="cuda")
     i32 = dict(dtype=torch.int32, device="cuda")
+    n0 = pa.pa_launch_count()
     out = pa.pa_attention(q, kc, kc.clone(), torch.zeros(0, 1, **i32),
                           torch.zeros(0, **i32), torch.zeros(1, **i32), 0, 0,
                           0.1)
     assert out.shape == (0, 8, 128)
+    assert pa.pa_launch_count() == n0
     assert pa.pa_get_device_error() == 0
+
+
+def test_launches_per_step_kind():
+    # decode-only step: the attention kernel plans itself, then the merge
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 1), (40, 1)], 32, 8))
+    assert pa.pa_launch_count() - n0 == 2
+    # K/V write + a step with bf16 prefill tiles: planner, tensor-core
+    # prefill kernel, attention kernel, merge
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 1), (100, 64)], 32, 8, write_new=True))
+    assert pa.pa_launch_count() - n0 == 5
 
 
 def test_bitwise_determinism_and_block_relabelling():

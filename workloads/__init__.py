@@ -388,4 +388,29 @@ def config5(batch: int = 16, lo: int = 32768, hi: int = 131072,
                                     "FP8 E4M3 KV"))
 
 
+def prefill_chunk(ctx: int = 4096, new: int = 4096) -> Workload:
+    """One chunked prefill, Llama-3.1-8B shape (32q/8kv heads, head_dim 128,
+    bf16): `new` prompt tokens after `ctx` cached ones, already in the cache
+    (the step attends only).  Used to measure the prefill tiles alone."""
+    seed = 82006
+    L = ctx + new
+    return decode_step("prefill_chunk_llama31_8b", seed, seq_lens=[L],
+                       q_lens=[new], num_q_heads=32, num_kv_heads=8,
+                       head_dim=128, num_blocks=_blocks_for(L) + 8,
+                       dtype="bf16", cache_dtype="bf16", write_new=False,
+                       description=f"1 prefill chunk: {new} new after {ctx}")
+
+
+def attention_flops(wl: Workload) -> int:
+    """Multiply-adds x 2 of Q.K^T and P.V over the visible (row, key) pairs
+    of the step: query i of a request with n new tokens and L keys sees
+    L - n + i + 1 keys."""
+    pairs = 0
+    for r in wl.requests:
+        L = r.num_computed + r.num_new
+        n = r.num_new
+        pairs += n * (L - n) + n * (n + 1) // 2
+    return pairs * wl.num_q_heads * wl.head_dim * 2 * 2
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
