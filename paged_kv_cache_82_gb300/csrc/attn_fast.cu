@@ -42,7 +42,9 @@ namespace {
 #define PA_NARROW_MIN_BLOCKS 3  // resident CTAs per SM, <= 8-row kernel
 #endif
 constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
-constexpr int kSelfPlanMaxSeqs = 1024;  // decode steps the kernel plans itself
+// requests of a step the attention kernel plans itself (narrow / wide build)
+constexpr int kSelfPlanMaxSeqs = 1024;
+constexpr int kSelfPlanMaxSeqsWide = 512;
 
 #ifndef PA_PRODUCER_PAGES
 #define PA_PRODUCER_PAGES 4     // pages the producer issues per step (2 lanes each)
@@ -134,7 +136,8 @@ struct FastParams {
   int max_query_len, max_seq_len;
   float score_scale;  // softmax scale * log2(e) (* k_scale for FP8)
   float out_scale;    // 1, or v_scale for FP8
-  int self_plan;      // 1: every CTA plans its own range (decode-only steps)
+  int self_plan;      // 1: every CTA plans its own range
+  int dec_rows_max;   // decode-class requests have at most this many rows
 };
 
 // ---------------------------------------------------------------------------
@@ -174,34 +177,6 @@ struct PlanArgs {
   int4* split_list;       // segments cut by CTA boundaries: {r, g, parts, first}
   int* n_split;
 };
-
-template <typename T>
-__device__ __forceinline__ T block_scan_excl(T v, T* total, T* warp_sums) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  T inc = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const T o = __shfl_up_sync(~0u, inc, d);
-    if (lane >= d) inc += o;
-  }
-  if (lane == 31) warp_sums[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    T w = lane < nw ? warp_sums[lane] : T(0);
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const T o = __shfl_up_sync(~0u, w, d);
-      if (lane >= d) w += o;
-    }
-    if (lane < nw) warp_sums[lane] = w;
-    if (lane == nw - 1) *total = w;
-  }
-  __syncthreads();
-  const T ex = (warp == 0 ? T(0) : warp_sums[warp - 1]) + inc - v;
-  __syncthreads();
-  return ex;
-}
 
 // key pages seen by prefill tile tt of a request (its last row's limit)
 __device__ __forceinline__ int tile_pages(const ReqMeta& m, int G, int tt,
@@ -312,10 +287,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs pa) {
   }
   if (threadIdx.x == 0) {
     s_atoms = run_atoms < pa.max_atoms ? run_atoms : pa.max_atoms;
-    if (pa.prefill_tc) {
-      pa.n_atoms_out[0] = (int)s_atoms;
-      pa.n_atoms_out[1] = 0;  // tiles handed out by the tensor-core kernel
-    }
+    if (pa.prefill_tc) *pa.n_atoms_out = (int)s_atoms;
     s_cost_pre = run_pcost;
     s_dec_total = run_dec;
   }
@@ -1022,9 +994,10 @@ struct Layout {
   // narrow kernel: the CTA's own plan (per-request decode offset, pages,
   // rows) and scan scratch
   static constexpr int kPlan = kAbort + 16;
-  static constexpr int kPlanBytes = kWide ? 0 : kSelfPlanMaxSeqs * 16;
+  static constexpr int kMaxSeqs = kWide ? kSelfPlanMaxSeqsWide : kSelfPlanMaxSeqs;
+  static constexpr int kPlanBytes = kMaxSeqs * 16;
   static constexpr int kScan = kPlan + kPlanBytes;
-  static constexpr int kScanBytes = kWide ? 0 : 34 * 8;
+  static constexpr int kScanBytes = 34 * 8;
   static constexpr int kBytes = kScan + kScanBytes;
   static constexpr int kSmemBytes = 1024 + kBytes;  // + alignment slack
 };
@@ -1415,7 +1388,7 @@ __device__ long long plan_prefix(const FastParams& p, long long* dec0,
       const ReqMeta m = load_req(p.qsl, p.seq_lens, r, p.num_tokens,
                                  p.max_query_len, p.max_seq_len,
                                  p.max_blocks_per_seq);
-      if (m.ok && m.n > 0 && m.n * p.group <= 8) {
+      if (m.ok && m.n > 0 && m.n * p.group <= p.dec_rows_max) {
         dl = m.nb;
         rw = m.n * p.group;
       } else if (!m.ok && blockIdx.x == 0) {
@@ -1497,11 +1470,11 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
   pdl_wait();               // the planner (and everything before it) is done
   ItemSource src{};
   src.self = false;
-  if constexpr (!kWide) {
+  {
     if (p.self_plan) {
       long long* dec0 = reinterpret_cast<long long*>(sm.ptr + Ly::kPlan);
-      int* declen = reinterpret_cast<int*>(dec0 + kSelfPlanMaxSeqs);
-      int* rows = declen + kSelfPlanMaxSeqs;
+      int* declen = reinterpret_cast<int*>(dec0 + Ly::kMaxSeqs);
+      int* rows = declen + Ly::kMaxSeqs;
       long long* scan = reinterpret_cast<long long*>(sm.ptr + Ly::kScan);
       const long long C = plan_prefix(p, dec0, declen, rows, scan + 32, scan);
       const int g_eff = self_plan_grid(C, gridDim.x);
@@ -1798,10 +1771,13 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   if (e != cudaSuccess) return e;
   if (grid > plan.grid_max) grid = plan.grid_max;
   pa.grid = grid;
-  // decode-only steps of up to kSelfPlanMaxSeqs requests plan inside the
-  // attention kernel (no planner launch)
+  // Steps whose decode work is all the attention kernel has to do (no
+  // prefill tiles, or prefill tiles on the tensor-core kernel) plan inside
+  // the kernels, up to a request count; the rest go through the planner.
   FastParams f = fp;
-  f.self_plan = !wide && fp.num_seqs <= kSelfPlanMaxSeqs;
+  f.dec_rows_max = wide ? kDecodeMaxRows : 8;
+  f.self_plan = fp.num_seqs <= (wide ? kSelfPlanMaxSeqsWide : kSelfPlanMaxSeqs) &&
+                (!plan.has_prefill || tc != nullptr);
   if (!f.self_plan) {
     plan_kernel<<<1, kPlanThreads, kPlanCacheBytes, stream>>>(pa);
     e = cudaGetLastError();
@@ -1826,8 +1802,8 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   if (pe.start) cudaEventRecord(pe.start, stream);
   if (tc) {
     // prefill tiles on the tensor cores, ahead of the decode work
-    e = launch_prefill_tc(a, *tc, pa.atoms, pa.n_atoms_out,
-                          pa.n_atoms_out + 1, pa.max_atoms, num_sms, stream);
+    e = launch_prefill_tc(a, *tc, f.self_plan != 0, pa.atoms, pa.n_atoms_out,
+                          pa.max_atoms, num_sms, stream);
     if (e != cudaSuccess) return e;
   }
   if (wide) {

@@ -68,6 +68,7 @@ constexpr int kHalf = 128 * 128;           // 128 rows x 128 B: one column half
 constexpr int kTileBytes = 2 * kHalf;      // 128 rows x 128 columns, 16-bit
 constexpr int kPageHalf = kBS * 128;       // one page, one column half
 constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (log2)
+constexpr int kTcMaxSeqs = 1024;           // requests of a step it plans itself
 #ifndef PA_TC_K_STAGES
 #define PA_TC_K_STAGES 3
 #endif
@@ -95,9 +96,7 @@ enum : int {
   kSFull = kVEmpty + kVStages,       // S of the buffer written
   kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
-  kTileFull = kPvDone + kSBufs,      // tile index slot filled
-  kTileEmpty = kTileFull + 2,        // tile index slot read (10 warps)
-  kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
+  kXchg = kPvDone + kSBufs,          // row halves exchanged, per quarter
   kMmaDone = kXchg + 4,
   kNumBars = kMmaDone + 1
 };
@@ -109,9 +108,12 @@ struct TcLayout {
   static constexpr int kBars = kQ + kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kTileSlot = kAbort + 4;               // int[2]
-  static constexpr int kXchgSlot = kTileSlot + 8;            // float[2][2][128]
-  static constexpr int kBytes = kXchgSlot + 2 * 2 * 128 * 4;
+  static constexpr int kXchgSlot = kAbort + 4;              // float[2][2][128]
+  // the step's tile list when the kernel plans it: per request, the first
+  // tile (x heads) and the tile count; block-scan scratch
+  static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
+  static constexpr int kScan = kPlan + 2 * kTcMaxSeqs * 4;   // int[33]
+  static constexpr int kBytes = kScan + 33 * 4;
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
 static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -121,10 +123,11 @@ struct TcParams {
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const int32_t* qsl;
-  const int4* atoms;     // prefill tiles {r, g, tile, pages} from the planner
+  int self_plan;         // 1: list the step's tiles here; 0: the planner's
+  const int4* atoms;     // planner's tiles {r, g, tile, pages}, request order
   const int* n_atoms;
-  int* tile_ctr;         // tiles handed out so far (zeroed by the planner)
   int max_atoms;
+  int dec_rows_max;      // requests with more query rows are prefill-class
   unsigned* err;
   int64_t num_tokens;
   int64_t num_blocks;
@@ -141,12 +144,33 @@ struct TcTile {
   bool ok;
 };
 
-__device__ __forceinline__ TcTile tc_tile(const TcParams& p, int a) {
-  const int4 at = __ldg(p.atoms + a);
+// Tile li of the step's list, which runs request by request, tile index
+// ascending (causal limits growing), KV head fastest: from the planner's
+// list, or located in the kernel's own per-request prefix.
+__device__ __forceinline__ TcTile tc_tile(const TcParams& p, const int* pre,
+                                          const int* ntl, int li) {
+  int r, g, tt;
+  if (p.self_plan) {
+    int lo = 0, hi = p.num_seqs - 1;  // last request with pre[r] <= li
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pre[mid] <= li) lo = mid; else hi = mid - 1;
+    }
+    r = lo;
+    const int j = li - pre[r];
+    tt = j / p.num_kv_heads;
+    g = j - tt * p.num_kv_heads;
+    if (tt >= ntl[r]) r = -1;  // (cannot happen for li < total)
+  } else {
+    const int4 at = __ldg(p.atoms + li);
+    r = at.x;
+    g = at.y;
+    tt = at.z;
+  }
   TcTile t{};
-  t.r = at.x;
-  t.g = at.y;
-  t.ok = at.x >= 0 && at.x < p.num_seqs && at.y >= 0 && at.y < p.num_kv_heads;
+  t.r = r;
+  t.g = g;
+  t.ok = r >= 0 && r < p.num_seqs && g >= 0 && g < p.num_kv_heads;
   if (!t.ok) return t;
   const ReqMeta m = load_req(p.qsl, p.seq_lens, t.r, p.num_tokens,
                              p.max_query_len, p.max_seq_len,
@@ -154,13 +178,17 @@ __device__ __forceinline__ TcTile tc_tile(const TcParams& p, int a) {
   t.q0 = m.q0;
   t.n = m.n;
   t.L = m.L;
-  t.i0 = at.z * p.tokens_per_tile;
+  t.i0 = tt * p.tokens_per_tile;
   t.ntok = min(p.tokens_per_tile, m.n - t.i0);
-  t.ok = m.ok && at.z >= 0 && t.ntok > 0;
+  t.ok = m.ok && tt >= 0 && t.ntok > 0;
   // keys up to the last token's limit L - n + i0 + ntok - 1
   t.pages = t.ok ? (t.L - t.n + t.i0 + t.ntok - 1) / kBS + 1 : 0;
   t.nc = (t.pages + kTcPages - 1) / kTcPages;
   return t;
+}
+
+__device__ __forceinline__ bool aborted(volatile int* abort_flag) {
+  return __any_sync(~0u, *abort_flag != 0);
 }
 
 // Bounded wait by a whole warp; false (and the CTA aborts) on a timeout.
@@ -175,18 +203,42 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
   return ok;
 }
 
-// The next tile of a consumer warp: index slot q % 2 once the producer has
-// filled it; the warp then hands the slot back.  -1: no more tiles.
-__device__ __forceinline__ int next_tile(uint32_t bars, volatile int* slots,
-                                         uint32_t q, volatile int* abort_flag,
-                                         unsigned* err) {
-  const int s = q & 1;
-  if (!warp_wait(bars + 8 * (kTileFull + s), (q >> 1) & 1, abort_flag, err))
-    return -1;
-  const int a = slots[s];
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
-  return a;
+// The step's prefill tiles: per request (prefill-class: more than
+// dec_rows_max query rows), ceil(rows / tile rows) tiles per KV head; the
+// exclusive prefix of tiles x heads into pre[], the tile counts into ntl[].
+// All threads of the block take part; returns the total.
+__device__ int plan_tiles(const TcParams& p, int* pre, int* ntl, int* scan) {
+  const int rows_per_tile = p.tokens_per_tile * p.group;
+  int run = 0;
+  for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+    const int r = base + threadIdx.x;
+    int tiles = 0;
+    if (r < p.num_seqs) {
+      const ReqMeta m = load_req(p.qsl, p.seq_lens, r, p.num_tokens,
+                                 p.max_query_len, p.max_seq_len,
+                                 p.max_blocks_per_seq);
+      if (m.ok && m.n * p.group > p.dec_rows_max)
+        tiles = (m.n * p.group + rows_per_tile - 1) / rows_per_tile;
+    }
+    const int ex = block_scan_excl<int>(tiles * p.num_kv_heads, scan + 32, scan);
+    const int tot = scan[32];
+    __syncthreads();
+    if (r < p.num_seqs) {
+      pre[r] = run + ex;
+      ntl[r] = tiles;
+    }
+    run += tot;
+  }
+  __syncthreads();
+  return run;
+}
+
+// k-th tile of CTA b of K: a snake over the list from its end (longest
+// tiles first): b, 2K-1-b, 2K+b, ...; -1 past the end
+__device__ __forceinline__ int snake_tile(int k, int total) {
+  const int K = gridDim.x, b = blockIdx.x;
+  const int idx = k * K + ((k & 1) ? K - 1 - b : b);
+  return idx < total ? total - 1 - idx : -1;
 }
 
 // Probabilities as two 16-bit parts each, p = hi + lo + O(2^-16 p): for bf16
@@ -228,7 +280,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   uint8_t* const sp = smem_raw + (base - raw);
   const uint32_t bars = base + TcLayout::kBars;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + TcLayout::kAbort);
-  volatile int* slots = reinterpret_cast<volatile int*>(sp + TcLayout::kTileSlot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
 
@@ -236,7 +287,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
       if (i >= kPFull && i < kPFull + kSBufs) count = kSoftmaxWarps * 32;
-      if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 2;
       if (i >= kXchg && i < kXchg + 4) count = 64;
       mbar_init(bars + 8 * i, count);
     }
@@ -250,8 +300,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const uint32_t tmem =
       *reinterpret_cast<volatile uint32_t*>(sp + TcLayout::kTmemSlot);
   pdl_launch_dependents();
-  pdl_wait();  // the planner's tile list is complete
-  const int n_atoms = min(*p.n_atoms, p.max_atoms);
+  pdl_wait();  // the step's inputs (and the planner's list) are complete
+  int* const pre = reinterpret_cast<int*>(sp + TcLayout::kPlan);
+  int* const ntl = pre + kTcMaxSeqs;
+  const int n_tiles =
+      p.self_plan ? plan_tiles(p, pre, ntl, reinterpret_cast<int*>(sp + TcLayout::kScan))
+                  : min(*p.n_atoms, p.max_atoms);
 
   // page rows of chunk c (lanes < np), checked against the pool
   auto chunk_rows = [&](const TcTile& t, int c, int np) -> int {
@@ -285,27 +339,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tma_prefetch_desc(&tmap_k);
     }
     const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
-    uint32_t u = 0, qt = 0, q = 0;
+    uint32_t u = 0, qt = 0;
     uint32_t used[kKStages] = {};  // loads issued into each stage
     bool go = true;
-    while (go) {
-      // hand out the next tile, longest first (the planner lists a request's
-      // tiles in causal order)
-      const int s = q & 1;
-      if (q >= 2 &&
-          !warp_wait(bars + 8 * (kTileEmpty + s), ((q >> 1) - 1) & 1, abort_flag, p.err))
-        break;
-      int a = -1;
-      if (lane == 0) {
-        const int ticket = *abort_flag ? n_atoms : atomicAdd(p.tile_ctr, 1);
-        a = ticket < n_atoms ? n_atoms - 1 - ticket : -1;
-        slots[s] = a;
-        mbar_arrive(bars + 8 * (kTileFull + s));
-      }
-      a = __shfl_sync(~0u, a, 0);
-      ++q;
-      if (a < 0) break;
-      const TcTile t = tc_tile(p, a);
+    for (int k = 0; go; ++k) {
+      const int li = snake_tile(k, n_tiles);
+      if (li < 0 || aborted(abort_flag)) break;
+      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       if (qt > 0 && !warp_wait(bars + 8 * kQEmpty, (qt - 1) & 1, abort_flag, p.err))
         break;
@@ -343,10 +383,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t u = 0;
     uint32_t used[kVStages] = {};
     bool go = true;
-    for (uint32_t q = 0; go; ++q) {
-      const int a = next_tile(bars, slots, q, abort_flag, p.err);
-      if (a < 0) break;
-      const TcTile t = tc_tile(p, a);
+    for (int k = 0; go; ++k) {
+      const int li = snake_tile(k, n_tiles);
+      if (li < 0 || aborted(abort_flag)) break;
+      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       for (int c = 0; c < t.nc; ++c, ++u) {
         const int st = u % kVStages;
@@ -398,10 +438,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       return true;
     };
     uint32_t u = 0, qt = 0;
-    for (uint32_t q = 0;; ++q) {
-      const int a = next_tile(bars, slots, q, abort_flag, p.err);
-      if (a < 0) break;
-      const TcTile t = tc_tile(p, a);
+    for (int k = 0;; ++k) {
+      const int li = snake_tile(k, n_tiles);
+      if (li < 0 || aborted(abort_flag)) break;
+      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
       ++qt;
@@ -483,10 +523,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       ++xk;
       return ok;
     };
-    for (uint32_t q = 0;; ++q) {
-      const int a = next_tile(bars, slots, q, abort_flag, p.err);
-      if (a < 0) break;
-      const TcTile t = tc_tile(p, a);
+    for (int k = 0;; ++k) {
+      const int li = snake_tile(k, n_tiles);
+      if (li < 0 || aborted(abort_flag)) break;
+      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
@@ -668,18 +708,19 @@ bool tc_prefill_supported(const AttnArgs& a) {
 int tc_prefill_tile_rows(int group) { return (kTcRows / group) * group; }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
-                              const int4* atoms, const int* n_atoms,
-                              int* tile_ctr, int max_atoms, int num_sms,
+                              bool self_plan, const int4* atoms,
+                              const int* n_atoms, int max_atoms, int num_sms,
                               cudaStream_t stream) {
   TcParams p{};
   p.out = a.out;
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.query_start_loc;
+  p.self_plan = self_plan ? 1 : 0;
   p.atoms = atoms;
   p.n_atoms = n_atoms;
-  p.tile_ctr = tile_ctr;
   p.max_atoms = max_atoms;
+  p.dec_rows_max = kDecodeMaxRows;
   p.err = a.err;
   p.num_tokens = a.num_tokens;
   p.num_blocks = a.num_blocks;

@@ -148,6 +148,39 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
 }
 
 // ----------------------------------------------------------------------------
+// exclusive block-wide prefix sum of one value per thread (every thread of
+// the block calls it); *total receives the block's sum.  warp_sums: 32
+// elements of shared memory.
+// ----------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ T block_scan_excl(T v, T* total, T* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const T o = __shfl_up_sync(~0u, inc, d);
+    if (lane >= d) inc += o;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    T w = lane < nw ? warp_sums[lane] : T(0);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const T o = __shfl_up_sync(~0u, w, d);
+      if (lane >= d) w += o;
+    }
+    if (lane < nw) warp_sums[lane] = w;
+    if (lane == nw - 1) *total = w;
+  }
+  __syncthreads();
+  const T ex = (warp == 0 ? T(0) : warp_sums[warp - 1]) + inc - v;
+  __syncthreads();
+  return ex;
+}
+
+// ----------------------------------------------------------------------------
 // programmatic dependent launch: let the next grid in the stream start its
 // prologue; wait until the previous grid has completed and its writes are
 // visible

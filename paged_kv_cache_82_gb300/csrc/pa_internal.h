@@ -106,11 +106,11 @@ bool tc_prefill_supported(const AttnArgs& a);
 // query rows of one of its tiles (128 / group tokens x group heads)
 int tc_prefill_tile_rows(int group);
 bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
-// prefill tiles listed by the planner (n_atoms of them; tile_ctr zeroed),
-// one persistent CTA per SM
+// the step's prefill tiles, listed by the kernel itself (self_plan) or by
+// the planner (atoms, n_atoms); one persistent CTA per SM
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
-                              const int4* atoms, const int* n_atoms,
-                              int* tile_ctr, int max_atoms, int num_sms,
+                              bool self_plan, const int4* atoms,
+                              const int* n_atoms, int max_atoms, int num_sms,
                               cudaStream_t stream);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge

@@ -163,6 +163,18 @@ def test_decode_batch_around_in_kernel_plan_limit(batch):
     _check_step(_custom(seq_q, 32, 8, write_new=True))
 
 
+@pytest.mark.parametrize("batch", [511, 600])
+def test_mixed_batch_around_in_kernel_plan_limit(batch):
+    # decodes next to one prefill chunk: up to 512 requests both kernels
+    # plan themselves, beyond that the planner lists the prefill tiles for
+    # the tensor-core kernel and cuts the decode work
+    rng = np.random.default_rng(batch)
+    seq_q = [(int(L), int(n)) for L, n in zip(rng.integers(20, 150, size=batch),
+                                              rng.integers(1, 5, size=batch))]
+    seq_q.append((700, 300))
+    _check_step(_custom(seq_q, 32, 8, write_new=True))
+
+
 @pytest.mark.parametrize("cache_dtype", ["bf16", "e4m3"])
 def test_one_long_sequence_split_over_many_ctas(cache_dtype):
     # every KV head's segment is cut by dozens of CTA boundaries
@@ -250,11 +262,16 @@ def test_launches_per_step_kind():
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (40, 1)], 32, 8))
     assert pa.pa_launch_count() - n0 == 2
-    # K/V write + a step with bf16 prefill tiles: planner, tensor-core
-    # prefill kernel, attention kernel, merge
+    # K/V write + a step with bf16 prefill tiles: the tensor-core prefill
+    # kernel and the attention kernel plan themselves, then the merge
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (100, 64)], 32, 8, write_new=True))
-    assert pa.pa_launch_count() - n0 == 5
+    assert pa.pa_launch_count() - n0 == 4
+    # FP8 cache with prefill tiles: planner, attention kernel, merge
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 1), (100, 64)], 32, 8, cache_dtype="e4m3",
+                     write_new=True))
+    assert pa.pa_launch_count() - n0 == 4
 
 
 def test_bitwise_determinism_and_block_relabelling():
