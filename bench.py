@@ -320,7 +320,8 @@ def run_ours(args):
 
     if args.only != "all":
         wl = {"decode": workloads.config2, "mixed": workloads.config4,
-              "prefill": workloads.prefill_chunk}[args.only]()
+              "prefill": workloads.prefill_chunk, "mha": workloads.config3,
+              "fp8long": workloads.config5}[args.only]()
         d = _device_inputs(wl, dev)
         step_ms, kern_ms, _ = _time_steps(pa, wl, d, args.steps, args.warmup,
                                           flush)
@@ -517,7 +518,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill"],
+    ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill",
+                                       "mha", "fp8long"],
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
                          "line")

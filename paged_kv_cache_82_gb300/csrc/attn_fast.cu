@@ -45,6 +45,9 @@ constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
 // requests of a step the attention kernel plans itself (narrow / wide build)
 constexpr int kSelfPlanMaxSeqs = 1024;
 constexpr int kSelfPlanMaxSeqsWide = 512;
+constexpr int kHg = 4;            // KV heads of a head-group decode item
+constexpr int kHgMaxSeqs = 512;   // requests of a step the head-group kernel takes
+constexpr int kHgPartRows = 32;   // partial rows per slot there: kHg heads x 8
 
 #ifndef PA_PRODUCER_PAGES
 #define PA_PRODUCER_PAGES 4     // pages the producer issues per step (2 lanes each)
@@ -138,6 +141,7 @@ struct FastParams {
   float out_scale;    // 1, or v_scale for FP8
   int self_plan;      // 1: every CTA plans its own range
   int dec_rows_max;   // decode-class requests have at most this many rows
+  int seg_heads;      // KV heads per decode segment (1, or kHg: head groups)
 };
 
 // ---------------------------------------------------------------------------
@@ -1396,7 +1400,8 @@ __device__ long long plan_prefix(const FastParams& p, long long* dec0,
       }
     }
     const long long ex =
-        block_scan_excl<long long>((long long)dl * p.num_kv_heads, scan_tot, scan_ws);
+        block_scan_excl<long long>((long long)dl * (p.num_kv_heads / p.seg_heads),
+                                   scan_tot, scan_ws);
     const long long tot = *scan_tot;
     __syncthreads();
     if (r < p.num_seqs) {
@@ -1466,8 +1471,10 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_launch_dependents();  // the merge may be scheduled behind this grid
   pdl_wait();               // the planner (and everything before it) is done
+  // the merge may be scheduled behind this grid; it reads the step's
+  // metadata before its own wait, which is safe from here on
+  pdl_launch_dependents();
   ItemSource src{};
   src.self = false;
   {
@@ -1483,7 +1490,7 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
       src.declen = declen;
       src.rows = rows;
       src.B = p.num_seqs;
-      src.H = p.num_kv_heads;
+      src.H = p.num_kv_heads / p.seg_heads;
       src.b = blockIdx.x;
       src.lo = src.hi = 0;
       if ((int)blockIdx.x < g_eff && C > 0) {
@@ -1526,8 +1533,10 @@ attn_fast_kernel(const __grid_constant__ CUtensorMap tmap_k,
         const int buf = (j0 >> 5) & 1;
         const int nidx = j0 + 32 + lane;
         const int nreg = nidx < n ? __ldg(bt + nidx) : 0;
-        // lanes 2k and 2k+1 issue page j + k of each group of PP pages
+        // lanes 2k and 2k+1 issue page j + k of each group of PP pages (PP
+        // distinct ring slots)
         constexpr int PP = PA_PRODUCER_PAGES;
+        static_assert(PP <= S, "pages per producer step exceed the ring");
         constexpr unsigned kMask = (PP >= 16) ? 0xFFFFFFFFu : ((1u << (2 * PP)) - 1u);
         if (lane < 2 * PP) {
           const int* cur = sm.ids + buf * 32;
@@ -1660,15 +1669,15 @@ merge_kernel(FastParams p) {
 }
 
 // Split-K merge of a self-planned decode step: CTA b looks at the range
-// boundary b; if it is the first boundary inside a segment it combines that
-// segment's parts -- the tail of range b-1 (slot 2(b-1)+1) and the heads of
-// ranges b, b+1, ... (slots 2k) -- in that order.
+// boundary b; if it cuts a segment, the CTA merges its share of that
+// segment's rows from the segment's parts, combined in a fixed order.
 template <typename TOut>
 __global__ void __launch_bounds__(128)
 merge_self_kernel(FastParams p) {
   extern __shared__ long long mplan[];
   __shared__ long long scan[34];
-  pdl_wait();
+  // The plan needs only the step's metadata, complete before the attention
+  // grid let this grid start: it overlaps the attention kernel.
   long long* dec0 = mplan;
   int* declen = reinterpret_cast<int*>(dec0 + p.num_seqs);
   int* rows = declen + p.num_seqs;
@@ -1677,52 +1686,329 @@ merge_self_kernel(FastParams p) {
   const int b = blockIdx.x;
   if (b == 0 || b >= g_eff || C <= 0) return;
   const long long lo_b = (long long)b * C / g_eff;
-  const long long lo_p = (long long)(b - 1) * C / g_eff;
   int r = request_of(dec0, p.num_seqs, lo_b);
   while (r < p.num_seqs && declen[r] == 0) ++r;
   if (r >= p.num_seqs) return;
   const int dl = declen[r];
   const int g = (int)((lo_b - dec0[r]) / dl);
   const long long ss = dec0[r] + (long long)g * dl, se = ss + dl;
-  if (ss >= lo_b || ss < lo_p) return;  // not cut here, or cut earlier
-  // parts in order: slot 2(b-1)+1, then 2k for the ranges b..k_end-1 that
-  // begin inside the segment
-  int k_end = b + 1;
-  while (k_end < g_eff && (long long)k_end * C / g_eff < se) ++k_end;
-  const int np = 1 + (k_end - b);
+  if (ss >= lo_b) return;  // boundary b does not cut a segment
+  // the boundaries that cut this segment: b0 .. b1-1.  Its parts, in order:
+  // the tail piece of range b0-1 (slot 2(b0-1)+1), then the head pieces of
+  // ranges b0 .. b1-1 (slots 2k).  The b1-b0 CTAs of these boundaries share
+  // the segment's rows.
+  int b0 = b;
+  while (b0 > 1 && (long long)(b0 - 1) * C / g_eff > ss) --b0;
+  int b1 = b + 1;
+  while (b1 < g_eff && (long long)b1 * C / g_eff < se) ++b1;
+  const int np = 1 + (b1 - b0);
   const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
                               p.max_seq_len, p.max_blocks_per_seq);
-  const int lane = threadIdx.x & 31;
-  for (int rr = threadIdx.x >> 5; rr < rows[r]; rr += blockDim.x >> 5) {
+  const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  pdl_wait();  // the attention grid has finished writing the parts
+  // rows of every KV head of the segment (one head, or a head group whose
+  // partial slots hold kHg x 8 rows)
+  const int sh = p.seg_heads;
+  const int part_rows = sh == 1 ? 16 : kHgPartRows;
+  const int total = sh * rows[r];
+  for (int x = (b - b0) * nwarps + (threadIdx.x >> 5); x < total;
+       x += (b1 - b0) * nwarps) {
+    const int w = x / rows[r], rr = x - w * rows[r];
+    const int prow = sh == 1 ? rr : w * 8 + rr;
     const int i = rr / p.group;
-    const int h = g * p.group + (rr - i * p.group);
+    const int h = (g * sh + w) * p.group + (rr - i * p.group);
     const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
+    // partial row of part s: slot 2(b0-1)+1 for s = 0, else slot 2(b0+s-1)
+    const int64_t pr_tail = (int64_t)(2 * (b0 - 1) + 1) * part_rows + prow;
+    const int64_t pr_head = (int64_t)(2 * b0) * part_rows + prow;
+    const int64_t pr_step = 2 * (int64_t)part_rows;
+    // M and the denominator with the parts spread over the lanes
     float M = -INFINITY;
     for (int s = lane; s < np; s += 32) {
-      const int slot = s == 0 ? 2 * (b - 1) + 1 : 2 * (b + s - 1);
-      M = fmaxf(M, p.ws_ml[((int64_t)slot * 16 + rr) * 2]);
+      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+      M = fmaxf(M, __ldg(p.ws_ml + pr * 2));
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float den = 0.f;
+    for (int s = lane; s < np; s += 32) {
+      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+      const float ms = __ldg(p.ws_ml + pr * 2);
+      if (ms != -INFINITY) den += exp2f(ms - M) * __ldg(p.ws_ml + pr * 2 + 1);
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
+    // the numerator in part order, loads of several parts in flight
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
     for (int s = 0; s < np; ++s) {
-      const int slot = s == 0 ? 2 * (b - 1) + 1 : 2 * (b + s - 1);
-      const int64_t pr = (int64_t)slot * 16 + rr;
-      const float ms = p.ws_ml[pr * 2];
-      if (ms == -INFINITY) continue;  // a part with no visible key
-      const float w = exp2f(ms - M);
-      den += w * p.ws_ml[pr * 2 + 1];
-      const float4 v = *reinterpret_cast<const float4*>(p.ws_acc + pr * 128 + 4 * lane);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
+      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+      const float ms = __ldg(p.ws_ml + pr * 2);
+      const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+      const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
+      acc[0] += wgt * v.x;
+      acc[1] += wgt * v.y;
+      acc[2] += wgt * v.z;
+      acc[3] += wgt * v.w;
     }
     const float inv = p.out_scale / den;
     TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// Decode steps by head groups.  An item is a range of key pages of one
+// (request, group of kHg KV heads).  The group's kHg pages of a block lie
+// next to each other in the cache, so one TMA box per cache brings all of
+// them, and consumer warp w owns KV head kHg * group + w for the whole item:
+// its own query rows and softmax state, no merge across warps.  A quarter of
+// the TMA instructions per byte of the one-head items; used for steps of
+// <= 8-row requests whose KV head count is a multiple of kHg.
+// ---------------------------------------------------------------------------
+template <int kKind>
+struct HgLayout {
+  using Tr = Traits<kKind>;
+  static constexpr int kPageBytes = Tr::kPageBytes;          // one KV head
+  static constexpr int kStageBytes = 2 * kHg * kPageBytes;   // K, V of a group
+  static constexpr int kStages = 3 * 32768 / kStageBytes;    // 96 KiB ring
+  static constexpr int kRing = 0;
+  static constexpr int kBars = kRing + kStages * kStageBytes;
+  static constexpr int kIds = kBars + 8 * 2 * kStages;       // int [2][32]
+  static constexpr int kAbort = kIds + 2 * 32 * 4;
+  static constexpr int kPlan = kAbort + 16;  // dec0, declen, rows per request
+  static constexpr int kScan = kPlan + kHgMaxSeqs * 16;
+  static constexpr int kBytes = kScan + 34 * 8;
+  static constexpr int kSmemBytes = 1024 + kBytes;           // + alignment slack
+};
+
+// One consumer warp's part of an item: every page of the item, its own KV
+// head g; the output rows of that head (or its partial, slot >= 0).
+template <int kKind>
+__device__ void consume_hg_item(const FastParams& p, uint32_t ring,
+                                uint32_t bars, volatile int* abort_flag,
+                                const ReqMeta& rm, int g, int slot, int page0,
+                                int npages, int rows, uint32_t c0, int warp,
+                                int lane) {
+  using Ly = HgLayout<kKind>;
+  constexpr int S = Ly::kStages;
+  const int rq = lane >> 2, c = lane & 3;
+  const int G = p.group;
+  uint32_t qa[8][4];
+  float rscale[2];
+  load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
+  const int lim = rq < rows ? rm.L - rm.n + rq / G : rm.L - 1;
+  int min_lim = rq < rows ? lim : INT_MAX;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1)
+    min_lim = min(min_lim, __shfl_xor_sync(~0u, min_lim, d));
+  min_lim = min(min_lim, rm.L - 1);
+  const float ss = p.score_scale * rscale[0];
+
+  NarrowState st;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+    st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
+  st.m = -INFINITY;
+  st.l = 0.f;
+  for (int j = 0; j < npages; ++j) {
+    const uint32_t cc = c0 + j;
+    const int s = cc % S;
+    if (!__all_sync(~0u, mbar_wait_bounded(bars + 8 * s, (cc / S) & 1))) {
+      if (lane == 0) {
+        flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return;
+    }
+    const int key0 = (page0 + j) * kBS;
+    const int valid = min(kBS, rm.L - key0);
+    const bool need_mask = key0 + kBS - 1 > min_lim;
+    const uint32_t kb = ring + s * Ly::kStageBytes + warp * Ly::kPageBytes;
+    process_page_narrow<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
+                               valid, need_mask, lim, ss, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (S + s));
+  }
+  st.l += __shfl_xor_sync(~0u, st.l, 1);
+  st.l += __shfl_xor_sync(~0u, st.l, 2);
+  // row 2c + h of O^T is held here; its (m, l) by lanes 4 (2c + h) ..
+  float mq[2], lq[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    mq[h] = __shfl_sync(~0u, st.m, (2 * c + h) * 4);
+    lq[h] = __shfl_sync(~0u, st.l, (2 * c + h) * 4);
+  }
+  const int Hq = p.num_q_heads;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int qrow = 2 * c + (e & 1);
+      if (qrow >= rows) continue;
+      const int col = narrow_col<kKind>(mt, e, rq);
+      if (slot < 0) {
+        const int i = qrow / G;
+        const int h = g * G + (qrow - i * G);
+        const int64_t orow = (int64_t)(rm.q0 + i) * Hq + h;
+        store_out<OutT<kKind>>(p.out, orow * 128 + col,
+                               st.o[mt][e] / lq[e & 1] * p.out_scale);
+      } else {
+        const int64_t pr = (int64_t)slot * kHgPartRows + warp * 8 + qrow;
+        p.ws_acc[pr * 128 + col] = st.o[mt][e];
+        if (mt == 0 && (e >> 1) == 0 && rq == 0) {
+          p.ws_ml[pr * 2 + 0] = mq[e & 1];
+          p.ws_ml[pr * 2 + 1] = lq[e & 1];
+        }
+      }
+    }
+  }
+}
+
+template <int kKind>
+__global__ void __launch_bounds__(kThreads, PA_CTAS_PER_SM)
+attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ FastParams p) {
+  using Tr = Traits<kKind>;
+  using Ly = HgLayout<kKind>;
+  constexpr int S = Ly::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sp = smem_raw + (base - raw);
+  const uint32_t bars = base + Ly::kBars;  // full[S], then empty[S]
+  int* ids = reinterpret_cast<int*>(sp + Ly::kIds);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sp + Ly::kAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(bars + 8 * i, 1);
+      mbar_init(bars + 8 * (S + i), kHg);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_wait();               // everything before this grid is done
+  pdl_launch_dependents();  // the merge may be scheduled behind this grid
+  // this CTA's stream-K range over the (request, head group) segments
+  long long* dec0 = reinterpret_cast<long long*>(sp + Ly::kPlan);
+  int* declen = reinterpret_cast<int*>(dec0 + kHgMaxSeqs);
+  int* rows = declen + kHgMaxSeqs;
+  long long* scan = reinterpret_cast<long long*>(sp + Ly::kScan);
+  const long long C = plan_prefix(p, dec0, declen, rows, scan + 32, scan);
+  const int g_eff = self_plan_grid(C, gridDim.x);
+  ItemSource src{};
+  src.self = true;
+  src.dec0 = dec0;
+  src.declen = declen;
+  src.rows = rows;
+  src.B = p.num_seqs;
+  src.H = p.num_kv_heads / kHg;
+  src.b = blockIdx.x;
+  src.lo = src.hi = 0;
+  if ((int)blockIdx.x < g_eff && C > 0) {
+    src.lo = (long long)blockIdx.x * C / g_eff;
+    src.hi = (long long)(blockIdx.x + 1) * C / g_eff;
+  }
+  src.cur = src.lo;
+  src.r = p.num_seqs > 0 ? request_of(dec0, p.num_seqs, src.lo) : 0;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------ producer ------------------------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_k);
+      tma_prefetch_desc(&tmap_v);
+    }
+    uint32_t c = 0;  // stages issued
+    int go = 1;
+    int4 rec0, rec1;
+    while (go && src.next(rec0, rec1)) {
+      const int32_t* bt =
+          p.block_tables + (int64_t)rec0.x * p.max_blocks_per_seq + rec1.x;
+      // block ids through shared memory 32 at a time; lanes 2k, 2k+1 issue
+      // the K and V boxes of page k of each group of PP pages
+      const int n = rec1.y - rec1.x;
+      ids[lane] = lane < n ? __ldg(bt + lane) : 0;
+      __syncwarp();
+      for (int j0 = 0; j0 < n && go; j0 += 32) {
+        const int buf = (j0 >> 5) & 1;
+        const int nidx = j0 + 32 + lane;
+        const int nreg = nidx < n ? __ldg(bt + nidx) : 0;
+        // pages of one step go to distinct ring slots (a lane must never wait
+        // for the slot another lane of the same step is about to fill)
+        constexpr int PP = PA_PRODUCER_PAGES < S ? PA_PRODUCER_PAGES : S;
+        constexpr unsigned kMask = (PP >= 16) ? 0xFFFFFFFFu : ((1u << (2 * PP)) - 1u);
+        if (lane < 2 * PP) {
+          const int* cur = ids + buf * 32;
+          const int cnt = min(32, n - j0);
+          const int kk = lane >> 1;
+          const int kv = lane & 1;
+          const CUtensorMap* map = kv ? &tmap_v : &tmap_k;
+          for (int jj = 0; jj < cnt; jj += PP) {
+            const bool mine = jj + kk < cnt;
+            const uint32_t cc = c + kk;
+            const int s = cc % S;
+            const bool ok = !mine || cc < (uint32_t)S ||
+                            mbar_wait_bounded(bars + 8 * (S + s), ((cc / S) - 1) & 1);
+            if (__any_sync(kMask, !ok)) {
+              if (lane == 0) {
+                flag_error(p.err, PA_DEV_ERR_TIMEOUT);
+                *abort_flag = 1;
+              }
+              go = 0;
+              break;
+            }
+            if (mine) {
+              int blk = cur[jj + kk];
+              if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                if (kv == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
+                blk = 0;
+              }
+              const int row = (blk * p.num_kv_heads + rec0.y * kHg) * kBS;
+              const uint32_t dst = base + Ly::kRing + s * Ly::kStageBytes +
+                                   kv * kHg * Ly::kPageBytes;
+              if (kv == 0) mbar_arrive_expect_tx(bars + 8 * s, Ly::kStageBytes);
+              __syncwarp(__activemask());
+              if constexpr (Tr::kFp8)
+                tma_load_2d(dst, map, bars + 8 * s, 0, row);
+              else
+                tma_load_3d(dst, map, bars + 8 * s, 0, 0, row);
+            }
+            c += min(PP, cnt - jj);
+          }
+        }
+        __syncwarp();
+        go = __shfl_sync(~0u, go, 0);
+        c = __shfl_sync(~0u, c, 0);
+        ids[(buf ^ 1) * 32 + lane] = nreg;
+        __syncwarp();
+      }
+    }
+    // after an abort, let the copies already in flight land before exiting
+    if (!go && lane == 0) {
+      const uint32_t from = c > (uint32_t)S ? c - S : 0;
+      for (uint32_t i = from; i < c; ++i)
+        mbar_wait_bounded(bars + 8 * (i % S), (i / S) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------ consumers -------------------------------
+  uint32_t c = 0;  // stages consumed (every warp reads every stage)
+  int4 rec0, rec1;
+  while (src.next(rec0, rec1)) {
+    if (consumers_sync_any(*abort_flag != 0)) break;
+    const ReqMeta rm = load_req(p.qsl, p.seq_lens, rec0.x, p.num_tokens,
+                                p.max_query_len, p.max_seq_len,
+                                p.max_blocks_per_seq);
+    consume_hg_item<kKind>(p, base + Ly::kRing, bars, abort_flag, rm,
+                           rec0.y * kHg + warp, rec0.w, rec1.x, rec1.y - rec1.x,
+                           rec1.z, c, warp, lane);
+    c += rec1.y - rec1.x;
   }
 }
 
@@ -1756,6 +2042,81 @@ cudaError_t prepare_kernel(int* grid) {
   }
   *grid = blocks_per_sm[dev] * sms[dev];
   return cudaSuccess;
+}
+
+template <int kKind>
+cudaError_t prepare_hg(int* grid) {
+  using Ly = HgLayout<kKind>;
+  static int blocks_per_sm[64] = {0};
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (blocks_per_sm[dev] == 0) {
+    e = cudaFuncSetAttribute(attn_decode_hg_kernel<kKind>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ly::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(attn_decode_hg_kernel<kKind>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &nb, attn_decode_hg_kernel<kKind>, kThreads, Ly::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int n_sm = 0;
+    e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n_sm;
+    blocks_per_sm[dev] = nb > 0 ? nb : 1;
+  }
+  *grid = blocks_per_sm[dev] * sms[dev];
+  return cudaSuccess;
+}
+
+// decode-only steps (<= 8 rows per request) in head groups: KV heads a
+// multiple of kHg, up to kHgMaxSeqs requests
+bool use_head_groups(const AttnArgs& a) {
+  const int G = a.num_q_heads / a.num_kv_heads;
+  return (int64_t)a.max_query_len * G <= 8 && a.num_kv_heads % kHg == 0 &&
+         a.num_seqs <= kHgMaxSeqs;
+}
+
+template <int kKind>
+cudaError_t launch_hg(const FastParams& fp, const AttnPlan& plan,
+                      const CUtensorMap& tk, const CUtensorMap& tv,
+                      cudaStream_t stream) {
+  int grid = 0;
+  cudaError_t e = prepare_hg<kKind>(&grid);
+  if (e != cudaSuccess) return e;
+  if (grid > plan.grid_max) grid = plan.grid_max;
+  FastParams f = fp;
+  f.self_plan = 1;
+  f.dec_rows_max = 8;
+  f.seg_heads = kHg;
+  const ProfileEvents& pe = profile_events();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pe.start == nullptr ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = HgLayout<kKind>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (pe.start) cudaEventRecord(pe.start, stream);
+  e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
+  if (pe.stop) cudaEventRecord(pe.stop, stream);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
+  e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 template <int kKind>
@@ -1833,6 +2194,10 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
 
 }  // namespace
 
+int decode_box_rows(const AttnArgs& a) {
+  return use_head_groups(a) ? kHg * kBS : kBS;
+}
+
 bool fast_path_supported(const AttnArgs& a) {
   if (a.head_dim != 128) return false;
   if (a.cache_dtype == PA_BF16 && a.q_dtype == PA_BF16) return true;
@@ -1871,10 +2236,11 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
   pl.off_seg_info = off;    off = up(off + (size_t)num_seqs * num_kv_heads * 8);
   pl.off_split = off;       off = up(off + (size_t)pl.max_slots * 16 + 16);
   pl.off_pref = off;        off = up(off + 16);
+  // partial slots of up to kHgPartRows rows (head-group items: kHg heads x 8)
   pl.off_acc = off;
-  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * 16 * head_dim * 4);
+  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * head_dim * 4);
   pl.off_ml = off;
-  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * 16 * 2 * 4);
+  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * 2 * 4);
   pl.total_bytes = off;
   return pl;
 }
@@ -1910,6 +2276,7 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
   fp.score_scale = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.0f);
   fp.out_scale = fp8 ? a.v_scale : 1.0f;
+  fp.seg_heads = 1;
 
   PlanArgs pa{};
   pa.qsl = a.query_start_loc;
@@ -1940,6 +2307,17 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.ws_ml = fp.ws_ml;
   pa.split_list = reinterpret_cast<int4*>(ws + plan.off_split + 16);
   pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
+  if (use_head_groups(a)) {
+    switch (a.cache_dtype == PA_BF16  ? kKindBF16
+            : a.cache_dtype == PA_F16 ? kKindF16
+            : a.q_dtype == PA_BF16    ? kKindFp8BF16
+                                      : kKindFp8F16) {
+      case kKindBF16: return launch_hg<kKindBF16>(fp, plan, tmap_k, tmap_v, stream);
+      case kKindF16: return launch_hg<kKindF16>(fp, plan, tmap_k, tmap_v, stream);
+      case kKindFp8BF16: return launch_hg<kKindFp8BF16>(fp, plan, tmap_k, tmap_v, stream);
+      default: return launch_hg<kKindFp8F16>(fp, plan, tmap_k, tmap_v, stream);
+    }
+  }
   if (a.cache_dtype == PA_BF16)
     return launch_kind<kKindBF16>(a, fp, pa, plan, tmap_k, tmap_v, tc, num_sms,
                                   stream);

@@ -132,7 +132,7 @@ bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
     if (segs == 1) {
       cuuint64_t dims[2] = {inner, rows};
       cuuint64_t strides[1] = {row_bytes};
-      cuuint32_t box[2] = {inner, PA_BLOCK_SIZE};
+      cuuint32_t box[2] = {inner, (cuuint32_t)decode_box_rows(a)};
       cuuint32_t es[2] = {1, 1};
       res = fn(maps[k], dt, 2, const_cast<void*>(ptrs[k]), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -141,7 +141,7 @@ bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
     } else {
       cuuint64_t dims[3] = {inner, segs, rows};
       cuuint64_t strides[2] = {128, row_bytes};
-      cuuint32_t box[3] = {inner, segs, PA_BLOCK_SIZE};
+      cuuint32_t box[3] = {inner, segs, (cuuint32_t)decode_box_rows(a)};
       cuuint32_t es[3] = {1, 1, 1};
       res = fn(maps[k], dt, 3, const_cast<void*>(ptrs[k]), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -42,7 +42,7 @@ constexpr int kDecodeMaxRows = 16;   // q_len * group rows handled by one warp
 // rows of a prefill tile: 16 per consumer warp
 constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
 
-constexpr int kMaxCtasPerSm = 4;     // bound used to size the workspace
+constexpr int kMaxCtasPerSm = 2;     // resident attention CTAs per SM (grid bound)
 
 struct AttnPlan {
   int group;            // Hq / Hkv
@@ -121,6 +121,11 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
 
 // warp-per-row kernel for the remaining types / shapes
 cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream);
+
+// Rows of one TMA box of the caches for the attention kernels of this step:
+// 16 (one page), or 64 (the pages of four KV heads of a block) when the step
+// runs in head groups.
+int decode_box_rows(const AttnArgs& a);
 
 // Encode the tensor maps of the two caches for the fast path.
 bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tmap_k,

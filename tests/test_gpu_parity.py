@@ -163,6 +163,20 @@ def test_decode_batch_around_in_kernel_plan_limit(batch):
     _check_step(_custom(seq_q, 32, 8, write_new=True))
 
 
+@pytest.mark.parametrize("Hq,Hkv,cache_dtype", [
+    (16, 4, "bf16"), (8, 8, "f16"), (36, 12, "bf16"), (64, 8, "e4m3"),
+])
+def test_decode_head_groups(Hq, Hkv, cache_dtype):
+    # decode steps whose KV head count is a multiple of 4 run four KV heads
+    # per work item (one TMA box for the four pages of a block), with 4, 1,
+    # 3 and 8 query rows per KV head
+    rng = np.random.default_rng(Hq * Hkv)
+    seq_q = [(int(L), 1) for L in rng.integers(1, 900, size=37)]
+    dtype = "f16" if cache_dtype == "f16" else "bf16"
+    _check_step(_custom(seq_q, Hq, Hkv, dtype=dtype, cache_dtype=cache_dtype,
+                        write_new=True))
+
+
 @pytest.mark.parametrize("batch", [511, 600])
 def test_mixed_batch_around_in_kernel_plan_limit(batch):
     # decodes next to one prefill chunk: up to 512 requests both kernels
