@@ -2078,15 +2078,19 @@ cudaError_t prepare_hg(int* grid) {
 
 // decode-only steps (<= 8 rows per request) in head groups: KV heads a
 // multiple of kHg, up to kHgMaxSeqs requests
-bool use_head_groups(const AttnArgs& a) {
+// Steps whose decode work runs in KV-head groups: KV heads a multiple of
+// kHg, at most kHgMaxSeqs requests, and every request of more than 8 query
+// rows (if any) handled by the tensor-core prefill kernel.
+bool use_head_groups(const AttnArgs& a, bool tc) {
   const int G = a.num_q_heads / a.num_kv_heads;
-  return (int64_t)a.max_query_len * G <= 8 && a.num_kv_heads % kHg == 0 &&
-         a.num_seqs <= kHgMaxSeqs;
+  if (a.num_kv_heads % kHg != 0 || a.num_seqs > kHgMaxSeqs) return false;
+  return (int64_t)a.max_query_len * G <= 8 || tc;
 }
 
 template <int kKind>
-cudaError_t launch_hg(const FastParams& fp, const AttnPlan& plan,
-                      const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
+                      const AttnPlan& plan, const CUtensorMap& tk,
+                      const CUtensorMap& tv, const TcMaps* tc, int num_sms,
                       cudaStream_t stream) {
   int grid = 0;
   cudaError_t e = prepare_hg<kKind>(&grid);
@@ -2108,6 +2112,12 @@ cudaError_t launch_hg(const FastParams& fp, const AttnPlan& plan,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (pe.start) cudaEventRecord(pe.start, stream);
+  if (tc) {
+    // requests of more than 8 query rows: prefill tiles on the tensor cores
+    e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
+                          num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
@@ -2164,7 +2174,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   if (tc) {
     // prefill tiles on the tensor cores, ahead of the decode work
     e = launch_prefill_tc(a, *tc, f.self_plan != 0, pa.atoms, pa.n_atoms_out,
-                          pa.max_atoms, num_sms, stream);
+                          pa.max_atoms, kDecodeMaxRows, num_sms, stream);
     if (e != cudaSuccess) return e;
   }
   if (wide) {
@@ -2194,8 +2204,8 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
 
 }  // namespace
 
-int decode_box_rows(const AttnArgs& a) {
-  return use_head_groups(a) ? kHg * kBS : kBS;
+int decode_box_rows(const AttnArgs& a, bool tc) {
+  return use_head_groups(a, tc) ? kHg * kBS : kBS;
 }
 
 bool fast_path_supported(const AttnArgs& a) {
@@ -2307,15 +2317,20 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.ws_ml = fp.ws_ml;
   pa.split_list = reinterpret_cast<int4*>(ws + plan.off_split + 16);
   pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
-  if (use_head_groups(a)) {
+  if (use_head_groups(a, tc != nullptr)) {
+    const TcMaps* t = plan.has_prefill ? tc : nullptr;
     switch (a.cache_dtype == PA_BF16  ? kKindBF16
             : a.cache_dtype == PA_F16 ? kKindF16
             : a.q_dtype == PA_BF16    ? kKindFp8BF16
                                       : kKindFp8F16) {
-      case kKindBF16: return launch_hg<kKindBF16>(fp, plan, tmap_k, tmap_v, stream);
-      case kKindF16: return launch_hg<kKindF16>(fp, plan, tmap_k, tmap_v, stream);
-      case kKindFp8BF16: return launch_hg<kKindFp8BF16>(fp, plan, tmap_k, tmap_v, stream);
-      default: return launch_hg<kKindFp8F16>(fp, plan, tmap_k, tmap_v, stream);
+      case kKindBF16:
+        return launch_hg<kKindBF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindF16:
+        return launch_hg<kKindF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindFp8BF16:
+        return launch_hg<kKindFp8BF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      default:
+        return launch_hg<kKindFp8F16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
     }
   }
   if (a.cache_dtype == PA_BF16)

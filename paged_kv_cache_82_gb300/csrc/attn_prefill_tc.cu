@@ -709,7 +709,8 @@ int tc_prefill_tile_rows(int group) { return (kTcRows / group) * group; }
 
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
-                              const int* n_atoms, int max_atoms, int num_sms,
+                              const int* n_atoms, int max_atoms,
+                              int dec_rows_max, int num_sms,
                               cudaStream_t stream) {
   TcParams p{};
   p.out = a.out;
@@ -720,7 +721,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
   p.atoms = atoms;
   p.n_atoms = n_atoms;
   p.max_atoms = max_atoms;
-  p.dec_rows_max = kDecodeMaxRows;
+  p.dec_rows_max = dec_rows_max;
   p.err = a.err;
   p.num_tokens = a.num_tokens;
   p.num_blocks = a.num_blocks;

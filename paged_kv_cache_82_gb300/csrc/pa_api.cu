@@ -112,7 +112,7 @@ ProfileEvents& profile_events() { return t_profile; }
 void count_launch() { ++t_launches; }
 
 bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
-                              CUtensorMap* tv) {
+                              CUtensorMap* tv, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int eb = elem_bytes(a.cache_dtype);
@@ -132,7 +132,7 @@ bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
     if (segs == 1) {
       cuuint64_t dims[2] = {inner, rows};
       cuuint64_t strides[1] = {row_bytes};
-      cuuint32_t box[2] = {inner, (cuuint32_t)decode_box_rows(a)};
+      cuuint32_t box[2] = {inner, (cuuint32_t)box_rows};
       cuuint32_t es[2] = {1, 1};
       res = fn(maps[k], dt, 2, const_cast<void*>(ptrs[k]), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -141,7 +141,7 @@ bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
     } else {
       cuuint64_t dims[3] = {inner, segs, rows};
       cuuint64_t strides[2] = {128, row_bytes};
-      cuuint32_t box[3] = {inner, segs, (cuuint32_t)decode_box_rows(a)};
+      cuuint32_t box[3] = {inner, segs, (cuuint32_t)box_rows};
       cuuint32_t es[3] = {1, 1, 1};
       res = fn(maps[k], dt, 3, const_cast<void*>(ptrs[k]), dims, strides, box,
                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -390,13 +390,14 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (fast) {
-    CUtensorMap tk, tv;
-    if (!encode_cache_tensor_maps(a, &tk, &tv)) return PA_ERR_CUDA;
     // prefill tiles go to the tensor-core kernel where it takes the step's
     // types (else the attention kernel runs them on the warp-level MMA)
     TcMaps tc;
     const bool use_tc = plan.has_prefill && tc_prefill_supported(a) &&
                         encode_prefill_tensor_maps(a, &tc);
+    CUtensorMap tk, tv;
+    if (!encode_cache_tensor_maps(a, &tk, &tv, decode_box_rows(a, use_tc)))
+      return PA_ERR_CUDA;
     e = launch_attention_fast(a, plan, tk, tv, use_tc ? &tc : nullptr,
                               di->num_sms, s);
   } else {

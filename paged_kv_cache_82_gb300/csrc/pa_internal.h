@@ -106,11 +106,13 @@ bool tc_prefill_supported(const AttnArgs& a);
 // query rows of one of its tiles (128 / group tokens x group heads)
 int tc_prefill_tile_rows(int group);
 bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
-// the step's prefill tiles, listed by the kernel itself (self_plan) or by
-// the planner (atoms, n_atoms); one persistent CTA per SM
+// the step's prefill tiles (requests of more than dec_rows_max query rows),
+// listed by the kernel itself (self_plan) or by the planner (atoms,
+// n_atoms); one persistent CTA per SM
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
-                              const int* n_atoms, int max_atoms, int num_sms,
+                              const int* n_atoms, int max_atoms,
+                              int dec_rows_max, int num_sms,
                               cudaStream_t stream);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge
@@ -125,10 +127,12 @@ cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream);
 // Rows of one TMA box of the caches for the attention kernels of this step:
 // 16 (one page), or 64 (the pages of four KV heads of a block) when the step
 // runs in head groups.
-int decode_box_rows(const AttnArgs& a);
+// tc: the step's prefill tiles go to the tensor-core kernel
+int decode_box_rows(const AttnArgs& a, bool tc);
 
-// Encode the tensor maps of the two caches for the fast path.
+// Encode the tensor maps of the two caches for the fast path (boxes of
+// box_rows rows of 128-byte segments).
 bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tmap_k,
-                              CUtensorMap* tmap_v);
+                              CUtensorMap* tmap_v, int box_rows);
 
 }  // namespace pa
