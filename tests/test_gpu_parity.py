@@ -220,6 +220,16 @@ def test_prefill_tiles(Hq, Hkv, seq_q, dtype):
     _check_step(_custom(seq_q, Hq, Hkv, dtype=dtype, write_new=True))
 
 
+@pytest.mark.parametrize("cache_dtype,dtype", [("bf16", "bf16"), ("f16", "f16")])
+def test_mixed_step_routing_by_rows(cache_dtype, dtype):
+    # KV heads a multiple of 4 with a long prefill: requests of <= 8 rows run
+    # on the head-group decode kernel, a 12-row (3-token) request and the
+    # prefill on the tensor-core kernel
+    seq_q = [(300, 3), (500, 1), (33, 2), (900, 40), (64, 1), (1200, 200)]
+    _check_step(_custom(seq_q, 32, 8, dtype=dtype, cache_dtype=cache_dtype,
+                        write_new=True))
+
+
 def test_prefill_row_max_growing_across_chunks():
     # with scores 11x larger than 1/sqrt(D) gives, row maxima keep growing
     # from chunk to chunk, so the running output is rescaled many times
