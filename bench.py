@@ -229,29 +229,42 @@ def _time_steps(pa, wl, d, steps, warmup, flush):
 
 def _e2e(pa, wl, d, steps, warmup):
     """Same step through the public API from pinned host buffers: per step the
-    host->device copy of q and the metadata, the step, and the device->host
-    copy of the output, all inside the timed region."""
+    host->device copy of the step's inputs (q, the metadata, and the new K/V
+    and slots when the step writes them) packed in one pinned buffer, the
+    step, and the device->host copy of the output, all inside the timed
+    region."""
     import torch
     md = d["md"]
-    host = {
-        "q": wl.q.pin_memory(),
-        "bt": torch.from_numpy(md["block_tables"]).pin_memory(),
-        "sl": torch.from_numpy(md["seq_lens"]).pin_memory(),
-        "qsl": torch.from_numpy(md["query_start_loc"]).pin_memory(),
-        "slots": torch.from_numpy(md["slot_mapping"]).pin_memory(),
+    parts = {
+        "q": wl.q,
+        "bt": torch.from_numpy(md["block_tables"]),
+        "sl": torch.from_numpy(md["seq_lens"]),
+        "qsl": torch.from_numpy(md["query_start_loc"]),
     }
     if wl.write_new:
-        host["key"] = wl.key.pin_memory()
-        host["value"] = wl.value.pin_memory()
+        parts["slots"] = torch.from_numpy(md["slot_mapping"])
+        parts["key"] = wl.key
+        parts["value"] = wl.value
+    # one pinned staging buffer and one device buffer, 256-byte aligned views
+    offs, total = {}, 0
+    for k, t in parts.items():
+        offs[k] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=d["q"].device)
+    dd = dict(d)
+    for k, t in parts.items():
+        n = t.numel() * t.element_size()
+        host_buf[offs[k]:offs[k] + n].copy_(t.contiguous().view(-1).view(torch.uint8))
+        dd[k] = dev_buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
     out_h = torch.empty(d["out"].shape, dtype=d["out"].dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in parts.values())
     d2h = out_h.numel() * out_h.element_size()
 
     def one():
-        for k, t in host.items():
-            d[k].copy_(t, non_blocking=True)
-        _step(pa, wl, d)
-        out_h.copy_(d["out"], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
+        _step(pa, wl, dd)
+        out_h.copy_(dd["out"], non_blocking=True)
 
     for _ in range(warmup):
         one()
