@@ -424,6 +424,27 @@ def run_ours(args):
     }
     del d4
 
+    # ---- the other decode workloads of the scope (kernel and step TB/s)
+    others = {}
+    for name, make in (("mha_fp16_32x8192", workloads.config3),
+                       ("fp8_long_context_70b", workloads.config5)):
+        wlo = make()
+        do = _device_inputs(wlo, dev)
+        o_step, o_kern, _ = _time_steps(pa, wlo, do, max(3, args.steps // 10),
+                                        args.warmup, flush)
+        flags = pa.pa_get_device_error()
+        if flags:
+            raise RuntimeError(f"device error flags 0x{flags:x} ({name})")
+        ob = wlo.kv_bytes() + wlo.qo_bytes()
+        others[name] = {
+            "workload": wlo.description,
+            "bytes": ob,
+            "kernel_tbs": ob / (statistics.mean(o_kern) * 1e-3) / 1e12,
+            "step_tbs": ob / (statistics.mean(o_step) * 1e-3) / 1e12,
+            "frac_of_measured_hbm": ob / (statistics.mean(o_kern) * 1e-3) / 1e9 / peak_gbs,
+        }
+        del do, wlo
+
     # ---- prefill tiles alone: one long chunked prefill (tensor cores)
     wlp = workloads.prefill_chunk()
     dp = _device_inputs(wlp, dev)
@@ -489,6 +510,7 @@ def run_ours(args):
         "clocks": clocks,
         "mixed_step": mixed,
         "prefill_step": prefill,
+        "other_decodes": others,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -42,6 +42,13 @@ namespace {
 #define PA_NARROW_MIN_BLOCKS 3  // resident CTAs per SM, <= 8-row kernel
 #endif
 constexpr int kMinUnitsPerCta = 8;  // smallest cost range given to a CTA
+#ifndef PA_SEG_COST
+#define PA_SEG_COST 2
+#endif
+// Cost units a decode segment adds to the in-kernel plan besides its pages
+// (the fixed work of starting an item: its Q rows, block ids, state): they
+// sit on the line ahead of the segment's pages.
+constexpr int kSegCost = PA_SEG_COST;
 // requests of a step the attention kernel plans itself (narrow / wide build)
 constexpr int kSelfPlanMaxSeqs = 1024;
 constexpr int kSelfPlanMaxSeqsWide = 512;
@@ -1360,10 +1367,15 @@ struct ItemSource {
     while (r < B && declen[r] == 0) ++r;
     if (r >= B) return false;
     const long long rs = dec0[r];
-    const int dl = declen[r];
+    const int dl = declen[r];  // segment length on the line: kSegCost + pages
     const int g = (int)((cur - rs) / dl);
     const long long ss = rs + (long long)g * dl, se = ss + dl;
     const long long pe = se < hi ? se : hi;
+    // pages of the piece (its line range minus the segment's leading cost
+    // units; a piece inside those units has none and writes an empty part)
+    const long long p0 = ss + kSegCost;
+    const int pg_begin = (int)(cur > p0 ? cur - p0 : 0);
+    const int pg_end = (int)(pe > p0 ? pe - p0 : 0);
     // a piece that continues a segment begun in an earlier range is this
     // CTA's "head" part (slot 2b); one that continues into a later range is
     // its "tail" part (slot 2b + 1)
@@ -1371,15 +1383,16 @@ struct ItemSource {
     const bool after = pe == hi && se > hi;
     const int slot = before ? 2 * b : (after ? 2 * b + 1 : -1);
     rec0 = make_int4(r, g, kItemDecode, slot);
-    rec1 = make_int4((int)(cur - ss), (int)(pe - ss), rows[r], 0);
+    rec1 = make_int4(pg_begin, pg_end, rows[r], 0);
     cur = pe;
     if (pe == se && g + 1 == H) ++r;
     return true;
   }
 };
 
-// Per-request decode pages of the step and their prefix (units of pages x
-// KV heads) into shared memory; all threads of the block take part.
+// Per-request decode segments of the step and their prefix on the cost line
+// (per segment kSegCost + its key pages; one segment per KV head, or per
+// group of KV heads) into shared memory; all threads of the block take part.
 // Returns the total.  Requests with invalid metadata contribute nothing.
 __device__ long long plan_prefix(const FastParams& p, long long* dec0,
                                  int* declen, int* rows, long long* scan_tot,
@@ -1393,7 +1406,7 @@ __device__ long long plan_prefix(const FastParams& p, long long* dec0,
                                  p.max_query_len, p.max_seq_len,
                                  p.max_blocks_per_seq);
       if (m.ok && m.n > 0 && m.n * p.group <= p.dec_rows_max) {
-        dl = m.nb;
+        dl = kSegCost + m.nb;
         rw = m.n * p.group;
       } else if (!m.ok && blockIdx.x == 0) {
         flag_error(p.err, PA_DEV_ERR_METADATA);
