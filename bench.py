@@ -58,6 +58,26 @@ def _tensor_peak():
         return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def _max_over_ranks(values, device):
+    """Replicas: every rank runs the same step on its own GPU; a job's time
+    is the slowest rank's.  Returns the element-wise max over ranks (the
+    values themselves on one process)."""
+    import torch
+    import torch.distributed as dist
+    vals = [float(v) for v in values]
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        t = torch.tensor(vals, dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        vals = [float(x) for x in t.tolist()]
+    return vals
+
+
+def _job_rate(units_per_rank, ms, world_size, scale=1e12):
+    """Whole-job rate: the units all ranks processed / the job's time (ms),
+    in units of `scale` per second."""
+    return units_per_rank * world_size / (ms * 1e-3) / scale
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -379,20 +399,17 @@ def run_ours(args):
     flags = pa.pa_get_device_error()
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x}")
-    ms = statistics.mean(step_ms)
-    kern = statistics.mean(kern_ms)
-    if ws > 1:
-        t = torch.tensor([ms, kern], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, kern = float(t[0]), float(t[1])
-    value = alg_bytes * ws / (ms * 1e-3) / 1e12
+    ms, kern = _max_over_ranks([statistics.mean(step_ms),
+                                statistics.mean(kern_ms)], dev)
+    value = _job_rate(alg_bytes, ms, ws)
     peak_gbs, peak_kind = _peaks()
     achieved_gbs = alg_bytes / (kern * 1e-3) / 1e9
     traffic = _traffic_record(_kernel_hash())
 
     # ---- end to end through the public API with host buffers
     e2e_ms, h2d, d2h = _e2e(pa, wl, d, max(3, args.steps // 2), 2)
-    e2e_value = alg_bytes * ws / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = _max_over_ranks([e2e_ms], dev)[0]
+    e2e_value = _job_rate(alg_bytes, e2e_ms, ws)
     del d
 
     # ---- mixed unified step (tokens/s)
@@ -403,11 +420,7 @@ def run_ours(args):
     flags = pa.pa_get_device_error()
     if flags:
         raise RuntimeError(f"device error flags 0x{flags:x} (mixed step)")
-    m_ms = statistics.mean(m_step)
-    if ws > 1:
-        t = torch.tensor([m_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        m_ms = float(t[0])
+    m_ms = _max_over_ranks([statistics.mean(m_step)], dev)[0]
     m_bytes = wl4.kv_bytes() + wl4.qo_bytes()
     mixed = {
         "workload": ("Llama-3.1-8B shape, bf16: 120 decodes (private context "
