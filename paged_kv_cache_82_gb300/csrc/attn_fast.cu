@@ -149,6 +149,7 @@ struct FastParams {
   int self_plan;      // 1: every CTA plans its own range
   int dec_rows_max;   // decode-class requests have at most this many rows
   int seg_heads;      // KV heads per decode segment (1, or kHg: head groups)
+  int attn_grid;      // CTAs of the attention kernel (the merge's plan)
 };
 
 // ---------------------------------------------------------------------------
@@ -1684,8 +1685,13 @@ merge_kernel(FastParams p) {
 // Split-K merge of a self-planned decode step: CTA b looks at the range
 // boundary b; if it cuts a segment, the CTA merges its share of that
 // segment's rows from the segment's parts, combined in a fixed order.
+#ifndef PA_MERGE_THREADS
+#define PA_MERGE_THREADS 256
+#endif
+constexpr int kMergeThreads = PA_MERGE_THREADS;  // merge_self_kernel CTA
+
 template <typename TOut>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeThreads)
 merge_self_kernel(FastParams p) {
   extern __shared__ long long mplan[];
   __shared__ long long scan[34];
@@ -1695,80 +1701,112 @@ merge_self_kernel(FastParams p) {
   int* declen = reinterpret_cast<int*>(dec0 + p.num_seqs);
   int* rows = declen + p.num_seqs;
   const long long C = plan_prefix(p, dec0, declen, rows, scan + 32, scan);
-  const int g_eff = self_plan_grid(C, gridDim.x);
-  const int b = blockIdx.x;
-  if (b == 0 || b >= g_eff || C <= 0) return;
-  const long long lo_b = (long long)b * C / g_eff;
-  int r = request_of(dec0, p.num_seqs, lo_b);
-  while (r < p.num_seqs && declen[r] == 0) ++r;
-  if (r >= p.num_seqs) return;
-  const int dl = declen[r];
-  const int g = (int)((lo_b - dec0[r]) / dl);
-  const long long ss = dec0[r] + (long long)g * dl, se = ss + dl;
-  if (ss >= lo_b) return;  // boundary b does not cut a segment
-  // the boundaries that cut this segment: b0 .. b1-1.  Its parts, in order:
-  // the tail piece of range b0-1 (slot 2(b0-1)+1), then the head pieces of
-  // ranges b0 .. b1-1 (slots 2k).  The b1-b0 CTAs of these boundaries share
-  // the segment's rows.
-  int b0 = b;
-  while (b0 > 1 && (long long)(b0 - 1) * C / g_eff > ss) --b0;
-  int b1 = b + 1;
-  while (b1 < g_eff && (long long)b1 * C / g_eff < se) ++b1;
-  const int np = 1 + (b1 - b0);
-  const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
-                              p.max_seq_len, p.max_blocks_per_seq);
+  const int g_eff = self_plan_grid(C, p.attn_grid);
+  if (C <= 0) return;
   const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  pdl_wait();  // the attention grid has finished writing the parts
-  // rows of every KV head of the segment (one head, or a head group whose
-  // partial slots hold kHg x 8 rows)
-  const int sh = p.seg_heads;
-  const int part_rows = sh == 1 ? 16 : kHgPartRows;
-  const int total = sh * rows[r];
-  for (int x = (b - b0) * nwarps + (threadIdx.x >> 5); x < total;
-       x += (b1 - b0) * nwarps) {
-    const int w = x / rows[r], rr = x - w * rows[r];
-    const int prow = sh == 1 ? rr : w * 8 + rr;
-    const int i = rr / p.group;
-    const int h = (g * sh + w) * p.group + (rr - i * p.group);
-    const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
-    // partial row of part s: slot 2(b0-1)+1 for s = 0, else slot 2(b0+s-1)
-    const int64_t pr_tail = (int64_t)(2 * (b0 - 1) + 1) * part_rows + prow;
-    const int64_t pr_head = (int64_t)(2 * b0) * part_rows + prow;
-    const int64_t pr_step = 2 * (int64_t)part_rows;
-    // M and the denominator with the parts spread over the lanes
-    float M = -INFINITY;
-    for (int s = lane; s < np; s += 32) {
-      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-      M = fmaxf(M, __ldg(p.ws_ml + pr * 2));
-    }
+  // this CTA takes range boundaries blockIdx.x, + gridDim.x, ...
+  for (int b = blockIdx.x; b < g_eff; b += gridDim.x) {
+    if (b == 0) continue;
+    const long long lo_b = (long long)b * C / g_eff;
+    int r = request_of(dec0, p.num_seqs, lo_b);
+    while (r < p.num_seqs && declen[r] == 0) ++r;
+    if (r >= p.num_seqs) continue;
+    const int dl = declen[r];
+    const int g = (int)((lo_b - dec0[r]) / dl);
+    const long long ss = dec0[r] + (long long)g * dl, se = ss + dl;
+    if (ss >= lo_b) continue;  // boundary b does not cut a segment
+    // the boundaries that cut this segment: b0 .. b1-1.  Its parts, in order:
+    // the tail piece of range b0-1 (slot 2(b0-1)+1), then the head pieces of
+    // ranges b0 .. b1-1 (slots 2k).  The b1-b0 CTAs of these boundaries share
+    // the segment's rows.
+    int b0 = b;
+    while (b0 > 1 && (long long)(b0 - 1) * C / g_eff > ss) --b0;
+    int b1 = b + 1;
+    while (b1 < g_eff && (long long)b1 * C / g_eff < se) ++b1;
+    const int np = 1 + (b1 - b0);
+    const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
+                                p.max_seq_len, p.max_blocks_per_seq);
+    pdl_wait();  // the attention grid has finished writing the parts
+    // rows of every KV head of the segment (one head, or a head group whose
+    // partial slots hold kHg x 8 rows)
+    const int sh = p.seg_heads;
+    const int part_rows = sh == 1 ? 16 : kHgPartRows;
+    const int total = sh * rows[r];
+    for (int x = (b - b0) * nwarps + (threadIdx.x >> 5); x < total;
+         x += (b1 - b0) * nwarps) {
+      const int w = x / rows[r], rr = x - w * rows[r];
+      const int prow = sh == 1 ? rr : w * 8 + rr;
+      const int i = rr / p.group;
+      const int h = (g * sh + w) * p.group + (rr - i * p.group);
+      const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
+      // partial row of part s: slot 2(b0-1)+1 for s = 0, else slot 2(b0+s-1)
+      const int64_t pr_tail = (int64_t)(2 * (b0 - 1) + 1) * part_rows + prow;
+      const int64_t pr_head = (int64_t)(2 * b0) * part_rows + prow;
+      const int64_t pr_step = 2 * (int64_t)part_rows;
+      float M = -INFINITY, den = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (np <= 32) {
+        // lane s holds part s's (m, l): one round trip gives M and the
+        // denominator; the weights go round by shuffle, so the numerator's
+        // loads are independent of each other
+        float ms = -INFINITY, ls = 0.f;
+        if (lane < np) {
+          const int64_t pr = lane == 0 ? pr_tail : pr_head + (lane - 1) * pr_step;
+          const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ws_ml) + pr);
+          ms = ml.x;
+          ls = ml.y;
+        }
+        M = ms;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
-    float den = 0.f;
-    for (int s = lane; s < np; s += 32) {
-      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-      const float ms = __ldg(p.ws_ml + pr * 2);
-      if (ms != -INFINITY) den += exp2f(ms - M) * __ldg(p.ws_ml + pr * 2 + 1);
-    }
+        for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+        const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
+        den = w * ls;
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
-    // the numerator in part order, loads of several parts in flight
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
 #pragma unroll 4
-    for (int s = 0; s < np; ++s) {
-      const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-      const float ms = __ldg(p.ws_ml + pr * 2);
-      const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
-      const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
-      acc[0] += wgt * v.x;
-      acc[1] += wgt * v.y;
-      acc[2] += wgt * v.z;
-      acc[3] += wgt * v.w;
-    }
-    const float inv = p.out_scale / den;
-    TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
+        for (int s = 0; s < np; ++s) {
+          const float wgt = __shfl_sync(~0u, w, s);
+          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+          const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+          acc[2] += wgt * v.z;
+          acc[3] += wgt * v.w;
+        }
+      } else {
+        // M and the denominator with the parts spread over the lanes
+        for (int s = lane; s < np; s += 32) {
+          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+          M = fmaxf(M, __ldg(p.ws_ml + pr * 2));
+        }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
-  }
+        for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+        for (int s = lane; s < np; s += 32) {
+          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+          const float ms = __ldg(p.ws_ml + pr * 2);
+          if (ms != -INFINITY) den += exp2f(ms - M) * __ldg(p.ws_ml + pr * 2 + 1);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
+        // the numerator in part order, loads of several parts in flight
+#pragma unroll 4
+        for (int s = 0; s < np; ++s) {
+          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+          const float ms = __ldg(p.ws_ml + pr * 2);
+          const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+          const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
+          acc[0] += wgt * v.x;
+          acc[1] += wgt * v.y;
+          acc[2] += wgt * v.z;
+          acc[3] += wgt * v.w;
+        }
+      }
+      const float inv = p.out_scale / den;
+      TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+    }
+  }  // boundaries
 }
 
 
@@ -2113,6 +2151,7 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   f.self_plan = 1;
   f.dec_rows_max = 8;
   f.seg_heads = kHg;
+  f.attn_grid = grid;
   const ProfileEvents& pe = profile_events();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2135,7 +2174,8 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
   count_launch();
-  cfg.blockDim = dim3(128);
+  // one merge CTA per range boundary
+  cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
   e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
   if (e == cudaSuccess) count_launch();
@@ -2159,6 +2199,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   // prefill tiles, or prefill tiles on the tensor-core kernel) plan inside
   // the kernels, up to a request count; the rest go through the planner.
   FastParams f = fp;
+  f.attn_grid = grid;
   f.dec_rows_max = wide ? kDecodeMaxRows : 8;
   f.self_plan = fp.num_seqs <= (wide ? kSelfPlanMaxSeqsWide : kSelfPlanMaxSeqs) &&
                 (!plan.has_prefill || tc != nullptr);
@@ -2202,11 +2243,12 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   count_launch();
   if (plan.has_decode) {
     // split segments: at most one fewer than the CTAs that got work
-    cfg.blockDim = dim3(128);
     if (f.self_plan) {
+      cfg.blockDim = dim3(kMergeThreads);
       cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
       e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
     } else {
+      cfg.blockDim = dim3(128);
       cfg.dynamicSmemBytes = 0;
       e = cudaLaunchKernelEx(&cfg, merge_kernel<OutT<kKind>>, f);
     }
