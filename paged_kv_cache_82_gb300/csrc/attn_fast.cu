@@ -2163,20 +2163,33 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (pe.start) cudaEventRecord(pe.start, stream);
+  // With prefill tiles (requests of more than 8 query rows) the decode
+  // kernel goes first and the tensor-core kernel right behind it: that one
+  // reads nothing the decode kernel writes, so its CTAs start on the SMs the
+  // decode kernel's CTAs leave and draw the tiles from a step-wide counter
+  // (zeroed here).  The merge then waits for both kernels.
+  int* tile_ctr = nullptr;
   if (tc) {
-    // requests of more than 8 query rows: prefill tiles on the tensor cores
-    e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
-                          num_sms, stream);
+    tile_ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
+                                      plan.off_pref) + 1;
+    e = cudaMemsetAsync(tile_ctr, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
   }
+  if (pe.start) cudaEventRecord(pe.start, stream);
   e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
-  if (pe.stop) cudaEventRecord(pe.stop, stream);
   if (e != cudaSuccess) return e;
   count_launch();
+  if (tc) {
+    e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
+                          tile_ctr, pe.start == nullptr, num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (pe.stop) cudaEventRecord(pe.stop, stream);
   // one merge CTA per range boundary
   cfg.blockDim = dim3(kMergeThreads);
   cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
+  attr[0].val.programmaticStreamSerializationAllowed =
+      (pe.start == nullptr && !tc) ? 1 : 0;
   e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
   if (e == cudaSuccess) count_launch();
   return e;
@@ -2228,7 +2241,8 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
   if (tc) {
     // prefill tiles on the tensor cores, ahead of the decode work
     e = launch_prefill_tc(a, *tc, f.self_plan != 0, pa.atoms, pa.n_atoms_out,
-                          pa.max_atoms, kDecodeMaxRows, num_sms, stream);
+                          pa.max_atoms, kDecodeMaxRows, nullptr, false, num_sms,
+                          stream);
     if (e != cudaSuccess) return e;
   }
   if (wide) {

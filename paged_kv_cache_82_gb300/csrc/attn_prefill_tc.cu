@@ -96,7 +96,9 @@ enum : int {
   kSFull = kVEmpty + kVStages,       // S of the buffer written
   kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
-  kXchg = kPvDone + kSBufs,          // row halves exchanged, per quarter
+  kTileFull = kPvDone + kSBufs,      // drawn tile index slot filled
+  kTileEmpty = kTileFull + 2,        // slot read by the other 10 warps
+  kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
   kMmaDone = kXchg + 4,
   kNumBars = kMmaDone + 1
 };
@@ -108,7 +110,8 @@ struct TcLayout {
   static constexpr int kBars = kQ + kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kXchgSlot = kAbort + 4;              // float[2][2][128]
+  static constexpr int kTileSlot = kAbort + 4;               // int[2]
+  static constexpr int kXchgSlot = kTileSlot + 8;            // float[2][2][128]
   // the step's tile list when the kernel plans it: per request, the first
   // tile (x heads) and the tile count; block-scan scratch
   static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
@@ -128,6 +131,10 @@ struct TcParams {
   const int* n_atoms;
   int max_atoms;
   int dec_rows_max;      // requests with more query rows are prefill-class
+  int* tile_ctr;         // non-null: tiles drawn from this step-wide counter
+                         // (zeroed before the launch), else a fixed order
+  int no_dep_wait;       // 1: start without waiting for the grid before (it
+                         // produces nothing this kernel reads)
   unsigned* err;
   int64_t num_tokens;
   int64_t num_blocks;
@@ -233,12 +240,31 @@ __device__ int plan_tiles(const TcParams& p, int* pre, int* ntl, int* scan) {
   return run;
 }
 
+// The k-th tile of a warp that does not draw tiles: from the slot the
+// drawing warp filled (dynamic order), else the fixed snake.  -1: no more.
+__device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
+                                           volatile int* slots, int k,
+                                           int n_tiles, volatile int* abort_flag);
+
 // k-th tile of CTA b of K: a snake over the list from its end (longest
 // tiles first): b, 2K-1-b, 2K+b, ...; -1 past the end
 __device__ __forceinline__ int snake_tile(int k, int total) {
   const int K = gridDim.x, b = blockIdx.x;
   const int idx = k * K + ((k & 1) ? K - 1 - b : b);
   return idx < total ? total - 1 - idx : -1;
+}
+
+__device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
+                                           volatile int* slots, int k,
+                                           int n_tiles, volatile int* abort_flag) {
+  if (p.tile_ctr == nullptr) return snake_tile(k, n_tiles);
+  const int s = k & 1;
+  if (!warp_wait(bars + 8 * (kTileFull + s), (k >> 1) & 1, abort_flag, p.err))
+    return -1;
+  const int li = slots[s];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
+  return li;
 }
 
 // Probabilities as two 16-bit parts each, p = hi + lo + O(2^-16 p): for bf16
@@ -288,6 +314,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       uint32_t count = 1;
       if (i >= kPFull && i < kPFull + kSBufs) count = kSoftmaxWarps * 32;
       if (i >= kXchg && i < kXchg + 4) count = 64;
+      if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 2;
       mbar_init(bars + 8 * i, count);
     }
     *abort_flag = 0;
@@ -300,7 +327,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   const uint32_t tmem =
       *reinterpret_cast<volatile uint32_t*>(sp + TcLayout::kTmemSlot);
   pdl_launch_dependents();
-  pdl_wait();  // the step's inputs (and the planner's list) are complete
+  // The step's inputs (and the planner's list) are complete.  When this grid
+  // follows the decode kernel of the step it need not wait for it: that
+  // kernel let it start only after its own wait on everything before.
+  if (!p.no_dep_wait) pdl_wait();
+  volatile int* slots = reinterpret_cast<volatile int*>(sp + TcLayout::kTileSlot);
   int* const pre = reinterpret_cast<int*>(sp + TcLayout::kPlan);
   int* const ntl = pre + kTcMaxSeqs;
   const int n_tiles =
@@ -343,7 +374,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t used[kKStages] = {};  // loads issued into each stage
     bool go = true;
     for (int k = 0; go; ++k) {
-      const int li = snake_tile(k, n_tiles);
+      int li;
+      if (p.tile_ctr != nullptr) {
+        // draw the next tile, longest first, and hand its index to the
+        // other warps through slot k % 2
+        const int s = k & 1;
+        if (k >= 2 &&
+            !warp_wait(bars + 8 * (kTileEmpty + s), ((k >> 1) - 1) & 1, abort_flag, p.err))
+          break;
+        li = -1;
+        if (lane == 0) {
+          const int ticket = *abort_flag ? n_tiles : atomicAdd(p.tile_ctr, 1);
+          li = ticket < n_tiles ? n_tiles - 1 - ticket : -1;
+          slots[s] = li;
+          mbar_arrive(bars + 8 * (kTileFull + s));
+        }
+        li = __shfl_sync(~0u, li, 0);
+      } else {
+        li = snake_tile(k, n_tiles);
+      }
       if (li < 0 || aborted(abort_flag)) break;
       const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
@@ -384,7 +433,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t used[kVStages] = {};
     bool go = true;
     for (int k = 0; go; ++k) {
-      const int li = snake_tile(k, n_tiles);
+      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
       if (li < 0 || aborted(abort_flag)) break;
       const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
@@ -439,7 +488,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     };
     uint32_t u = 0, qt = 0;
     for (int k = 0;; ++k) {
-      const int li = snake_tile(k, n_tiles);
+      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
       if (li < 0 || aborted(abort_flag)) break;
       const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
@@ -524,7 +573,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       return ok;
     };
     for (int k = 0;; ++k) {
-      const int li = snake_tile(k, n_tiles);
+      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
       if (li < 0 || aborted(abort_flag)) break;
       const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
@@ -710,8 +759,8 @@ int tc_prefill_tile_rows(int group) { return (kTcRows / group) * group; }
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
                               const int* n_atoms, int max_atoms,
-                              int dec_rows_max, int num_sms,
-                              cudaStream_t stream) {
+                              int dec_rows_max, int* tile_ctr, bool after_decode,
+                              int num_sms, cudaStream_t stream) {
   TcParams p{};
   p.out = a.out;
   p.block_tables = a.block_tables;
@@ -722,6 +771,8 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
   p.n_atoms = n_atoms;
   p.max_atoms = max_atoms;
   p.dec_rows_max = dec_rows_max;
+  p.tile_ctr = tile_ctr;
+  p.no_dep_wait = after_decode ? 1 : 0;
   p.err = a.err;
   p.num_tokens = a.num_tokens;
   p.num_blocks = a.num_blocks;

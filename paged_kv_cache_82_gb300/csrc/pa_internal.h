@@ -108,12 +108,14 @@ int tc_prefill_tile_rows(int group);
 bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
 // the step's prefill tiles (requests of more than dec_rows_max query rows),
 // listed by the kernel itself (self_plan) or by the planner (atoms,
-// n_atoms); one persistent CTA per SM
+// n_atoms); one persistent CTA per SM.  tile_ctr (zeroed int, or null):
+// tiles drawn dynamically; after_decode: launched right behind the step's
+// decode kernel, whose output it does not read (starts as its CTAs retire).
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
                               const int* n_atoms, int max_atoms,
-                              int dec_rows_max, int num_sms,
-                              cudaStream_t stream);
+                              int dec_rows_max, int* tile_ctr, bool after_decode,
+                              int num_sms, cudaStream_t stream);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
