@@ -24,14 +24,16 @@
 //    ahead of the P.V that frees the V stages.  The same shared-memory
 //    layout serves as the K-major B operand of Q.K^T and as the MN-major B
 //    operand of P.V.
-//  * warp 10 (MMA): allocates tensor memory (512 columns: three S buffers and
-//    O) and issues, from one lane, S = Q.K^T (M 128, N = 16 x pages of the
-//    chunk, K 128) into the S buffer of the chunk, and O += P.V with P read
-//    from tensor memory, where the softmax wrote it over that chunk's S.  P
-//    goes in two 16-bit parts, P = hi + lo, so that the rounding of the
-//    probabilities to 16 bits costs no accuracy.  Completion is tracked with
-//    tcgen05.commit on mbarriers; with three buffers the softmax of one chunk
-//    overlaps the MMAs of its neighbours.
+//  * warps 10 and 11 (MMA): warp 10 allocates tensor memory (512 columns:
+//    three S buffers and O) and issues S = Q.K^T (M 128, N = 16 x pages of
+//    the chunk, K 128) into the S buffer of the chunk; warp 11 issues
+//    O += P.V with P read from tensor memory, where the softmax wrote it over
+//    that chunk's S.  (Two issuing threads: one keeps the tensor core only
+//    about half busy with N = 128 MMAs.)  P goes in two 16-bit parts,
+//    P = hi + lo, so that the rounding of the probabilities to 16 bits costs
+//    no accuracy.  Completion is tracked with tcgen05.commit on mbarriers;
+//    with three buffers the softmax of one chunk overlaps the MMAs of its
+//    neighbours.
 //  * warps 0-7 (softmax): two threads per query row, one per half of the
 //    key columns (warps w and w + 4 share lane quarter w % 4 of tensor
 //    memory).  Each chunk: S from tensor memory, causal mask, online softmax
@@ -62,8 +64,9 @@ constexpr int kTcPages = kTcKeys / kBS;    // pages of a chunk
 constexpr int kSoftmaxWarps = 8;           // two per row quarter
 constexpr int kKWarp = kSoftmaxWarps;      // tiles, Q and K
 constexpr int kVWarp = kSoftmaxWarps + 1;  // V
-constexpr int kMmaWarp = kSoftmaxWarps + 2;
-constexpr int kTcThreads = (kSoftmaxWarps + 3) * 32;
+constexpr int kQkWarp = kSoftmaxWarps + 2; // S = Q.K^T MMAs (owns TMEM)
+constexpr int kPvWarp = kSoftmaxWarps + 3; // O += P.V MMAs
+constexpr int kTcThreads = (kSoftmaxWarps + 4) * 32;
 constexpr int kHalf = 128 * 128;           // 128 rows x 128 B: one column half
 constexpr int kTileBytes = 2 * kHalf;      // 128 rows x 128 columns, 16-bit
 constexpr int kPageHalf = kBS * 128;       // one page, one column half
@@ -97,10 +100,11 @@ enum : int {
   kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
   kTileFull = kPvDone + kSBufs,      // drawn tile index slot filled
-  kTileEmpty = kTileFull + 2,        // slot read by the other 10 warps
+  kTileEmpty = kTileFull + 2,        // slot read by the other 11 warps
   kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
-  kMmaDone = kXchg + 4,
-  kNumBars = kMmaDone + 1
+  kQkDone = kXchg + 4,               // every S MMA has completed
+  kPvDone2 = kQkDone + 1,            // every P.V MMA has completed
+  kNumBars = kPvDone2 + 1
 };
 
 struct TcLayout {
@@ -314,13 +318,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       uint32_t count = 1;
       if (i >= kPFull && i < kPFull + kSBufs) count = kSoftmaxWarps * 32;
       if (i >= kXchg && i < kXchg + 4) count = 64;
-      if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 2;
+      if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 3;
       mbar_init(bars + 8 * i, count);
     }
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) tc_alloc<kTmemCols>(base + TcLayout::kTmemSlot);
+  if (warp == kQkWarp) tc_alloc<kTmemCols>(base + TcLayout::kTmemSlot);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -455,37 +459,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int st = 0; st < kVStages; ++st)
       if (used[st] > 0)
         mbar_wait_bounded(bars + 8 * (kVFull + st), (used[st] - 1) & 1);
-  } else if (warp == kMmaWarp) {
-    // -------------------------------- MMA ---------------------------------
+  } else if (warp == kQkWarp) {
+    // ----------------------------- S = Q.K^T ------------------------------
+    // The two MMA streams are issued by two warps: a tcgen05.mma keeps its
+    // issuing thread busy for about twice the time the tensor core needs
+    // for an N = 128 MMA, so one issuer could keep it only half busy.
     const uint32_t q_s = base + TcLayout::kQ;
-    const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
-    // S of chunk uu (chunk c of tile t) into buffer uu % 3, once the P.V
-    // that last read that buffer has completed
-    auto issue_qk = [&](uint32_t uu, int c, const TcTile& t) -> bool {
-      const int st = uu % kKStages;
-      const int b = uu % kSBufs;
-      if (!warp_wait(bars + 8 * (kKFull + st), (uu / kKStages) & 1, abort_flag, p.err))
-        return false;
-      if (uu >= kSBufs &&
-          !warp_wait(bars + 8 * (kPvDone + b), ((uu / kSBufs) - 1) & 1, abort_flag, p.err))
-        return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const int np = min(kTcPages, t.pages - c * kTcPages);
-        const uint32_t idesc = tc_idesc_f16(kBF16, false, kTcRows, np * kBS);
-        const uint32_t k_s = base + TcLayout::kK + st * kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          tc_mma_ss(tmem + b * 128, tc_desc_sw128(q_s + off, 16, 1024),
-                    tc_desc_sw128(k_s + off, 16, 1024), idesc, kk > 0);
-        }
-        tc_commit(bars + 8 * (kSFull + b));
-        tc_commit(bars + 8 * (kKEmpty + st));
-      }
-      __syncwarp();
-      return true;
-    };
     uint32_t u = 0, qt = 0;
     for (int k = 0;; ++k) {
       const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
@@ -494,7 +473,53 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (!t.ok) continue;
       if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
       ++qt;
-      if (!issue_qk(u, 0, t)) break;
+      bool go = true;
+      for (int c = 0; c < t.nc; ++c) {
+        // S of chunk uu into buffer uu % 3, once the P.V that last read
+        // that buffer has completed
+        const uint32_t uu = u + c;
+        const int st = uu % kKStages;
+        const int b = uu % kSBufs;
+        if (!warp_wait(bars + 8 * (kKFull + st), (uu / kKStages) & 1, abort_flag, p.err) ||
+            (uu >= kSBufs &&
+             !warp_wait(bars + 8 * (kPvDone + b), ((uu / kSBufs) - 1) & 1, abort_flag,
+                        p.err))) {
+          go = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const int np = min(kTcPages, t.pages - c * kTcPages);
+          const uint32_t idesc = tc_idesc_f16(kBF16, false, kTcRows, np * kBS);
+          const uint32_t k_s = base + TcLayout::kK + st * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+            tc_mma_ss(tmem + b * 128, tc_desc_sw128(q_s + off, 16, 1024),
+                      tc_desc_sw128(k_s + off, 16, 1024), idesc, kk > 0);
+          }
+          tc_commit(bars + 8 * (kSFull + b));
+          tc_commit(bars + 8 * (kKEmpty + st));
+          if (c + 1 == t.nc) tc_commit(bars + 8 * kQEmpty);  // Q is free then
+        }
+        __syncwarp();
+      }
+      if (!go) break;
+      u += t.nc;
+    }
+    // every MMA issued has completed before tensor memory is freed
+    if (lane == 0) tc_commit(bars + 8 * kQkDone);
+    __syncwarp();
+    mbar_wait_bounded(bars + 8 * kQkDone, 0);
+  } else if (warp == kPvWarp) {
+    // ------------------------------ O += P.V ------------------------------
+    const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
+    uint32_t u = 0;
+    for (int k = 0;; ++k) {
+      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
+      if (li < 0 || aborted(abort_flag)) break;
+      const TcTile t = tc_tile(p, pre, ntl, li);
+      if (!t.ok) continue;
       const int last = (t.L - 1) / kBS;  // page holding the last key
       const int tail = t.L % kBS;        // its keys (0: a full page)
       bool go = true;
@@ -502,11 +527,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const uint32_t uu = u + c;
         const int sv = uu % kVStages;
         const int b = uu % kSBufs;
-        if (c + 1 < t.nc) {
-          if (!issue_qk(uu + 1, c + 1, t)) { go = false; break; }
-        } else if (lane == 0) {
-          tc_commit(bars + 8 * kQEmpty);  // Q is free once the last S is done
-        }
         if (!warp_wait(bars + 8 * (kPFull + b), (uu / kSBufs) & 1, abort_flag, p.err) ||
             !warp_wait(bars + 8 * (kVFull + sv), (uu / kVStages) & 1, abort_flag, p.err)) {
           go = false;
@@ -544,10 +564,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (!go) break;
       u += t.nc;
     }
-    // every MMA issued has completed before tensor memory is freed
-    if (lane == 0) tc_commit(bars + 8 * kMmaDone);
+    if (lane == 0) tc_commit(bars + 8 * kPvDone2);
     __syncwarp();
-    mbar_wait_bounded(bars + 8 * kMmaDone, 0);
+    mbar_wait_bounded(bars + 8 * kPvDone2, 0);
   } else {
     // ------------------------------ softmax -------------------------------
     // Warps w and w + 4 share the rows of lane quarter w % 4: w takes key
@@ -708,7 +727,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc_fence_after();
     tc_dealloc<kTmemCols>(tmem);
   }
