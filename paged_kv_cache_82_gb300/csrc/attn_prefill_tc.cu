@@ -124,6 +124,10 @@ struct TcLayout {
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
 static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
+// the MMA groups move descriptor start addresses by plain adds: the largest
+// operand address plus the largest step stays inside the 14-bit field
+static_assert(((TcLayout::kQ + kTileBytes + 1024) >> 4) + (kHalf >> 4) < (1 << 14),
+              "descriptor start-address field");
 
 struct TcParams {
   void* out;
@@ -488,19 +492,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           break;
         }
         tc_fence_after();
-        if (lane == 0) {
+        {
+          // the whole warp: one elected lane issues the group
           const int np = min(kTcPages, t.pages - c * kTcPages);
           const uint32_t idesc = tc_idesc_f16(kBF16, false, kTcRows, np * kBS);
           const uint32_t k_s = base + TcLayout::kK + st * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-            tc_mma_ss(tmem + b * 128, tc_desc_sw128(q_s + off, 16, 1024),
-                      tc_desc_sw128(k_s + off, 16, 1024), idesc, kk > 0);
-          }
-          tc_commit(bars + 8 * (kSFull + b));
-          tc_commit(bars + 8 * (kKEmpty + st));
-          if (c + 1 == t.nc) tc_commit(bars + 8 * kQEmpty);  // Q is free then
+          tc_mma_ss_k128<kHalf>(tmem + b * 128, tc_desc_sw128(q_s, 16, 1024),
+                                tc_desc_sw128(k_s, 16, 1024), idesc);
+          tc_commit_elect(bars + 8 * (kSFull + b));
+          tc_commit_elect(bars + 8 * (kKEmpty + st));
+          if (c + 1 == t.nc) tc_commit_elect(bars + 8 * kQEmpty);  // Q is free then
         }
         __syncwarp();
       }
@@ -508,8 +509,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       u += t.nc;
     }
     // every MMA issued has completed before tensor memory is freed
-    if (lane == 0) tc_commit(bars + 8 * kQkDone);
     __syncwarp();
+    tc_commit_elect(bars + 8 * kQkDone);
     mbar_wait_bounded(bars + 8 * kQkDone, 0);
   } else if (warp == kPvWarp) {
     // ------------------------------ O += P.V ------------------------------
@@ -547,25 +548,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          const uint32_t v_s = base + TcLayout::kV + sv * kTileBytes;
+        {
+          // the whole warp: one elected lane issues four pages (8 MMAs) per
+          // group, single pages for the rest of a short chunk
+          const uint64_t bv =
+              tc_desc_sw128(base + TcLayout::kV + sv * kTileBytes, kHalf, 1024);
           const uint32_t t_p = tmem + b * 128;
-          for (int pp = 0; pp < np; ++pp) {
-            const uint64_t bv = tc_desc_sw128(v_s + pp * kPageHalf, kHalf, 1024);
-            tc_mma_ts(tmem + kColO, t_p + pp * 16, bv, idesc_pv,
-                      (c > 0 || pp > 0) ? 1u : 0u);
-            tc_mma_ts(tmem + kColO, t_p + pp * 16 + 8, bv, idesc_pv, 1u);
-          }
-          tc_commit(bars + 8 * (kVEmpty + sv));
-          tc_commit(bars + 8 * (kPvDone + b));
+          int pp = 0;
+          for (; pp + 4 <= np; pp += 4)
+            tc_mma_ts_pair4<kPageHalf>(tmem + kColO, t_p + pp * 16,
+                                       bv + (uint64_t)(pp * (kPageHalf >> 4)), idesc_pv,
+                                       (c > 0 || pp > 0) ? 1u : 0u);
+          for (; pp < np; ++pp)
+            tc_mma_ts_pair1(tmem + kColO, t_p + pp * 16,
+                            bv + (uint64_t)(pp * (kPageHalf >> 4)), idesc_pv,
+                            (c > 0 || pp > 0) ? 1u : 0u);
+          tc_commit_elect(bars + 8 * (kVEmpty + sv));
+          tc_commit_elect(bars + 8 * (kPvDone + b));
         }
         __syncwarp();
       }
       if (!go) break;
       u += t.nc;
     }
-    if (lane == 0) tc_commit(bars + 8 * kPvDone2);
     __syncwarp();
+    tc_commit_elect(bars + 8 * kPvDone2);
     mbar_wait_bounded(bars + 8 * kPvDone2, 0);
   } else {
     // ------------------------------ softmax -------------------------------

@@ -67,34 +67,100 @@ __host__ __device__ constexpr uint32_t tc_idesc_f16(bool bf16, bool b_mn_major,
          ((uint32_t)(m >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc,
-                                          uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
+// ---------------------------------------------------------------------------
+// MMA issue.  Each call is executed by a whole, converged warp: one lane,
+// chosen by elect.sync, issues the whole group of MMAs from a single asm
+// block.  (Issued one by one from a lone lane next to busy warps on the same
+// SM sub-partition, each MMA took two to three times the tensor core's time
+// for it; a group issued back to back keeps the tensor core fed.)
+// Descriptor arithmetic: the start address field holds (byte address >> 4)
+// in its low 14 bits; shared addresses stay below 2^18 bytes and every
+// offset added here keeps the field below 2^14, so a plain 64-bit add moves
+// the start address.
+// ---------------------------------------------------------------------------
+
+// S = A * B^T over K = 128: A (M rows) and B (N rows) K-major in 128-byte
+// swizzled tiles of 64 columns, the two column halves kHalfBytes apart.
+// Step kk reads columns 16kk .. 16kk + 15; the first step overwrites D.
+template <uint32_t kHalfBytes>
+__device__ __forceinline__ void tc_mma_ss_k128(uint32_t d_tmem, uint64_t a_desc,
+                                               uint64_t b_desc, uint32_t idesc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
-          d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred e;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 a4, %1, %4;\n\tadd.s64 a5, a4, 2;\n\tadd.s64 a6, a4, 4;\n\tadd.s64 a7, a4, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "add.s64 b4, %2, %4;\n\tadd.s64 b5, b4, 2;\n\tadd.s64 b6, b4, 4;\n\tadd.s64 b7, b4, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, 1;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kHalfBytes >> 4)
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem,
-                                          uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
+
+// O (+)= P * V for four 16-row steps of B: A (P) in tensor memory, each step
+// as two 16-bit parts, hi in columns 16j .. 16j + 7 and lo in 16j + 8 ..
+// 16j + 15 from a_tmem; B (V) in shared memory, step j at b_desc moved by
+// j * kStepBytes.  acc = 0: the first MMA overwrites D.
+template <uint32_t kStepBytes>
+__device__ __forceinline__ void tc_mma_ts_pair4(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 b1, b2, b3;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"
+      "add.u32 a4, %1, 32;\n\tadd.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\t"
+      "add.u32 a7, %1, 56;\n\t"
+      "add.s64 b1, %2, %5;\n\tadd.s64 b2, b1, %5;\n\tadd.s64 b3, b2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b1, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b2, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %3, 1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b3, %3, 1;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc),
+      "n"(kStepBytes >> 4)
       : "memory");
 }
-// the mbarrier gets one arrival once every MMA this thread issued before it
-// has completed
+// one step of the above (two MMAs)
+__device__ __forceinline__ void tc_mma_ts_pair1(uint32_t d_tmem, uint32_t a_tmem,
+                                                uint64_t b_desc, uint32_t idesc,
+                                                uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 a1;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %2, %3, 1;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// The mbarrier gets one arrival once every MMA this thread issued before it
+// has completed.  tc_commit: the calling thread alone; tc_commit_elect: a
+// whole converged warp, for the MMAs its elected lane issued (elect.sync
+// picks the same lane every time in a fully active warp).
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
