@@ -275,17 +275,19 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
   return li;
 }
 
-// Probabilities as two 16-bit parts each, p = hi + lo + O(2^-16 p): for bf16
-// hi keeps the top half of the fp32 bits (truncation, exact) and lo is the
-// rest rounded to nearest; for f16 both parts are rounded to nearest.
+// Probabilities as two 16-bit parts each, p = hi + lo + O(2^-14 p): for bf16
+// hi keeps the top half of the fp32 bits and lo the top half of the
+// remainder p - hi (which is exact), both by truncation, so the split takes
+// no conversion instructions; for f16 both parts are rounded to nearest.
 template <bool kBF16>
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi,
                                            uint32_t& lo) {
   if constexpr (kBF16) {
     const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
     hi = __byte_perm(ua, ub, 0x7632);
-    lo = pack2<true>(a - __uint_as_float(ua & 0xFFFF0000u),
-                     b - __uint_as_float(ub & 0xFFFF0000u));
+    const float ra = a - __uint_as_float(ua & 0xFFFF0000u);
+    const float rb = b - __uint_as_float(ub & 0xFFFF0000u);
+    lo = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x7632);
   } else {
     hi = pack2<false>(a, b);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hi));
@@ -346,12 +348,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       p.self_plan ? plan_tiles(p, pre, ntl, reinterpret_cast<int*>(sp + TcLayout::kScan))
                   : min(*p.n_atoms, p.max_atoms);
 
-  // page rows of chunk c (lanes < np), checked against the pool
-  auto chunk_rows = [&](const TcTile& t, int c, int np) -> int {
+  // Cache rows of the tile's pages 32 G .. 32 G + 31 (four chunks), one
+  // page per lane, checked against the pool.  The producers fetch the next
+  // group while they issue the current one: under the step's L2 traffic a
+  // block-table read fetched at its own chunk would hold the producer for
+  // about a chunk's time.
+  static_assert(kTcPages * 4 == 32, "four chunks per group of rows");
+  auto group_rows = [&](const TcTile& t, int grp) -> int {
     int row = 0;
-    if (lane < np) {
-      int blk = __ldg(p.block_tables + (int64_t)t.r * p.max_blocks_per_seq +
-                      c * kTcPages + lane);
+    const int pg = grp * 32 + lane;
+    if (pg < t.pages) {
+      int blk = __ldg(p.block_tables + (int64_t)t.r * p.max_blocks_per_seq + pg);
       if (blk < 0 || blk >= p.num_blocks) {
         flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
         blk = 0;
@@ -359,6 +366,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       row = (blk * p.num_kv_heads + t.g) * kBS;
     }
     return row;
+  };
+  // lanes < pages of chunk c: their page's row, from the group held in cur
+  auto chunk_rows = [&](int cur, int c) -> int {
+    return __shfl_sync(~0u, cur, ((c & 3) << 3) | (lane & 7));
   };
   // one chunk of K or V: np pages, two 64-column halves each
   auto load_chunk = [&](const CUtensorMap* map, uint32_t dst, uint32_t full,
@@ -414,10 +425,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                     t.q0 + t.i0);
       }
       ++qt;
+      int cur = group_rows(t, 0), nxt = t.nc > 4 ? group_rows(t, 1) : 0;
       for (int c = 0; c < t.nc; ++c, ++u) {
+        if (c > 0 && (c & 3) == 0) {
+          cur = nxt;
+          nxt = c + 4 < t.nc ? group_rows(t, (c >> 2) + 1) : 0;
+        }
         const int st = u % kKStages;
         const int np = min(kTcPages, t.pages - c * kTcPages);
-        const int row = chunk_rows(t, c, np);
+        const int row = chunk_rows(cur, c);
         if (u >= kKStages &&
             !warp_wait(bars + 8 * (kKEmpty + st), ((u / kKStages) & 1) ^ 1,
                        abort_flag, p.err)) {
@@ -445,10 +461,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       if (li < 0 || aborted(abort_flag)) break;
       const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
+      int cur = group_rows(t, 0), nxt = t.nc > 4 ? group_rows(t, 1) : 0;
       for (int c = 0; c < t.nc; ++c, ++u) {
+        if (c > 0 && (c & 3) == 0) {
+          cur = nxt;
+          nxt = c + 4 < t.nc ? group_rows(t, (c >> 2) + 1) : 0;
+        }
         const int st = u % kVStages;
         const int np = min(kTcPages, t.pages - c * kTcPages);
-        const int row = chunk_rows(t, c, np);
+        const int row = chunk_rows(cur, c);
         if (u >= kVStages &&
             !warp_wait(bars + 8 * (kVEmpty + st), ((u / kVStages) & 1) ^ 1,
                        abort_flag, p.err)) {
