@@ -99,7 +99,7 @@ enum : int {
   kSFull = kVEmpty + kVStages,       // S of the buffer written
   kPFull = kSFull + kSBufs,          // P of the buffer written (128 threads)
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
-  kTileFull = kPvDone + kSBufs,      // drawn tile index slot filled
+  kTileFull = kPvDone + kSBufs,      // tile slot filled (index and metadata)
   kTileEmpty = kTileFull + 2,        // slot read by the other 11 warps
   kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
   kQkDone = kXchg + 4,               // every S MMA has completed
@@ -114,8 +114,8 @@ struct TcLayout {
   static constexpr int kBars = kQ + kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kTileSlot = kAbort + 4;               // int[2]
-  static constexpr int kXchgSlot = kTileSlot + 8;            // float[2][2][128]
+  static constexpr int kTileSlot = kAbort + 4;               // int[2][kSlotInts]
+  static constexpr int kXchgSlot = kTileSlot + 2 * 12 * 4;   // float[2][2][128]
   // the step's tile list when the kernel plans it: per request, the first
   // tile (x heads) and the tile count; block-scan scratch
   static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
@@ -248,12 +248,6 @@ __device__ int plan_tiles(const TcParams& p, int* pre, int* ntl, int* scan) {
   return run;
 }
 
-// The k-th tile of a warp that does not draw tiles: from the slot the
-// drawing warp filled (dynamic order), else the fixed snake.  -1: no more.
-__device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
-                                           volatile int* slots, int k,
-                                           int n_tiles, volatile int* abort_flag);
-
 // k-th tile of CTA b of K: a snake over the list from its end (longest
 // tiles first): b, 2K-1-b, 2K+b, ...; -1 past the end
 __device__ __forceinline__ int snake_tile(int k, int total) {
@@ -262,14 +256,44 @@ __device__ __forceinline__ int snake_tile(int k, int total) {
   return idx < total ? total - 1 - idx : -1;
 }
 
+// Tile slots: the warp that draws the tiles decodes each one (its metadata
+// takes global reads whose latency would otherwise hit every warp at every
+// tile start) and hands it to the other warps through slot k % 2.
+constexpr int kSlotInts = 12;  // li, then the TcTile fields
+__device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTile& t) {
+  slot[0] = li;
+  slot[1] = t.r;
+  slot[2] = t.g;
+  slot[3] = t.q0;
+  slot[4] = t.n;
+  slot[5] = t.L;
+  slot[6] = t.i0;
+  slot[7] = t.ntok;
+  slot[8] = t.pages;
+  slot[9] = t.nc;
+  slot[10] = t.ok ? 1 : 0;
+}
+
+// The k-th tile of a warp that does not draw tiles, from slot k % 2; the
+// index is -1 when there are no more (or on a timeout).
 __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
                                            volatile int* slots, int k,
-                                           int n_tiles, volatile int* abort_flag) {
-  if (p.tile_ctr == nullptr) return snake_tile(k, n_tiles);
+                                           volatile int* abort_flag, TcTile& t) {
   const int s = k & 1;
   if (!warp_wait(bars + 8 * (kTileFull + s), (k >> 1) & 1, abort_flag, p.err))
     return -1;
-  const int li = slots[s];
+  volatile int* sl = slots + s * kSlotInts;
+  const int li = sl[0];
+  t.r = sl[1];
+  t.g = sl[2];
+  t.q0 = sl[3];
+  t.n = sl[4];
+  t.L = sl[5];
+  t.i0 = sl[6];
+  t.ntok = sl[7];
+  t.pages = sl[8];
+  t.nc = sl[9];
+  t.ok = sl[10] != 0;
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
   return li;
@@ -393,27 +417,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t used[kKStages] = {};  // loads issued into each stage
     bool go = true;
     for (int k = 0; go; ++k) {
+      // draw the next tile (longest first: from the step-wide counter, else
+      // the fixed snake), decode it and hand it to the other warps through
+      // slot k % 2
+      const int s = k & 1;
+      if (k >= 2 &&
+          !warp_wait(bars + 8 * (kTileEmpty + s), ((k >> 1) - 1) & 1, abort_flag, p.err))
+        break;
       int li;
       if (p.tile_ctr != nullptr) {
-        // draw the next tile, longest first, and hand its index to the
-        // other warps through slot k % 2
-        const int s = k & 1;
-        if (k >= 2 &&
-            !warp_wait(bars + 8 * (kTileEmpty + s), ((k >> 1) - 1) & 1, abort_flag, p.err))
-          break;
         li = -1;
         if (lane == 0) {
           const int ticket = *abort_flag ? n_tiles : atomicAdd(p.tile_ctr, 1);
           li = ticket < n_tiles ? n_tiles - 1 - ticket : -1;
-          slots[s] = li;
-          mbar_arrive(bars + 8 * (kTileFull + s));
         }
         li = __shfl_sync(~0u, li, 0);
       } else {
         li = snake_tile(k, n_tiles);
       }
+      TcTile t{};
+      if (li >= 0) t = tc_tile(p, pre, ntl, li);
+      if (lane == 0) {
+        put_tile(slots + s * kSlotInts, li, t);
+        mbar_arrive(bars + 8 * (kTileFull + s));
+      }
+      __syncwarp();
       if (li < 0 || aborted(abort_flag)) break;
-      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       if (qt > 0 && !warp_wait(bars + 8 * kQEmpty, (qt - 1) & 1, abort_flag, p.err))
         break;
@@ -457,9 +486,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     uint32_t used[kVStages] = {};
     bool go = true;
     for (int k = 0; go; ++k) {
-      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
+      TcTile t;
+      const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
-      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       int cur = group_rows(t, 0), nxt = t.nc > 4 ? group_rows(t, 1) : 0;
       for (int c = 0; c < t.nc; ++c, ++u) {
@@ -492,9 +521,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t q_s = base + TcLayout::kQ;
     uint32_t u = 0, qt = 0;
     for (int k = 0;; ++k) {
-      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
+      TcTile t;
+      const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
-      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
       ++qt;
@@ -538,9 +567,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
     uint32_t u = 0;
     for (int k = 0;; ++k) {
-      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
+      TcTile t;
+      const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
-      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       const int last = (t.L - 1) / kBS;  // page holding the last key
       const int tail = t.L % kBS;        // its keys (0: a full page)
@@ -620,9 +649,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       return ok;
     };
     for (int k = 0;; ++k) {
-      const int li = follow_tile(p, bars, slots, k, n_tiles, abort_flag);
+      TcTile t;
+      const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
-      const TcTile t = tc_tile(p, pre, ntl, li);
       if (!t.ok) continue;
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
