@@ -304,19 +304,28 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
 // remainder p - hi (which is exact), both by truncation, so the split takes
 // no conversion instructions; for f16 both parts are rounded to nearest.
 template <bool kBF16>
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi,
-                                           uint32_t& lo) {
+__device__ __forceinline__ void split_pair(float2 pr, uint32_t& hi, uint32_t& lo) {
+  const float a = pr.x, b = pr.y;
   if constexpr (kBF16) {
     const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
     hi = __byte_perm(ua, ub, 0x7632);
-    const float ra = a - __uint_as_float(ua & 0xFFFF0000u);
-    const float rb = b - __uint_as_float(ub & 0xFFFF0000u);
-    lo = __byte_perm(__float_as_uint(ra), __float_as_uint(rb), 0x7632);
+    // remainder p - hi, exact, as one packed fma
+    const float2 r = __ffma2_rn(make_float2(__uint_as_float(ua & 0xFFFF0000u),
+                                            __uint_as_float(ub & 0xFFFF0000u)),
+                                make_float2(-1.f, -1.f), pr);
+    lo = __byte_perm(__float_as_uint(r.x), __float_as_uint(r.y), 0x7632);
   } else {
     hi = pack2<false>(a, b);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hi));
     lo = pack2<false>(a - f.x, b - f.y);
   }
+}
+
+// max of three (one instruction)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // 2^x by the hardware approximation (relative error about 2^-22; results
@@ -679,17 +688,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (__any_sync(~0u, vis < 63)) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const float x = j <= vis ? __uint_as_float(sr[j >> 5][j & 31]) : -INFINITY;
-            sr[j >> 5][j & 31] = __float_as_uint(x);
-            mx4[j & 3] = fmaxf(mx4[j & 3], x);
-          }
-        } else {
-#pragma unroll
           for (int j = 0; j < 64; ++j)
-            mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j >> 5][j & 31]));
+            if (j > vis) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
         }
-        float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+#pragma unroll
+        for (int j = 0; j < 64; j += 2)
+          mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(sr[j >> 5][j & 31]),
+                                    __uint_as_float(sr[j >> 5][(j & 31) + 1]));
+        float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
         float mx_other;
         if (!exchange(mx, mx_other)) {
           go = false;
@@ -727,22 +733,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // P = 2^(s * scale - m_ref) over the S just read, in place: the 16
         // keys of MMA step k take columns 16k .. 16k+7 (hi parts) and
         // 16k+8 .. 16k+15 (lo parts), key pairs packed low key first
-        const float neg_m = -m_ref;
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        // (key pairs in packed fp32x2 arithmetic)
+        const float2 scale2 = make_float2(p.score_scale, p.score_scale);
+        const float2 neg_m2 = make_float2(-m_ref, -m_ref);
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           uint32_t w[32];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[j][2 * k]), p.score_scale, neg_m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[j][2 * k + 1]), p.score_scale, neg_m));
-            l4[k & 3] += p0 + p1;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[j][2 * k]),
+                                                    __uint_as_float(sr[j][2 * k + 1])),
+                                        scale2, neg_m2);
+            const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            l2[k & 1] = __fadd2_rn(l2[k & 1], pr);
             const int slot = (k >> 3) * 16 + (k & 7);  // hi at slot, lo at slot + 8
-            split_pair<kBF16>(p0, p1, w[slot], w[slot + 8]);
+            split_pair<kBF16>(pr, w[slot], w[slot + 8]);
           }
           tc_st32(t_b + j * 32, w);
         }
-        l += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        const float2 lsum = __fadd2_rn(l2[0], l2[1]);
+        l += lsum.x + lsum.y;
         tc_wait_st();
         tc_fence_before();
         mbar_arrive(bars + 8 * (kPFull + b));
