@@ -13,9 +13,9 @@
 // How (one CTA per SM, persistent over the step's prefill tiles):
 //  * A tile is 128 query rows of one (request, KV head): 128 / G consecutive
 //    tokens times the G q heads of the group, row = token * G + head.  Keys
-//    go in chunks of 128 (8 pages).  Warp 8 draws tiles from a
-//    step-wide counter, longest first, and passes each tile's index to the
-//    other warps through a two-slot ring in shared memory.
+//    go in chunks of 128 (8 pages).  Warp 8 draws tiles (from a step-wide
+//    counter, longest first, or in a fixed snake), decodes each and passes
+//    it to the other warps through a two-slot ring in shared memory.
 //  * warps 8 and 9 (TMA producers): the Q tile through a 3-D map over q
 //    [token][head][dim] and, for every chunk, its pages of K (warp 8) and of
 //    V (warp 9) through 2-D maps over the cache rows, each page as two
@@ -23,15 +23,17 @@
 //    two (V) chunks deep.  The two rings advance independently, so K runs
 //    ahead of the P.V that frees the V stages.  The same shared-memory
 //    layout serves as the K-major B operand of Q.K^T and as the MN-major B
-//    operand of P.V.
+//    operand of P.V.  Block-table rows come a group of four chunks ahead.
 //  * warps 10 and 11 (MMA): warp 10 allocates tensor memory (512 columns:
 //    three S buffers and O) and issues S = Q.K^T (M 128, N = 16 x pages of
 //    the chunk, K 128) into the S buffer of the chunk; warp 11 issues
 //    O += P.V with P read from tensor memory, where the softmax wrote it over
-//    that chunk's S.  (Two issuing threads: one keeps the tensor core only
-//    about half busy with N = 128 MMAs.)  P goes in two 16-bit parts,
-//    P = hi + lo, so that the rounding of the probabilities to 16 bits costs
-//    no accuracy.  Completion is tracked with tcgen05.commit on mbarriers;
+//    that chunk's S.  Each warp issues its MMAs from one elected lane of the
+//    converged warp, eight per asm block, so that the softmax warps sharing
+//    its SM sub-partition do not slow the issue below the tensor rate.
+//    P goes in two 16-bit parts, P = hi + lo, so that the rounding of the
+//    probabilities to 16 bits costs no accuracy.  Completion is tracked with
+//    tcgen05.commit on mbarriers;
 //    with three buffers the softmax of one chunk overlaps the MMAs of its
 //    neighbours.
 //  * warps 0-7 (softmax): two threads per query row, one per half of the
@@ -39,8 +41,8 @@
 //    memory).  Each chunk: S from tensor memory, causal mask, online softmax
 //    against a reference max that only moves when the row max has grown by
 //    more than 2^8 (O is then rescaled in tensor memory; otherwise the
-//    exponentials stay below 2^8), P into tensor memory.  At the end of the
-//    tile: O / l in the output type.
+//    exponentials stay below 2^8), P into tensor memory; key pairs in packed
+//    fp32x2 arithmetic.  At the end of the tile: O / l in the output type.
 //  * V rows of the request's last page that lie past the sequence end are
 //    cleared in shared memory before P.V (their P is 0, but 0 x NaN is not).
 //
