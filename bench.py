@@ -360,9 +360,11 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     if args.only != "all":
-        wl = {"decode": workloads.config2, "mixed": workloads.config4,
-              "prefill": workloads.prefill_chunk, "mha": workloads.config3,
-              "fp8long": workloads.config5}[args.only]()
+        make = {"decode": workloads.config2, "mixed": workloads.config4,
+                "prefill": workloads.prefill_chunk, "mha": workloads.config3,
+                "fp8long": workloads.config5}[args.only]
+        # a smaller batch of the same decode shape (profiler captures)
+        wl = make(batch=args.batch) if args.batch else make()
         d = _device_inputs(wl, dev)
         step_ms, kern_ms, _ = _time_steps(pa, wl, d, args.steps, args.warmup,
                                           flush)
@@ -606,6 +608,9 @@ def main():
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
                          "line")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --only decode/mha/fp8long: that many requests "
+                         "instead of the workload's own batch")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

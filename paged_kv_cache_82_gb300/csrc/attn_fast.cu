@@ -662,8 +662,8 @@ __device__ __forceinline__ void qk_page(uint32_t k_base,
         const uint32_t wv[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
         for (int tt = 0; tt < 4; ++tt) {
-          const uint32_t b0 = e4m3x2_to_f16x2(wv[tt]);
-          const uint32_t b1 = e4m3x2_to_f16x2(wv[tt] >> 16);
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(wv[tt], b0, b1);
           if (tt & 1)
             mma_acc<false, kRows16>(s2[nt], qa[4 * hh + tt], b0, b1);
           else
@@ -823,14 +823,15 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
       const uint32_t cd01 = __byte_perm(vc[w], vd[w], 0x5140);
       const uint32_t cd23 = __byte_perm(vc[w], vd[w], 0x7362);
       const int T = 4 * w;
-      mma_acc<false, kRows16>(st.o[T], pa, e4m3x2_to_f16x2(ab01),
-                              e4m3x2_to_f16x2(cd01));
-      mma_acc<false, kRows16>(st.o[T + 1], pa, e4m3x2_to_f16x2(ab01 >> 16),
-                              e4m3x2_to_f16x2(cd01 >> 16));
-      mma_acc<false, kRows16>(st.o[T + 2], pa, e4m3x2_to_f16x2(ab23),
-                              e4m3x2_to_f16x2(cd23));
-      mma_acc<false, kRows16>(st.o[T + 3], pa, e4m3x2_to_f16x2(ab23 >> 16),
-                              e4m3x2_to_f16x2(cd23 >> 16));
+      uint32_t x[8];
+      e4m3x4_to_f16x2x2(ab01, x[0], x[1]);
+      e4m3x4_to_f16x2x2(cd01, x[2], x[3]);
+      e4m3x4_to_f16x2x2(ab23, x[4], x[5]);
+      e4m3x4_to_f16x2x2(cd23, x[6], x[7]);
+      mma_acc<false, kRows16>(st.o[T], pa, x[0], x[2]);
+      mma_acc<false, kRows16>(st.o[T + 1], pa, x[1], x[3]);
+      mma_acc<false, kRows16>(st.o[T + 2], pa, x[4], x[6]);
+      mma_acc<false, kRows16>(st.o[T + 3], pa, x[5], x[7]);
     }
   }
 }
@@ -970,10 +971,8 @@ __device__ __forceinline__ void process_page_narrow(
       const uint32_t ab = __byte_perm(va[mt >> 1], vb[mt >> 1], sel);
       const uint32_t cd = __byte_perm(vc[mt >> 1], vd[mt >> 1], sel);
       uint32_t a[4];
-      a[0] = e4m3x2_to_f16x2(ab);
-      a[1] = e4m3x2_to_f16x2(ab >> 16);
-      a[2] = e4m3x2_to_f16x2(cd);
-      a[3] = e4m3x2_to_f16x2(cd >> 16);
+      e4m3x4_to_f16x2x2(ab, a[0], a[1]);
+      e4m3x4_to_f16x2x2(cd, a[2], a[3]);
       mma16816<false>(st.o[mt], a, b0, b1);
     }
   }

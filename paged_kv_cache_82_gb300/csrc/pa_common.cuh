@@ -253,11 +253,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// two E4M3 bytes (lo byte first) -> packed f16 pair, exact
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-      static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// four E4M3 bytes (lowest byte first) -> two packed f16 pairs, exact: bytes
+// 0, 1 into lo and 2, 3 into hi.  The two 16-bit halves of the word feed the
+// conversions directly (no shift to bring the upper pair down).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t& lo,
+                                                  uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_bytes));
 }
 
 // ----------------------------------------------------------------------------
