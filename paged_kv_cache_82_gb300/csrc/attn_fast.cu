@@ -150,6 +150,8 @@ struct FastParams {
   int dec_rows_max;   // decode-class requests have at most this many rows
   int seg_heads;      // KV heads per decode segment (1, or kHg: head groups)
   int attn_grid;      // CTAs of the attention kernel (the merge's plan)
+  int no_dep_wait;    // 1: start without waiting for the grid before (it let
+                      // this one start only after its own wait)
 };
 
 // ---------------------------------------------------------------------------
@@ -1942,8 +1944,10 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();               // everything before this grid is done
-  pdl_launch_dependents();  // the merge may be scheduled behind this grid
+  // everything before this grid is done (when a prefill grid runs ahead of
+  // it, that grid let this one start only after its own wait)
+  if (!p.no_dep_wait) pdl_wait();
+  pdl_launch_dependents();  // the next grid may be scheduled behind this one
   // this CTA's stream-K range over the (request, head group) segments
   long long* dec0 = reinterpret_cast<long long*>(sp + Ly::kPlan);
   int* declen = reinterpret_cast<int*>(dec0 + kHgMaxSeqs);
@@ -2137,6 +2141,28 @@ bool use_head_groups(const AttnArgs& a, bool tc) {
   return (int64_t)a.max_query_len * G <= 8 || tc;
 }
 
+// SMs that run prefill tiles while the decode kernel of a mixed step runs on
+// the others.  The tiles' share of the step's time from host-known sizes:
+// per key, a prefill token costs 4 D Hq flops on the tensor cores (~1e15
+// flop/s in this kernel) and a decode request 2 D Hkv x 2 bytes from HBM
+// (~6e12 B/s), so the prefill : decode time ratio is about
+// r = G x (prefill tokens / requests) x 0.006, the key counts taken as equal
+// and tokens beyond one per request counted as prefill tokens.  The decode
+// kernel slows almost in proportion to the SMs it loses, so the split gives
+// the tiles half their balanced share: the rest run behind the decode kernel
+// on every SM, which measured best (a 1022-token chunk beside 120 decodes:
+// 13 SMs, step 437 -> 428 us; 20 SMs or more were slower than none).
+int prefill_ctas_ahead(const AttnArgs& a, int num_sms) {
+  const int64_t n_pf = a.num_tokens - a.num_seqs + 1;
+  if (n_pf <= 0 || a.num_seqs <= 0 || num_sms < 16) return 0;
+  const double G = (double)a.num_q_heads / a.num_kv_heads;
+  const double r = G * (double)n_pf / (double)a.num_seqs * 0.006;
+  int p = (int)(0.5 * num_sms * r / (1.0 + r) + 0.5);
+  if (p < 4) p = 4;
+  if (p > num_sms / 4) p = num_sms / 4;
+  return p;
+}
+
 template <int kKind>
 cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
                       const AttnPlan& plan, const CUtensorMap& tk,
@@ -2162,19 +2188,39 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // With prefill tiles (requests of more than 8 query rows) the decode
-  // kernel goes first and the tensor-core kernel right behind it: that one
-  // reads nothing the decode kernel writes, so its CTAs start on the SMs the
-  // decode kernel's CTAs leave and draw the tiles from a step-wide counter
-  // (zeroed here).  The merge then waits for both kernels.
+  // With prefill tiles (requests of more than 8 query rows) the tensor-core
+  // kernel and the decode kernel share the GPU, the tiles drawn from one
+  // step-wide counter (zeroed here):
+  //  1. a prefill grid of P CTAs (one per SM) goes first; it waits for the
+  //     step's inputs and then lets the next grid start;
+  //  2. the decode kernel, on the other SMs (its CTAs do not fit next to a
+  //     prefill CTA), starts without a wait of its own;
+  //  3. a second prefill grid, behind the decode kernel, takes the SMs its
+  //     CTAs leave and draws whatever tiles are left (none: it exits).
+  // The merge, a plain launch, waits for all three.
   int* tile_ctr = nullptr;
+  int pf_ctas = 0;
   if (tc) {
     tile_ctr = reinterpret_cast<int*>(static_cast<uint8_t*>(a.workspace) +
                                       plan.off_pref) + 1;
     e = cudaMemsetAsync(tile_ctr, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
+    // (with the profiling events on, launches are plain and run one after
+    // the other: no grid ahead, the tiles all behind the decode kernel)
+    pf_ctas = pe.start == nullptr ? prefill_ctas_ahead(a, num_sms) : 0;
+    const int per_sm = num_sms > 0 && grid >= num_sms ? grid / num_sms : 1;
+    const int dec_grid = per_sm * (num_sms - pf_ctas);
+    if (dec_grid >= 1 && dec_grid < grid) grid = dec_grid;
+    f.attn_grid = grid;
+    f.no_dep_wait = (pe.start == nullptr && pf_ctas > 0) ? 1 : 0;
+    cfg.gridDim = dim3(grid);
   }
   if (pe.start) cudaEventRecord(pe.start, stream);
+  if (tc && pf_ctas > 0) {
+    e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
+                          tile_ctr, false, pf_ctas, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
   if (e != cudaSuccess) return e;
   count_launch();

@@ -371,11 +371,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   tc_fence_after();
   const uint32_t tmem =
       *reinterpret_cast<volatile uint32_t*>(sp + TcLayout::kTmemSlot);
-  pdl_launch_dependents();
   // The step's inputs (and the planner's list) are complete.  When this grid
   // follows the decode kernel of the step it need not wait for it: that
-  // kernel let it start only after its own wait on everything before.
+  // kernel let it start only after everything before it was complete.  The
+  // grid behind this one may start once every CTA is past this wait.
   if (!p.no_dep_wait) pdl_wait();
+  pdl_launch_dependents();
   volatile int* slots = reinterpret_cast<volatile int*>(sp + TcLayout::kTileSlot);
   int* const pre = reinterpret_cast<int*>(sp + TcLayout::kPlan);
   int* const ntl = pre + kTcMaxSeqs;

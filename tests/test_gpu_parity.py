@@ -286,11 +286,12 @@ def test_launches_per_step_kind():
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (40, 1)], 32, 8))
     assert pa.pa_launch_count() - n0 == 2
-    # K/V write + a step with bf16 prefill tiles: the tensor-core prefill
-    # kernel and the attention kernel plan themselves, then the merge
+    # K/V write + a step with bf16 prefill tiles: a tensor-core prefill grid
+    # beside the decode kernel, a second one behind it (both plan
+    # themselves), then the merge
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (100, 64)], 32, 8, write_new=True))
-    assert pa.pa_launch_count() - n0 == 4
+    assert pa.pa_launch_count() - n0 == 5
     # FP8 cache with prefill tiles: planner, attention kernel, merge
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (100, 64)], 32, 8, cache_dtype="e4m3",
