@@ -71,6 +71,9 @@ constexpr int kHgPartRows = 32;   // partial rows per slot there: kHg heads x 8
 #ifndef PA_STAGES_16BIT
 #define PA_STAGES_16BIT 8       // ring depth in pages, bf16 / fp16 caches
 #endif
+#ifndef PA_HG_RING_BYTES
+#define PA_HG_RING_BYTES 98304  // ring of the head-group kernel (96 KiB)
+#endif
 
 constexpr int kConsumerWarps = PA_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -1825,7 +1828,7 @@ struct HgLayout {
   using Tr = Traits<kKind>;
   static constexpr int kPageBytes = Tr::kPageBytes;          // one KV head
   static constexpr int kStageBytes = 2 * kHg * kPageBytes;   // K, V of a group
-  static constexpr int kStages = 3 * 32768 / kStageBytes;    // 96 KiB ring
+  static constexpr int kStages = PA_HG_RING_BYTES / kStageBytes;
   static constexpr int kRing = 0;
   static constexpr int kBars = kRing + kStages * kStageBytes;
   static constexpr int kIds = kBars + 8 * 2 * kStages;       // int [2][32]

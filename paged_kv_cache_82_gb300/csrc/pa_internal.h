@@ -42,7 +42,10 @@ constexpr int kDecodeMaxRows = 16;   // q_len * group rows handled by one warp
 // rows of a prefill tile: 16 per consumer warp
 constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
 
-constexpr int kMaxCtasPerSm = 2;     // resident attention CTAs per SM (grid bound)
+#ifndef PA_CTAS_PER_SM
+#define PA_CTAS_PER_SM 2  // resident attention CTAs per SM the kernels are built for
+#endif
+constexpr int kMaxCtasPerSm = PA_CTAS_PER_SM;  // grid bound of the attention kernels
 
 struct AttnPlan {
   int group;            // Hq / Hkv
