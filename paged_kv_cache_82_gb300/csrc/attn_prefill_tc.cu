@@ -19,7 +19,7 @@
 //  * warps 8 and 9 (TMA producers): the Q tile through a 3-D map over q
 //    [token][head][dim] and, for every chunk, its pages of K (warp 8) and of
 //    V (warp 9) through 2-D maps over the cache rows, each page as two
-//    64-column halves under the 128-byte swizzle, into rings three (K) and
+//    64-column halves under the 128-byte swizzle, into rings two (K) and
 //    two (V) chunks deep.  The two rings advance independently, so K runs
 //    ahead of the P.V that frees the V stages.  The same shared-memory
 //    layout serves as the K-major B operand of Q.K^T and as the MN-major B
@@ -75,13 +75,17 @@ constexpr int kPageHalf = kBS * 128;       // one page, one column half
 constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (log2)
 constexpr int kTcMaxSeqs = 1024;           // requests of a step it plans itself
 #ifndef PA_TC_K_STAGES
-#define PA_TC_K_STAGES 3
+#define PA_TC_K_STAGES 2
 #endif
 #ifndef PA_TC_V_STAGES
 #define PA_TC_V_STAGES 2
 #endif
+#ifndef PA_TC_Q_STAGES
+#define PA_TC_Q_STAGES 1
+#endif
 constexpr int kKStages = PA_TC_K_STAGES;  // ring depth in chunks, K
 constexpr int kVStages = PA_TC_V_STAGES;  // ring depth in chunks, V
+constexpr int kQStages = PA_TC_Q_STAGES;  // Q tiles in shared memory
 constexpr int kSBufs = 3;                   // S / P buffers in tensor memory
 
 // Tensor memory: three S buffers of 128 columns; the softmax overwrites each
@@ -93,8 +97,8 @@ constexpr uint32_t kColO = 384;
 // barriers
 enum : int {
   kQFull = 0,
-  kQEmpty = 1,
-  kKFull = 2,
+  kQEmpty = kQFull + kQStages,
+  kKFull = kQEmpty + kQStages,
   kKEmpty = kKFull + kKStages,
   kVFull = kKEmpty + kKStages,
   kVEmpty = kVFull + kVStages,
@@ -112,8 +116,8 @@ enum : int {
 struct TcLayout {
   static constexpr int kK = 0;                               // K stages
   static constexpr int kV = kK + kKStages * kTileBytes;      // V stages
-  static constexpr int kQ = kV + kVStages * kTileBytes;      // Q tile
-  static constexpr int kBars = kQ + kTileBytes;
+  static constexpr int kQ = kV + kVStages * kTileBytes;      // Q tiles
+  static constexpr int kBars = kQ + kQStages * kTileBytes;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileSlot = kAbort + 4;               // int[2][kSlotInts]
@@ -128,7 +132,7 @@ struct TcLayout {
 static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
 // the MMA groups move descriptor start addresses by plain adds: the largest
 // operand address plus the largest step stays inside the 14-bit field
-static_assert(((TcLayout::kQ + kTileBytes + 1024) >> 4) + (kHalf >> 4) < (1 << 14),
+static_assert(((TcLayout::kQ + kQStages * kTileBytes + 1024) >> 4) + (kHalf >> 4) < (1 << 14),
               "descriptor start-address field");
 
 struct TcParams {
@@ -323,6 +327,15 @@ __device__ __forceinline__ void split_pair(float2 pr, uint32_t& hi, uint32_t& lo
   }
 }
 
+// 32 bytes (eight words from r[first]) to a 32-byte aligned global address
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t (&r)[16],
+                                             int first) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst),
+               "r"(r[first]), "r"(r[first + 1]), "r"(r[first + 2]), "r"(r[first + 3]),
+               "r"(r[first + 4]), "r"(r[first + 5]), "r"(r[first + 6]), "r"(r[first + 7])
+               : "memory");
+}
+
 // max of three (one instruction)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -456,13 +469,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       __syncwarp();
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
-      if (qt > 0 && !warp_wait(bars + 8 * kQEmpty, (qt - 1) & 1, abort_flag, p.err))
+      // Q of this CTA's tile qt into buffer qt % kQStages, once the S MMAs of
+      // the tile that last used it have completed
+      const uint32_t qb = qt % kQStages;
+      if (qt >= (uint32_t)kQStages &&
+          !warp_wait(bars + 8 * (kQEmpty + qb), ((qt / kQStages) - 1) & 1, abort_flag,
+                     p.err))
         break;
       if (lane == 0) {
-        const uint32_t fb = bars + 8 * kQFull;
+        const uint32_t fb = bars + 8 * (kQFull + qb);
+        const uint32_t qd = base + TcLayout::kQ + qb * kTileBytes;
         mbar_arrive_expect_tx(fb, q_bytes);
-        tma_load_3d(base + TcLayout::kQ, &tmap_q, fb, 0, t.g * G, t.q0 + t.i0);
-        tma_load_3d(base + TcLayout::kQ + kHalf, &tmap_q, fb, 64, t.g * G,
+        tma_load_3d(qd, &tmap_q, fb, 0, t.g * G, t.q0 + t.i0);
+        tma_load_3d(qd + kHalf, &tmap_q, fb, 64, t.g * G,
                     t.q0 + t.i0);
       }
       ++qt;
@@ -490,7 +509,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int st = 0; st < kKStages; ++st)
       if (used[st] > 0)
         mbar_wait_bounded(bars + 8 * (kKFull + st), (used[st] - 1) & 1);
-    if (qt > 0) mbar_wait_bounded(bars + 8 * kQFull, (qt - 1) & 1);
+    for (uint32_t qb = 0; qb < (uint32_t)kQStages; ++qb) {
+      const uint32_t n = qt > qb ? (qt - qb + kQStages - 1) / kQStages : 0;  // loads into qb
+      if (n > 0) mbar_wait_bounded(bars + 8 * (kQFull + qb), (n - 1) & 1);
+    }
   } else if (warp == kVWarp) {
     // ----------------------------- producer: V ------------------------------
     if (lane == 0) tma_prefetch_desc(&tmap_v);
@@ -530,14 +552,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     // The two MMA streams are issued by two warps: a tcgen05.mma keeps its
     // issuing thread busy for about twice the time the tensor core needs
     // for an N = 128 MMA, so one issuer could keep it only half busy.
-    const uint32_t q_s = base + TcLayout::kQ;
     uint32_t u = 0, qt = 0;
     for (int k = 0;; ++k) {
       TcTile t;
       const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
-      if (!warp_wait(bars + 8 * kQFull, qt & 1, abort_flag, p.err)) break;
+      const uint32_t qb = qt % kQStages;
+      if (!warp_wait(bars + 8 * (kQFull + qb), (qt / kQStages) & 1, abort_flag, p.err))
+        break;
+      const uint32_t q_s = base + TcLayout::kQ + qb * kTileBytes;
       ++qt;
       bool go = true;
       for (int c = 0; c < t.nc; ++c) {
@@ -563,7 +587,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                                 tc_desc_sw128(k_s, 16, 1024), idesc);
           tc_commit_elect(bars + 8 * (kSFull + b));
           tc_commit_elect(bars + 8 * (kKEmpty + st));
-          if (c + 1 == t.nc) tc_commit_elect(bars + 8 * kQEmpty);  // Q is free then
+          if (c + 1 == t.nc) tc_commit_elect(bars + 8 * (kQEmpty + qb));  // Q is free then
         }
         __syncwarp();
       }
@@ -772,6 +796,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         break;
       tc_fence_after();
       const float inv = 1.f / l_tot;
+      // each thread writes 128 contiguous bytes of its row: 32-byte stores
+      // when the output allows them (row starts are 256-byte multiples apart)
+      const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
       TOut* o = static_cast<TOut*>(p.out) +
                 ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128 +
                 half * 64;
@@ -786,10 +813,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           for (int k = 0; k < 16; ++k)
             pk[k] = pack2<kBF16>(__uint_as_float(v[2 * k]) * inv,
                                  __uint_as_float(v[2 * k + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(o + j * 32);
+          if (out32) {
+            // whole 32-byte sectors, two per 32 columns
+            st_global_v8(o + j * 32, pk, 0);
+            st_global_v8(o + j * 32 + 16, pk, 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(o + j * 32);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
       }
       tc_fence_before();
