@@ -487,3 +487,20 @@ def test_host_validation_rejects_before_launch():
     assert call(cdt=pa.PA_FP8_E4M3, ks=0.0) == pa.PA_ERR_INVALID_ARG
     assert call(qdt=pa.PA_F16) == pa.PA_ERR_UNSUPPORTED          # q != cache
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_output_16_byte_aligned(dtype):
+    # an output view 16 bytes past a 32-byte boundary: the prefill tiles
+    # write it with 16-byte stores instead of 32-byte ones
+    wl = _custom([(300, 1), (700, 300), (90, 64)], 32, 8, dtype=dtype)
+    T = int(wl.q.shape[0])
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    base = torch.full((T * 32 * 128 + 8,), float("nan"), dtype=tdt, device="cuda")
+    out_view = base[8:].view(T, 32, 128)
+    assert out_view.data_ptr() % 32 == 16
+    out, kc, vc, md, flags = gpu_step(wl, out=out_view)
+    assert flags == 0
+    assert out.data_ptr() == out_view.data_ptr()
+    ref, *_ = _oracle_full(wl)
+    assert_close(out, ref, md, dtype, dtype)
