@@ -130,6 +130,10 @@ struct TcLayout {
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
 static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
+// Each CTA allocates all 512 tensor-memory columns: a second CTA of this
+// kernel on the same SM would wait in its allocation.  Its shared memory
+// keeps it off (228 KB per SM).
+static_assert(2 * TcLayout::kSmemBytes > 228 * 1024, "one CTA per SM");
 // the MMA groups move descriptor start addresses by plain adds: the largest
 // operand address plus the largest step stays inside the 14-bit field
 static_assert(((TcLayout::kQ + kQStages * kTileBytes + 1024) >> 4) + (kHalf >> 4) < (1 << 14),
