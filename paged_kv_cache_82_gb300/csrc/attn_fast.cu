@@ -1752,7 +1752,17 @@ merge_self_kernel(FastParams p) {
       if (np <= 32) {
         // lane s holds part s's (m, l): one round trip gives M and the
         // denominator; the weights go round by shuffle, so the numerator's
-        // loads are independent of each other
+        // loads are independent of each other.  The first four parts' rows
+        // are loaded together with (m, l).
+        float4 vpre[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          vpre[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (s < np) {
+            const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+            vpre[s] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+          }
+        }
         float ms = -INFINITY, ls = 0.f;
         if (lane < np) {
           const int64_t pr = lane == 0 ? pr_tail : pr_head + (lane - 1) * pr_step;
@@ -1767,10 +1777,20 @@ merge_self_kernel(FastParams p) {
         den = w * ls;
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
-#pragma unroll 4
-        for (int s = 0; s < np; ++s) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
           const float wgt = __shfl_sync(~0u, w, s);
-          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+          if (s < np) {
+            acc[0] += wgt * vpre[s].x;
+            acc[1] += wgt * vpre[s].y;
+            acc[2] += wgt * vpre[s].z;
+            acc[3] += wgt * vpre[s].w;
+          }
+        }
+#pragma unroll 4
+        for (int s = 4; s < np; ++s) {
+          const float wgt = __shfl_sync(~0u, w, s);
+          const int64_t pr = pr_head + (s - 1) * pr_step;
           const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
           acc[0] += wgt * v.x;
           acc[1] += wgt * v.y;
