@@ -230,6 +230,14 @@ def test_mixed_step_routing_by_rows(cache_dtype, dtype):
                         write_new=True))
 
 
+def test_mixed_step_prefill_heavy():
+    # a long chunk next to two decodes: the prefill grid ahead of the decode
+    # kernel takes its largest share of the SMs and most tiles, the grid
+    # behind the decode kernel the rest
+    seq_q = [(4000, 2000), (300, 1), (777, 1)]
+    _check_step(_custom(seq_q, 32, 8, write_new=True))
+
+
 def test_prefill_row_max_growing_across_chunks():
     # with scores 11x larger than 1/sqrt(D) gives, row maxima keep growing
     # from chunk to chunk, so the running output is rescaled many times
