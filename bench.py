@@ -325,6 +325,29 @@ def _e2e(pa, wl, d, steps, warmup):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else the Arm
+    implementer / part codes), with the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if fields.get("model name"):
+        name = fields["model name"]
+    elif fields.get("CPU implementer"):
+        name = (f"implementer {fields['CPU implementer']}, "
+                f"part {fields.get('CPU part', '?')}")
+    else:
+        name = platform.processor() or "unknown"
+    return f"{platform.machine()}: {name}"
+
+
 def _cpu_baseline(wl, bytes_per_step, budget_s=12.0, max_reps=20):
     """The oracle, as it stands, on the host cores: whole decode steps of the
     same workload until about `budget_s` of CPU work."""
@@ -342,6 +365,7 @@ def _cpu_baseline(wl, bytes_per_step, budget_s=12.0, max_reps=20):
         times.append(time.perf_counter() - t0)
     t = statistics.mean(times)
     return {"value": bytes_per_step / t / 1e12, "unit": "TB/s", "cores": cores,
+            "cpu": _cpu_model(),
             "kind": "oracle",
             "sample": (f"{len(times)} whole decode steps of the same batch "
                        f"(64 seqs), fp64, {cores} threads, "
@@ -619,6 +643,7 @@ def run_reference(args):
                                 "bf16 KV, block 16, 20,000-block permuted "
                                 "pool")},
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores,
+                         "cpu": _cpu_model(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
