@@ -113,6 +113,8 @@ enum : int {
   kNumBars = kPvDone2 + 1
 };
 
+constexpr int kSlotInts = 12;  // a tile slot: its index, then the TcTile fields
+
 struct TcLayout {
   static constexpr int kK = 0;                               // K stages
   static constexpr int kV = kK + kKStages * kTileBytes;      // V stages
@@ -121,7 +123,7 @@ struct TcLayout {
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileSlot = kAbort + 4;               // int[2][kSlotInts]
-  static constexpr int kXchgSlot = kTileSlot + 2 * 12 * 4;   // float[2][2][128]
+  static constexpr int kXchgSlot = kTileSlot + 2 * kSlotInts * 4;  // float[2][2][128]
   // the step's tile list when the kernel plans it: per request, the first
   // tile (x heads) and the tile count; block-scan scratch
   static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
@@ -269,7 +271,6 @@ __device__ __forceinline__ int snake_tile(int k, int total) {
 // Tile slots: the warp that draws the tiles decodes each one (its metadata
 // takes global reads whose latency would otherwise hit every warp at every
 // tile start) and hands it to the other warps through slot k % 2.
-constexpr int kSlotInts = 12;  // li, then the TcTile fields
 __device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTile& t) {
   slot[0] = li;
   slot[1] = t.r;
