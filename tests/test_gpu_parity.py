@@ -512,3 +512,19 @@ def test_output_16_byte_aligned(dtype):
     assert out.data_ptr() == out_view.data_ptr()
     ref, *_ = _oracle_full(wl)
     assert_close(out, ref, md, dtype, dtype)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (36, 3)])
+def test_fp8_cache_every_code(Hq, Hkv):
+    # cache bytes cover every E4M3 code but the two NaNs (subnormals, both
+    # zeros, +-448): the kernels widen each exactly as the oracle decodes it.
+    # 32/8 heads run the head-group kernel, 36/3 (12 rows per KV head) the
+    # one-head kernel's 16-row path
+    wl = _custom([(700, 1), (300, 1), (45, 1)], Hq, Hkv, cache_dtype="e4m3")
+    codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)],
+                         dtype=torch.uint8)
+    for t, mul in ((wl.k_cache, 7), (wl.v_cache, 11)):
+        idx = (torch.arange(t.numel(), dtype=torch.int64) * mul) % codes.numel()
+        t.view(-1).copy_(codes[idx])
+    wl.k_scale, wl.v_scale = 0.004, 0.005
+    _check_step(wl)
