@@ -43,6 +43,10 @@ reshape_vec_kernel(const Tin* __restrict__ key, const Tin* __restrict__ value,
   const int rem2 = rem - which * num_kv_heads * chunks;
   const int h = rem2 / chunks;
   const int c = rem2 - h * chunks;
+  // the row does not depend on the slot: both loads go out together
+  const Tin* src = (which ? value + t * value_stride : key + t * key_stride) +
+                   (int64_t)h * head_dim + c * 8;
+  const Vec<Tin, 8> in = *reinterpret_cast<const Vec<Tin, 8>*>(src);
   const int64_t slot = __ldg(slot_mapping + t);
   if (slot < 0) return;  // padding token
   if (slot >= num_slots) {
@@ -50,10 +54,7 @@ reshape_vec_kernel(const Tin* __restrict__ key, const Tin* __restrict__ value,
     return;
   }
   const int64_t b = slot / kBS, o = slot - (slot / kBS) * kBS;
-  const Tin* src = (which ? value + t * value_stride : key + t * key_stride) +
-                   (int64_t)h * head_dim + c * 8;
   const int64_t dst = ((b * num_kv_heads + h) * kBS + o) * head_dim + c * 8;
-  const Vec<Tin, 8> in = *reinterpret_cast<const Vec<Tin, 8>*>(src);
   if constexpr (!kFp8) {
     Tin* cache = static_cast<Tin*>(which ? v_cache : k_cache);
     *reinterpret_cast<Vec<Tin, 8>*>(cache + dst) = in;
