@@ -341,8 +341,12 @@ def _cpu_model() -> str:
     if fields.get("model name"):
         name = fields["model name"]
     elif fields.get("CPU implementer"):
-        name = (f"implementer {fields['CPU implementer']}, "
-                f"part {fields.get('CPU part', '?')}")
+        part = fields.get("CPU part", "?")
+        arm = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1",
+               "0xd49": "Arm Neoverse N2", "0xd0c": "Arm Neoverse N1"}
+        known = arm.get(part) if fields["CPU implementer"] == "0x41" else None
+        name = (f"{known + ' (' if known else ''}implementer "
+                f"{fields['CPU implementer']}, part {part}{')' if known else ''}")
     else:
         name = platform.processor() or "unknown"
     return f"{platform.machine()}: {name}"
