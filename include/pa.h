@@ -268,10 +268,13 @@ pa_status pa_attention_noalloc(const void* q, pa_dtype q_dtype,
  * pa_set_profile_events -- measurement hook (no counterpart on the pages).
  * When both events are non-NULL, every later pa_attention call on this
  * thread records `start` on its stream immediately before the launch of its
- * attention kernels (the tensor-core prefill kernel, when the step has
- * prefill tiles for it, then the main attention kernel) and `stop`
- * immediately after them, so that cudaEventElapsedTime gives their device
- * time alone (the planning and split-merge launches are outside the pair).
+ * attention kernels (the main attention kernel and, when the step has
+ * prefill tiles for it, the tensor-core prefill kernel, in the order the
+ * step runs them) and `stop` immediately after them, so that
+ * cudaEventElapsedTime gives their device time alone (the planning and
+ * split-merge launches are outside the pair).  While the events are on,
+ * these launches run one after the other: a step that would otherwise run
+ * part of its prefill tiles beside the decode kernel runs them all behind it.
  * NULL, NULL turns it off.  The events are owned by the caller and must
  * outlive the calls.
  */
