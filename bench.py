@@ -400,6 +400,20 @@ def _kernel_hash():
     return h.hexdigest()
 
 
+def _headline_config(wl, ws):
+    """The `config` object of the headline line, identical in both arms: the
+    workload and its sizes (the reference arm attends a bounded sample of it,
+    described in its cpu_baseline)."""
+    return {
+        "workload": ("Llama-3.1-8B-shaped decode: 64 seqs, context "
+                     "U[512,4096], 32q/8kv heads, head_dim 128, bf16 KV, "
+                     "block 16, 20,000-block permuted pool"),
+        "kv_bytes": wl.kv_bytes(), "q_out_bytes": wl.qo_bytes(),
+        "l2": "flushed between timed steps (512 MiB read); KV 595 MB > L2",
+        "parallelism": f"replicas x{ws}",
+    }
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -556,15 +570,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {
-            "workload": ("Llama-3.1-8B-shaped decode: 64 seqs, context "
-                         "U[512,4096], 32q/8kv heads, head_dim 128, bf16 KV, "
-                         "block 16, 20,000-block permuted pool"),
-            "kv_bytes": kv_bytes, "q_out_bytes": wl.qo_bytes(),
-            "l2": "flushed between timed steps (512 MiB read); KV 595 MB > L2",
-            "parallelism": f"replicas x{ws}",
-            "wall_s": wall,
-        },
+        "config": _headline_config(wl, ws),
+        "wall_s": wall,
         "roofline": {
             "bound": "hbm", "kernel": "attn_decode_hg_kernel (bf16, KV-head groups of 4)",
             "achieved": achieved_gbs, "peak": peak_gbs, "unit": "GB/s",
@@ -642,10 +649,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": ("Llama-3.1-8B-shaped decode: 64 seqs, context "
-                                "U[512,4096], 32q/8kv heads, head_dim 128, "
-                                "bf16 KV, block 16, 20,000-block permuted "
-                                "pool")},
+        "config": _headline_config(wl, ws),
         "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores,
                          "cpu": _cpu_model(),
                          "kind": "oracle", "sample": sample},

@@ -27,6 +27,10 @@
  *    and records a flag that pa_get_device_error reports.
  *  - Unsupported type / shape combinations return PA_ERR_UNSUPPORTED; there
  *    is no fallback path of any kind.
+ *  - The library looks up a few device addresses of its own (the device
+ *    error word, the scratch of pa_attention_noalloc) once per device and
+ *    keeps them for the life of the process.  cudaDeviceReset invalidates
+ *    them: after a reset, make no further call in that process.
  *
  * KV-cache layout (fixed by this library; the pages do not prescribe one):
  *    k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
@@ -219,6 +223,17 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
                        pa_stream_t stream);
 
 /*
+ * pa_set_debug_bounds -- the device-side index checks of the pages' metadata
+ * (block ids, slots, lengths, query offsets; see the conventions above).
+ * In this library those checks are compiled into every kernel and cannot be
+ * switched off: they are integer compares on values the kernels load anyway,
+ * one per physical page or per request, beside 4 KiB page copies.
+ * enable != 0: PA_OK (the checks are on).  enable == 0: PA_ERR_UNSUPPORTED,
+ * nothing changes.
+ */
+pa_status pa_set_debug_bounds(int enable);
+
+/*
  * pa_get_device_error -- synchronise `stream`, then read and clear the
  * device-side error flags of the current device (PA_DEV_ERR_* bits, 0 if
  * none) into *flags.  Returns PA_ERR_DEVICE if any flag was set, PA_OK
@@ -244,7 +259,11 @@ pa_status pa_get_device_error(pa_stream_t stream, uint32_t* flags);
  *    anything runs.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept until the process
+ *    exits; a cudaDeviceReset invalidates it.
+ *  - Every decode step needs a fixed floor of split-K partial slots (about
+ *    65 KiB per SM); the scratch size is checked against that floor for up
+ *    to 160 SMs when the library is compiled.
  *  - All calls share the one array, which keeps the previous call's
  *    contents (nothing in it needs to start at zero).  Calls whose work
  *    overlaps on the GPU -- on different streams, or from different host

@@ -36,7 +36,8 @@ BLOCK_SIZE = 16
 EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_copy_blocks",
             "pa_attention_workspace_size", "pa_attention",
             "pa_get_device_error", "pa_set_profile_events",
-            "pa_launch_count", "pa_attention_noalloc")
+            "pa_launch_count", "pa_attention_noalloc",
+            "pa_set_debug_bounds")
 
 _DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3}
 _lib = None
@@ -82,6 +83,12 @@ def load_library(path: str = LIB_PATH):
     lib.pa_set_profile_events.restype = i32
     lib.pa_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     lib.pa_launch_count.restype = i32
+    lib.pa_set_debug_bounds.argtypes = [i32]
+    lib.pa_set_debug_bounds.restype = i32
+    lib.pa_attention_noalloc.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32,
+                                         i32, P, i32, P, P, i32, i64, i32, i32,
+                                         f32, f32, f32, P, P]
+    lib.pa_attention_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -121,6 +128,35 @@ def _stream(stream) -> int:
 def _check(status: int, what: str) -> None:
     if status != PA_OK:
         raise PaError(status, what)
+
+
+def _step_shapes(q, k_cache, v_cache, block_tables, seq_lens,
+                 query_start_loc, out):
+    """Check the tensors of one attention step the way the C ABI reads them
+    (contiguous, int32 metadata, consistent sizes) and return (T, Hq, D, NB,
+    Hkv, block_size, B).  Runs before any pointer is taken, so a strided q or
+    an int64 length array is refused instead of being read as raw bytes."""
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [T, Hq, D] and the caches [NB, Hkv, 16, D]")
+    T, Hq, D = q.shape
+    NB, Hkv, bs, Dc = k_cache.shape
+    if Dc != D:
+        raise ValueError("head_dim of q and of the caches differ")
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"),
+                 (query_start_loc, "query_start_loc")):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 tensor")
+    B = seq_lens.numel()
+    if (query_start_loc.numel() != B + 1 or block_tables.dim() != 2
+            or block_tables.shape[0] != B):
+        raise ValueError("inconsistent number of sequences")
+    if out is not None and (out.shape != q.shape or out.dtype != q.dtype
+                            or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor like q")
+    return T, Hq, D, NB, Hkv, bs, B
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor,
@@ -188,17 +224,8 @@ def pa_attention(q: torch.Tensor, k_cache: torch.Tensor,
     """q [T, Hq, D]; caches [NB, Hkv, 16, D]; block_tables int32 [B, M];
     seq_lens int32 [B]; query_start_loc int32 [B+1].  Returns out [T, Hq, D]
     (allocated if not given; the workspace too)."""
-    T, Hq, D = q.shape
-    NB, Hkv, bs, Dc = k_cache.shape
-    B = seq_lens.numel()
-    for t, n in ((block_tables, "block_tables"), (seq_lens, "seq_lens"),
-                 (query_start_loc, "query_start_loc")):
-        if t.dtype != torch.int32 or not t.is_contiguous():
-            raise ValueError(f"{n} must be a contiguous int32 tensor")
-    if query_start_loc.numel() != B + 1 or block_tables.shape[0] != B:
-        raise ValueError("inconsistent number of sequences")
-    if not q.is_contiguous():
-        raise ValueError("q must be contiguous")
+    T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
+                                            seq_lens, query_start_loc, out)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -243,6 +270,13 @@ def pa_set_profile_events(start: Optional[torch.cuda.Event],
            "pa_set_profile_events")
 
 
+def pa_set_debug_bounds(enable: bool) -> None:
+    """The device-side index checks are always on: True is accepted, False
+    raises (PA_ERR_UNSUPPORTED)."""
+    _check(_load().pa_set_debug_bounds(1 if enable else 0),
+           "pa_set_debug_bounds")
+
+
 def pa_launch_count() -> int:
     """Kernels the library has launched from this thread so far."""
     n = ctypes.c_uint64(0)
@@ -261,19 +295,11 @@ def pa_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
     """pa_attention with the library's fixed device scratch instead of a
     workspace, for callers that cannot allocate device memory per step (the
     output tensor is still the caller's)."""
-    lib = _load()
-    f = lib.pa_attention_noalloc
-    P, i64, i32, f32 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
-                        ctypes.c_float)
-    f.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32, i32, P, i32, P, P,
-                  i32, i64, i32, i32, f32, f32, f32, P, P]
-    f.restype = i32
-    T, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_cache.shape
-    B = seq_lens.numel()
     if out is None:
         raise ValueError("pa_attention_noalloc needs a caller-provided out")
-    st = f(_dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
+    T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
+                                            seq_lens, query_start_loc, out)
+    st = _load().pa_attention_noalloc(_dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
            _dev(v_cache, "v_cache"), _dtype_code(k_cache, cache_dtype), NB, bs,
            Hq, Hkv, D, _dev(block_tables, "block_tables"),
            block_tables.shape[1], _dev(seq_lens, "seq_lens"),

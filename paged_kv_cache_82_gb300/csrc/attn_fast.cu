@@ -55,6 +55,7 @@ constexpr int kSelfPlanMaxSeqsWide = 512;
 constexpr int kHg = 4;            // KV heads of a head-group decode item
 constexpr int kHgMaxSeqs = 512;   // requests of a step the head-group kernel takes
 constexpr int kHgPartRows = 32;   // partial rows per slot there: kHg heads x 8
+static_assert(kHgPartRows == kPartialRowsPerSlot, "partial slot rows");
 
 #ifndef PA_PRODUCER_PAGES
 #define PA_PRODUCER_PAGES 4     // pages the producer issues per step (2 lanes each)

@@ -406,6 +406,10 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_set_debug_bounds(int enable) {
+  return enable ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 pa_status pa_launch_count(uint64_t* count) {
   if (!count) return PA_ERR_INVALID_ARG;
   *count = t_launches;

@@ -47,6 +47,14 @@ constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
 #endif
 constexpr int kMaxCtasPerSm = PA_CTAS_PER_SM;  // grid bound of the attention kernels
 
+// Rows of one split-K partial slot (a head group's 4 KV heads x 8 rows) and
+// the partial-result bytes make_plan reserves per SM whatever the step's
+// size: two slots per resident attention CTA, each rows x head_dim 128 fp32
+// accumulators plus (m, l).  A batch-1 decode needs this much workspace.
+constexpr int kPartialRowsPerSlot = 32;
+constexpr size_t kPartialBytesPerSm =
+    (size_t)2 * kMaxCtasPerSm * kPartialRowsPerSlot * (128 + 2) * 4;
+
 struct AttnPlan {
   int group;            // Hq / Hkv
   int has_prefill;      // some request may have > 16 query rows

@@ -13,14 +13,28 @@
 // holds it (PA_NOALLOC_SCRATCH_BYTES) until the process exits.  Host code
 // cannot use the array's name as a device address; its address is looked up
 // once per device with cudaGetSymbolAddress, on the first call made while
-// that device is current.
+// that device is current, and kept for the life of the process (a
+// cudaDeviceReset invalidates it, as it does every other device address the
+// library holds; pa.h says so).
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/pa.h"
+#include "pa_internal.h"
 
 namespace {
+
+// The workspace of every decode step holds the split-K partial slots of all
+// resident attention CTAs, whatever the batch: kPartialBytesPerSm per SM.
+// The scratch must hold that floor on the largest GPU this library targets
+// (160 SMs; GB300 enables 152) with room to spare for the step's lists,
+// otherwise every decode call would be rejected.  A build with more resident
+// CTAs per SM (PA_CTAS_PER_SM) that breaks this must raise the size.
+constexpr size_t kMaxTargetSms = 160;
+static_assert(pa::kPartialBytesPerSm * kMaxTargetSms + (2u << 20) <=
+                  (size_t)PA_NOALLOC_SCRATCH_BYTES,
+              "PA_NOALLOC_SCRATCH_BYTES is below the decode workspace floor");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 

@@ -41,6 +41,21 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"{name} not exported by libpa.so"
 
 
+def test_exports_match_the_boundary_table():
+    """The design doc's boundary table lists every entry point of pa.h (the
+    proposed declarations mapped to the header's); nothing is missing and
+    nothing extra is exported."""
+    text = open(os.path.join(ROOT, "DESIGN.md")).read()
+    start = text.index("**The boundary against the survey's proposed header.**")
+    table = text[start:text.index("\n\n", text.index("| proposed |", start))]
+    in_table = set()
+    for line in table.splitlines()[2:]:
+        cells = line.split("|")
+        if len(cells) > 2 and line.startswith("|"):
+            in_table |= set(re.findall(r"`(pa_[a-z_]+)", cells[2]))
+    assert in_table == set(_declared())
+
+
 def test_binding_names_match_the_abi():
     import paged_kv_cache_82_gb300 as pa
     for name in _declared():
@@ -95,13 +110,37 @@ def test_step_metadata_matches_oracle_bit_exact():
         assert a["max_seq_len"] == b["max_seq_len"]
 
 
-def test_workspace_plan_is_pure_host_logic():
-    """The workspace size depends only on host-known sizes; it grows with the
-    step and stays modest (split partials bounded)."""
-    pytest.importorskip("torch")
-    # exercised through the C ABI on GPU machines; here only the formula's
-    # inputs are validated by the header (no device to query the SM count)
-    assert "pa_attention_workspace_size" in _declared()
+@pytest.mark.gpu
+def test_workspace_size_grows_with_the_step_and_stays_bounded():
+    """The workspace depends on host-known sizes only: it never shrinks when
+    the step grows, it is the partial-slot floor plus a few bytes per request
+    and per query token, and the benchmark steps fit the 16 MiB scratch of
+    pa_attention_noalloc."""
+    import paged_kv_cache_82_gb300 as pa
+    ws = pa.pa_attention_workspace_size
+    floor = ws(1, 32, 8, 128, 1, 1, 16)
+    prev = 0
+    for B in (1, 2, 64, 512, 4096):
+        n = ws(B, 32, 8, 128, B, 1, 4096)
+        assert n >= prev and n >= floor
+        # decode only: lists of O(1) bytes per (request, KV head)
+        assert n - floor <= B * 8 * 64 + (1 << 16)
+        prev = n
+    # a longer context needs no more workspace (its pages are walked, not
+    # stored); more query rows (prefill tiles) need more
+    assert ws(64, 32, 8, 128, 64, 1, 131072) == ws(64, 32, 8, 128, 64, 1, 512)
+    assert ws(1142, 32, 8, 128, 121, 1022, 8193) > ws(121, 32, 8, 128, 121, 1,
+                                                      8193)
+    scratch = 16 << 20
+    for T, Hq, Hkv, B, mq, ms in ((64, 32, 8, 64, 1, 4096),        # decode
+                                  (1142, 32, 8, 121, 1022, 10193),  # mixed
+                                  (32, 32, 32, 32, 1, 8192),       # MHA
+                                  (16, 64, 8, 16, 1, 131073)):     # FP8 long
+        assert ws(T, Hq, Hkv, 128, B, mq, ms) <= scratch
+    with pytest.raises(pa.PaError):
+        ws(1, 7, 2, 128, 1, 1, 16)        # heads not a multiple
+    with pytest.raises(pa.PaError):
+        ws(1, 8, 2, 96, 1, 1, 16)         # head_dim
 
 
 def test_launch_count_without_a_gpu(lib):
