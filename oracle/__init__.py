@@ -78,11 +78,12 @@ def _bind(lib):
     lib.orc_copy_blocks.restype = i32
     lib.orc_paged_attention.argtypes = [P, i32, P, P, i32, i64, i32, i32,
                                         i32, i32, P, i32, P, P, i32, f64,
-                                        f64, f64, P, i32]
+                                        f64, f64, P, i32, i32]
     lib.orc_paged_attention.restype = i32
     lib.orc_paged_attention_row.argtypes = [P, i32, P, P, i32, i64, i32,
                                             i32, i32, i32, P, i32, P, P,
-                                            i32, i32, i32, f64, f64, f64, P]
+                                            i32, i32, i32, f64, f64, f64, P,
+                                            i32]
     lib.orc_paged_attention_row.restype = i32
     lib.orc_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
     lib.orc_kv_bytes_per_token.restype = i64
@@ -273,8 +274,10 @@ def copy_blocks(k_cache, v_cache, block_mapping, *, cache_dtype):
 
 def paged_attention(q, k_cache, v_cache, block_tables, seq_lens,
                     query_start_loc, *, scale, cache_dtype=None, q_dtype=None,
-                    k_scale=1.0, v_scale=1.0, num_threads=None):
-    """fp64 output [T, Hq, D] of the step (rows of unowned tokens are NaN)."""
+                    k_scale=1.0, v_scale=1.0, num_threads=None, window=0):
+    """fp64 output [T, Hq, D] of the step (rows of unowned tokens are NaN).
+    window > 0: each query sees only its own key and the window - 1 keys
+    before it (sliding-window attention)."""
     qa, qdt = _as_np(q)
     kc, kcdt = _as_np(k_cache)
     vc, _ = _as_np(v_cache)
@@ -291,15 +294,15 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens,
     _check(_load().orc_paged_attention(
         _ptr(qa), qdt, _ptr(kc), _ptr(vc), cdt, NB, bs, Hq, Hkv, D, _ptr(bt),
         bt.shape[1], _ptr(sl), _ptr(qsl), sl.shape[0], float(scale),
-        float(k_scale), float(v_scale), _ptr(out), int(num_threads)),
-        "paged_attention")
+        float(k_scale), float(v_scale), _ptr(out), int(num_threads),
+        int(window)), "paged_attention")
     return out
 
 
 def paged_attention_row(q, k_cache, v_cache, block_tables, seq_lens,
                         query_start_loc, r: int, i: int, h: int, *, scale,
                         cache_dtype=None, q_dtype=None, k_scale=1.0,
-                        v_scale=1.0):
+                        v_scale=1.0, window=0):
     """fp64 output row of request r, query i, head h (same definition)."""
     qa, qdt = _as_np(q)
     kc, kcdt = _as_np(k_cache)
@@ -315,7 +318,8 @@ def paged_attention_row(q, k_cache, v_cache, block_tables, seq_lens,
     _check(_load().orc_paged_attention_row(
         _ptr(qa), qdt, _ptr(kc), _ptr(vc), cdt, NB, bs, Hq, Hkv, D, _ptr(bt),
         bt.shape[1], _ptr(sl), _ptr(qsl), r, i, h, float(scale),
-        float(k_scale), float(v_scale), _ptr(out)), "paged_attention_row")
+        float(k_scale), float(v_scale), _ptr(out), int(window)),
+        "paged_attention_row")
     return out
 
 
@@ -342,5 +346,6 @@ def run_step(wl, num_threads=None):
                           md["seq_lens"], md["query_start_loc"],
                           scale=wl.scale, cache_dtype=cdt,
                           k_scale=wl.k_scale, v_scale=wl.v_scale,
-                          num_threads=num_threads)
+                          num_threads=num_threads,
+                          window=getattr(wl, "sliding_window", 0))
     return out, kc, vc, md

@@ -25,6 +25,11 @@
  *  - "vLLM V0 vs V1" (llm.rainlin.net), section 3.1: per step the model runner
  *    builds attention metadata from each request's query length, context
  *    length and block table; V0's scheduler output carries blocks_to_copy.
+ *  - "vLLM: a general inference engine" (niuwancheng.cn), section "KV cache
+ *    management and prefix caching", the hybrid KV cache manager paragraph:
+ *    sliding-window attention layers, whose blocks outside the window can be
+ *    released early.  A window of W keys lets the query at position p see
+ *    keys max(0, p - W + 1) .. p: its own key and the W - 1 before it.
  *  - "vLLM: a general inference engine" (niuwancheng.cn), KV cache table:
  *    --kv-cache-dtype fp8 stores KV in 1-byte FP8.  The E4M3 "FN" format
  *    (bias 7, no infinities, S.1111.111 = NaN, max 448) is taken from the
@@ -249,7 +254,16 @@ int orc_copy_blocks(void* k_cache, void* v_cache, int cache_dtype,
 /*   out = sum_j exp(s_j - max s) v_j / sum_j exp(s_j - max s)             */
 /*                                                                         */
 /* with k_j = k_scale * stored value (k_scale = 1 unless FP8), likewise v. */
+/*                                                                         */
+/* With a sliding window of W > 0 keys the query at position p sees only   */
+/* keys max(0, p - W + 1) .. p; W = 0 means no window.                     */
 /* ---------------------------------------------------------------------- */
+static int first_visible_key(int position, int window) {
+  if (window <= 0) return 0;
+  int first = position - window + 1;
+  return first > 0 ? first : 0;
+}
+
 typedef struct {
   const void* q;
   int q_dtype;
@@ -264,6 +278,7 @@ typedef struct {
   const int32_t* query_start_loc;
   int num_seqs;
   double scale, k_scale, v_scale;
+  int window;
   double* out;
   /* work distribution */
   int64_t next_item;
@@ -289,11 +304,12 @@ static int attend_one(attn_job* J, int r, int h) {
   for (int i = 0; i < n; ++i) {
     const int64_t t = J->query_start_loc[r] + i;
     const int visible = L - n + i + 1; /* keys 0 .. L-n+i */
+    const int first = first_visible_key(L - n + i, J->window);
     for (int d = 0; d < D; ++d)
       qv[d] = load_elem(J->q, (t * J->num_q_heads + h) * (int64_t)D + d,
                         J->q_dtype);
     double smax = -INFINITY;
-    for (int j = 0; j < visible; ++j) {
+    for (int j = first; j < visible; ++j) {
       int32_t b = J->block_tables[(int64_t)r * J->max_blocks_per_seq + j / bs];
       if (b < 0 || b >= J->num_blocks || j / bs >= J->max_blocks_per_seq) {
         free(s);
@@ -309,13 +325,13 @@ static int attend_one(attn_job* J, int r, int h) {
       if (s[j] > smax) smax = s[j];
     }
     double denom = 0.0;
-    for (int j = 0; j < visible; ++j) {
+    for (int j = first; j < visible; ++j) {
       s[j] = exp(s[j] - smax);
       denom += s[j];
     }
     double* o = J->out + (t * J->num_q_heads + h) * (int64_t)D;
     for (int d = 0; d < D; ++d) o[d] = 0.0;
-    for (int j = 0; j < visible; ++j) {
+    for (int j = first; j < visible; ++j) {
       int32_t b = J->block_tables[(int64_t)r * J->max_blocks_per_seq + j / bs];
       int64_t base = (((int64_t)b * J->num_kv_heads + g) * bs + j % bs) * D;
       for (int d = 0; d < D; ++d)
@@ -359,10 +375,10 @@ int orc_paged_attention(const void* q, int q_dtype, const void* k_cache,
                         const int32_t* seq_lens,
                         const int32_t* query_start_loc, int num_seqs,
                         double scale, double k_scale, double v_scale,
-                        double* out, int num_threads) {
+                        double* out, int num_threads, int window) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
       block_size <= 0 || elem_bytes(q_dtype) == 0 ||
-      elem_bytes(cache_dtype) == 0)
+      elem_bytes(cache_dtype) == 0 || window < 0)
     return ORC_BAD_ARG;
   attn_job J;
   memset(&J, 0, sizeof J);
@@ -384,6 +400,7 @@ int orc_paged_attention(const void* q, int q_dtype, const void* k_cache,
   J.scale = scale;
   J.k_scale = (cache_dtype == ORC_E4M3) ? k_scale : 1.0;
   J.v_scale = (cache_dtype == ORC_E4M3) ? v_scale : 1.0;
+  J.window = window;
   J.out = out;
   J.next_item = 0;
   J.status = ORC_OK;
@@ -413,21 +430,22 @@ int orc_paged_attention_row(const void* q, int q_dtype, const void* k_cache,
                             int max_blocks_per_seq, const int32_t* seq_lens,
                             const int32_t* query_start_loc, int r, int i,
                             int h, double scale, double k_scale,
-                            double v_scale, double* out_row) {
+                            double v_scale, double* out_row, int window) {
   const int D = head_dim, bs = block_size;
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return ORC_BAD_ARG;
   const int g = h / (num_q_heads / num_kv_heads);
   const int n = query_start_loc[r + 1] - query_start_loc[r];
   const int L = seq_lens[r];
-  if (i < 0 || i >= n || L < n) return ORC_BAD_ARG;
+  if (i < 0 || i >= n || L < n || window < 0) return ORC_BAD_ARG;
   const double ks = (cache_dtype == ORC_E4M3) ? k_scale : 1.0;
   const double vs = (cache_dtype == ORC_E4M3) ? v_scale : 1.0;
   const int64_t t = query_start_loc[r] + i;
   const int visible = L - n + i + 1;
+  const int first = first_visible_key(L - n + i, window);
   double* s = (double*)malloc(sizeof(double) * (size_t)visible);
   if (!s) return ORC_BAD_ARG;
   double smax = -INFINITY;
-  for (int j = 0; j < visible; ++j) {
+  for (int j = first; j < visible; ++j) {
     int32_t b = block_tables[(int64_t)r * max_blocks_per_seq + j / bs];
     if (b < 0 || b >= num_blocks) {
       free(s);
@@ -442,12 +460,12 @@ int orc_paged_attention_row(const void* q, int q_dtype, const void* k_cache,
     if (s[j] > smax) smax = s[j];
   }
   double denom = 0.0;
-  for (int j = 0; j < visible; ++j) {
+  for (int j = first; j < visible; ++j) {
     s[j] = exp(s[j] - smax);
     denom += s[j];
   }
   for (int d = 0; d < D; ++d) out_row[d] = 0.0;
-  for (int j = 0; j < visible; ++j) {
+  for (int j = first; j < visible; ++j) {
     int32_t b = block_tables[(int64_t)r * max_blocks_per_seq + j / bs];
     int64_t base = (((int64_t)b * num_kv_heads + g) * bs + j % bs) * D;
     for (int d = 0; d < D; ++d)

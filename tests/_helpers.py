@@ -20,12 +20,12 @@ def scatter_paged(seqs, block_lists, num_blocks, fill=np.nan):
     return cache
 
 
-def sdpa_reference(q_seqs, k_seqs, v_seqs, group, scale):
+def sdpa_reference(q_seqs, k_seqs, v_seqs, group, scale, window=0):
     """Per request: q [n, Hq, D], k/v [L, Hkv, D] (float64) -> [n, Hq, D].
 
     Query i of a request with n queries and L keys sees keys 0..L-n+i
-    (bottom-right causal alignment); GQA by repeating each KV head `group`
-    times."""
+    (bottom-right causal alignment), and with window > 0 only the last
+    `window` of those; GQA by repeating each KV head `group` times."""
     outs = []
     for q, k, v in zip(q_seqs, k_seqs, v_seqs):
         n, L = q.shape[0], k.shape[0]
@@ -37,6 +37,8 @@ def sdpa_reference(q_seqs, k_seqs, v_seqs, group, scale):
         i = torch.arange(n)[:, None]
         j = torch.arange(L)[None, :]
         mask = j <= (L - n + i)
+        if window > 0:
+            mask = mask & (j > (L - n + i - window))
         o = torch.nn.functional.scaled_dot_product_attention(
             Q, K, V, attn_mask=mask, scale=scale)
         outs.append(o.numpy().transpose(1, 0, 2))

@@ -31,6 +31,9 @@ MUTANTS = {
     # K scale applied to V
     "scale_swap": (["o[d] += s[j] * (J->v_scale *"],
                    ["o[d] += s[j] * (J->k_scale *"]),
+    # sliding window one key wide too many (keys p - W .. p)
+    "window_off_by_one": (["  int first = position - window + 1;"],
+                          ["  int first = position - window;"]),
     # ties to odd
     "ties_to_odd": (["(c & 1) == 0 && (best & 1) == 1"],
                     ["(c & 1) == 1 && (best & 1) == 0"]),
@@ -53,6 +56,7 @@ CATCHERS = {
     "no_max_shift": pins.test_closed_forms,
     "scale_swap": pins.test_paged_bf16_and_fp8_match_sdpa_on_decoded_values,
     "ties_to_odd": pins.test_e4m3_encode_roundtrip_and_ties,
+    "window_off_by_one": pins.test_window_of_one_key_is_the_own_value,
     "layout_swap": pins.test_fig2_reshape_writes_only_the_new_slots,
     "copy_k_only": pins.test_copy_blocks_copies_whole_blocks_only,
 }

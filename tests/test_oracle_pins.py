@@ -467,7 +467,7 @@ def test_closed_forms():
 # ---------------------------------------------------------------------------
 # brute force: a second, naive formulation on tiny shapes
 # ---------------------------------------------------------------------------
-def _brute(q, kc, vc, reqs, Hq, Hkv, scale):
+def _brute(q, kc, vc, reqs, Hq, Hkv, scale, window=0):
     out = {}
     t = 0
     G = Hq // Hkv
@@ -478,7 +478,8 @@ def _brute(q, kc, vc, reqs, Hq, Hkv, scale):
             for h in range(Hq):
                 g = h // G
                 keys, vals = [], []
-                for j in range(limit + 1):
+                start = max(0, limit - window + 1) if window else 0
+                for j in range(start, limit + 1):
                     b = r.block_ids[j // BS]
                     keys.append([float(x) for x in kc[b, g, j % BS]])
                     vals.append([float(x) for x in vc[b, g, j % BS]])
@@ -540,3 +541,103 @@ def test_zero_length_request_produces_nothing():
                                  scale=1.0)
     assert md["query_start_loc"].tolist() == [0, 0, 2]
     assert np.isfinite(out).all()
+
+
+# ---------------------------------------------------------------------------
+# sliding window ("01. vLLM", hybrid KV cache manager paragraph: layers with
+# sliding-window attention; their blocks outside the window can be released)
+# ---------------------------------------------------------------------------
+def _window_step(seed=31, shapes=((1, 70), (9, 40), (1, 16), (20, 53)),
+                 Hq=8, Hkv=2, D=16, NB=24):
+    rng = np.random.default_rng(seed)
+    q, kc, vc, reqs, qs, ks, vs = random_paged_step(rng, list(shapes), Hq, Hkv,
+                                                    D, NB)
+    return q, kc, vc, reqs, qs, ks, vs, oracle.step_metadata(reqs)
+
+
+def _attn(q, kc, vc, md, window, scale=0.4):
+    return oracle.paged_attention(q, kc, vc, md["block_tables"],
+                                  md["seq_lens"], md["query_start_loc"],
+                                  scale=scale, window=window)
+
+
+def test_window_wider_than_the_context_is_no_window():
+    q, kc, vc, reqs, *_, md = _window_step()
+    base = _attn(q, kc, vc, md, 0)
+    for w in (70, 71, 1000):
+        assert np.array_equal(_attn(q, kc, vc, md, w), base)
+
+
+def test_window_of_one_key_is_the_own_value():
+    q, kc, vc, reqs, qs, ks, vs, md = _window_step()
+    out = _attn(q, kc, vc, md, 1)
+    G = 4
+    t = 0
+    for r, v in zip(reqs, vs):
+        L = r.num_computed + r.num_new
+        for i in range(r.num_new):
+            for h in range(8):
+                assert np.array_equal(out[t + i, h],
+                                      v[L - r.num_new + i, h // G].astype(
+                                          np.float64))
+        t += r.num_new
+
+
+@pytest.mark.parametrize("window", [2, 7, 16, 17, 33])
+def test_window_matches_banded_sdpa(window):
+    q, kc, vc, reqs, qs, ks, vs, md = _window_step()
+    out = _attn(q, kc, vc, md, window)
+    ref = sdpa_reference([x.astype(np.float64) for x in qs],
+                         [x.astype(np.float64) for x in ks],
+                         [x.astype(np.float64) for x in vs], 4, 0.4,
+                         window=window)
+    np.testing.assert_allclose(out, np.concatenate(ref, 0), rtol=0,
+                               atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_window_brute_force_tiny(seed):
+    rng = np.random.default_rng(2000 + seed)
+    shapes = [(int(rng.integers(1, 6)), int(rng.integers(6, 41)))
+              for _ in range(3)]
+    q, kc, vc, reqs, *_ = random_paged_step(rng, shapes, 4, 2, 8, 12)
+    md = oracle.step_metadata(reqs)
+    for window in (3, 16, 21):
+        out = _attn(q, kc, vc, md, window, scale=0.7)
+        ref = _brute(q, kc, vc, reqs, 4, 2, 0.7, window=window)
+        for (t, h), row in ref.items():
+            np.testing.assert_allclose(out[t, h], row, rtol=0, atol=1e-12)
+
+
+def test_blocks_outside_the_window_are_never_read():
+    """The blocks a request's queries cannot see may be released: poisoning
+    them, or pointing the table at a block that does not exist, changes
+    nothing."""
+    q, kc, vc, reqs, *_, md = _window_step()
+    window = 17
+    base = _attn(q, kc, vc, md, window)
+    bt = md["block_tables"].copy()
+    kc2, vc2 = kc.copy(), vc.copy()
+    for b, r in enumerate(reqs):
+        first = max(0, r.num_computed - window + 1)  # first query's first key
+        for k in range(first // 16):
+            kc2[bt[b, k]] = np.nan
+            vc2[bt[b, k]] = np.nan
+            bt[b, k] = 10 ** 6
+    md2 = dict(md, block_tables=bt)
+    assert np.array_equal(_attn(q, kc2, vc2, md2, window), base)
+    # without the window the same table is out of range
+    with pytest.raises(oracle.OracleError):
+        _attn(q, kc2, vc2, md2, 0)
+
+
+def test_window_row_function_equals_full_step():
+    q, kc, vc, reqs, *_, md = _window_step()
+    out = _attn(q, kc, vc, md, 9)
+    args = (q, kc, vc, md["block_tables"], md["seq_lens"],
+            md["query_start_loc"])
+    for r, i in ((0, 0), (1, 8), (3, 19), (3, 0)):
+        for h in (0, 7):
+            row = oracle.paged_attention_row(*args, r, i, h, scale=0.4,
+                                             window=9)
+            assert np.array_equal(row, out[md["query_start_loc"][r] + i, h])
