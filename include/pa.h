@@ -75,7 +75,8 @@ typedef enum {
 #define PA_DEV_ERR_SLOT 0x1u      /* slot >= num_blocks * block_size        */
 #define PA_DEV_ERR_BLOCK_ID 0x2u  /* block id outside [0, num_blocks)       */
 #define PA_DEV_ERR_METADATA 0x4u  /* seq_len / query_start_loc inconsistent */
-#define PA_DEV_ERR_TIMEOUT 0x8u   /* a bounded pipeline wait ran out        */
+#define PA_DEV_ERR_TIMEOUT 0x8u   /* a bounded pipeline wait ran out
+                                     (pa_set_wait_limit_ns)                   */
 
 /* The only block size supported: 16 tokens per physical block, the default
  * block size named in [Anatomy], "PagedAttention: paging the KV cache", and
@@ -221,6 +222,76 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
                        float scale, float k_scale, float v_scale, void* out,
                        void* workspace, size_t workspace_bytes,
                        pa_stream_t stream);
+
+/*
+ * pa_attention_window -- pa_attention for a layer with sliding-window
+ * attention.
+ *
+ * Defines: models with sliding-window attention layers, whose KV blocks
+ * that fall out of the window the hybrid KV cache manager can release early
+ * ([Overview], "KV cache management and prefix caching", the hybrid KV cache
+ * manager paragraph).  With a window of W keys, query i of request r (at
+ * position p = L_r - n_r + i) sees keys max(0, p - W + 1) .. p: its own key
+ * and the W - 1 before it.
+ *
+ * Arguments and results as pa_attention, plus sliding_window = W >= 0
+ * (negative: PA_ERR_INVALID_ARG).  W = 0 is no window, the same computation
+ * as pa_attention; a window of max_seq_len keys or more cuts nothing.  The
+ * workspace must hold pa_attention_window_workspace_size bytes for the same
+ * sizes and window.  Block-table entries of blocks that lie wholly before
+ * the first query's window (entries below (L_r - n_r - W + 1) / 16) are
+ * never read: those blocks may already be released and reused.
+ */
+pa_status pa_attention_window(const void* q, pa_dtype q_dtype,
+                              const void* k_cache, const void* v_cache,
+                              pa_dtype cache_dtype, int64_t num_blocks,
+                              int block_size, int num_q_heads, int num_kv_heads,
+                              int head_dim, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int num_seqs,
+                              int64_t num_tokens, int max_query_len,
+                              int max_seq_len, float scale, float k_scale,
+                              float v_scale, int sliding_window, void* out,
+                              void* workspace, size_t workspace_bytes,
+                              pa_stream_t stream);
+
+/*
+ * pa_attention_window_workspace_size -- bytes of device workspace
+ * pa_attention_window needs: pa_attention's, plus each request's block-table
+ * row and key count through the window (4 bytes per block of
+ * min(max_seq_len, max_query_len + W + 14) keys, and 4, per request).
+ */
+pa_status pa_attention_window_workspace_size(int64_t num_tokens,
+                                             int num_q_heads, int num_kv_heads,
+                                             int head_dim, int num_seqs,
+                                             int max_query_len, int max_seq_len,
+                                             int sliding_window, size_t* bytes);
+
+/*
+ * pa_set_wait_limit_ns -- the longest one pipeline wait inside the attention
+ * kernels may last (no counterpart on the pages; failure detection).  A
+ * kernel whose wait runs out records PA_DEV_ERR_TIMEOUT (pa_get_device_error),
+ * lets the copies and tensor-core work it has in flight complete, frees its
+ * tensor memory and returns: the CUDA context stays usable and the next
+ * call runs normally.  ns = 0 restores the default of 2 s; otherwise 0.1 ms
+ * <= ns <= 60 s (else PA_ERR_INVALID_ARG).  Applies to the current device
+ * and to kernels launched after the call; it copies to device memory
+ * synchronously, so it is a configuration call, not one for the step loop.
+ */
+pa_status pa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * pa_test_skip_copy -- testing hook for the bounded waits (no counterpart on
+ * the pages).  stage >= 0: in every later launch of the pipelined attention
+ * kernels (the head-group decode kernel, the tensor-core prefill kernel) on
+ * the current device, CTA 0 leaves out the copy of its pipeline stage
+ * number `stage` (counted from 0 per CTA), so that the waits on that stage
+ * can only run out: the step then reports PA_DEV_ERR_TIMEOUT and its output
+ * is undefined.  Nothing faults and nothing is left in flight.  stage = -1
+ * (the default) turns the hook off.  Same device-memory copy as
+ * pa_set_wait_limit_ns.
+ */
+pa_status pa_test_skip_copy(int64_t stage);
 
 /*
  * pa_set_debug_bounds -- the device-side index checks of the pages' metadata

@@ -37,7 +37,9 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_copy_blocks",
             "pa_attention_workspace_size", "pa_attention",
             "pa_get_device_error", "pa_set_profile_events",
             "pa_launch_count", "pa_attention_noalloc",
-            "pa_set_debug_bounds")
+            "pa_set_debug_bounds", "pa_attention_window",
+            "pa_attention_window_workspace_size", "pa_set_wait_limit_ns",
+            "pa_test_skip_copy")
 
 _DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3}
 _lib = None
@@ -83,6 +85,17 @@ def load_library(path: str = LIB_PATH):
     lib.pa_set_profile_events.restype = i32
     lib.pa_launch_count.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
     lib.pa_launch_count.restype = i32
+    lib.pa_attention_window.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32,
+                                        i32, P, i32, P, P, i32, i64, i32, i32,
+                                        f32, f32, f32, i32, P, P, sz, P]
+    lib.pa_attention_window.restype = i32
+    lib.pa_attention_window_workspace_size.argtypes = [
+        i64, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.pa_attention_window_workspace_size.restype = i32
+    lib.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.pa_set_wait_limit_ns.restype = i32
+    lib.pa_test_skip_copy.argtypes = [i64]
+    lib.pa_test_skip_copy.restype = i32
     lib.pa_set_debug_bounds.argtypes = [i32]
     lib.pa_set_debug_bounds.restype = i32
     lib.pa_attention_noalloc.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32,
@@ -247,6 +260,53 @@ def pa_attention(q: torch.Tensor, k_cache: torch.Tensor,
     return out
 
 
+def pa_attention_window_workspace_size(num_tokens: int, num_q_heads: int,
+                                       num_kv_heads: int, head_dim: int,
+                                       num_seqs: int, max_query_len: int,
+                                       max_seq_len: int,
+                                       sliding_window: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = _load().pa_attention_window_workspace_size(
+        num_tokens, num_q_heads, num_kv_heads, head_dim, num_seqs,
+        max_query_len, max_seq_len, sliding_window, ctypes.byref(out))
+    _check(st, "pa_attention_window_workspace_size")
+    return int(out.value)
+
+
+def pa_attention_window(q: torch.Tensor, k_cache: torch.Tensor,
+                        v_cache: torch.Tensor, block_tables: torch.Tensor,
+                        seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                        max_query_len: int, max_seq_len: int, scale: float,
+                        sliding_window: int, k_scale: float = 1.0,
+                        v_scale: float = 1.0,
+                        out: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        cache_dtype: Optional[str] = None,
+                        stream=None) -> torch.Tensor:
+    """pa_attention with a sliding window of `sliding_window` keys (each
+    query sees its own key and the window - 1 keys before it; 0: none)."""
+    T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
+                                            seq_lens, query_start_loc, out)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = pa_attention_window_workspace_size(
+            T, Hq, Hkv, D, B, max_query_len, max_seq_len, sliding_window)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8,
+                                device=q.device)
+    st = _load().pa_attention_window(
+        _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dtype_code(k_cache, cache_dtype), NB, bs, Hq,
+        Hkv, D, _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(seq_lens, "seq_lens"), _dev(query_start_loc, "query_start_loc"),
+        B, T, int(max_query_len), int(max_seq_len), float(scale),
+        float(k_scale), float(v_scale), int(sliding_window), _dev(out, "out"),
+        _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_attention_window")
+    return out
+
+
 def pa_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error flags."""
     flags = ctypes.c_uint32(0)
@@ -275,6 +335,18 @@ def pa_set_debug_bounds(enable: bool) -> None:
     raises (PA_ERR_UNSUPPORTED)."""
     _check(_load().pa_set_debug_bounds(1 if enable else 0),
            "pa_set_debug_bounds")
+
+
+def pa_set_wait_limit_ns(ns: int) -> None:
+    """Longest one pipeline wait in the kernels may last (0: the default
+    2 s); a wait that runs out is reported as PA_DEV_ERR_TIMEOUT."""
+    _check(_load().pa_set_wait_limit_ns(int(ns)), "pa_set_wait_limit_ns")
+
+
+def pa_test_skip_copy(stage: int) -> None:
+    """Testing hook: CTA 0 of the pipelined kernels leaves out the copy of
+    pipeline stage `stage` (-1: off), so that the waits on it run out."""
+    _check(_load().pa_test_skip_copy(int(stage)), "pa_test_skip_copy")
 
 
 def pa_launch_count() -> int:

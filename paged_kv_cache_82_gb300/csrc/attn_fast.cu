@@ -32,6 +32,8 @@
 // only keeps the ALU work (group x 128 MACs per key) off the CUDA cores.
 #include <float.h>
 
+#include <algorithm>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -156,6 +158,8 @@ struct FastParams {
   int attn_grid;      // CTAs of the attention kernel (the merge's plan)
   int no_dep_wait;    // 1: start without waiting for the grid before (it let
                       // this one start only after its own wait)
+  int window;         // sliding window in keys (kNoWindow: none): a row with
+                      // causal limit lim sees keys lim - window + 1 .. lim
 };
 
 // ---------------------------------------------------------------------------
@@ -688,7 +692,7 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
                                              const uint32_t (&qa)[8][4],
                                              WarpState& st, int key0,
                                              int valid_keys, bool need_mask,
-                                             int lim0, int lim1,
+                                             int lim0, int lim1, int win,
                                              float sscale0, float sscale1,
                                              int lane) {
   using Tr = Traits<kKind>;
@@ -705,8 +709,10 @@ __device__ __forceinline__ void process_page(uint32_t k_base, uint32_t v_base,
     for (int e = 0; e < 4; ++e) {
       float v = s[nt][e] * (e < 2 ? sscale0 : sscale1);
       if (need_mask) {
+        // visible: lim - win < key <= lim (the causal limit, the window)
         const int key = key0 + nt * 8 + ((e & 1) ? tB : tA);
-        if (key > (e < 2 ? lim0 : lim1)) v = -INFINITY;
+        const int lim = e < 2 ? lim0 : lim1;
+        if (key > lim || key <= lim - win) v = -INFINITY;
       }
       s[nt][e] = v;
     }
@@ -875,7 +881,7 @@ template <int kKind>
 __device__ __forceinline__ void process_page_narrow(
     uint32_t k_base, uint32_t v_base, const uint32_t (&qa)[8][4],
     NarrowState& st, int key0, int valid_keys, bool need_mask, int lim,
-    float sscale, int lane) {
+    int win, float sscale, int lane) {
   using Tr = Traits<kKind>;
   constexpr bool kB = Tr::kMmaBF16;
   constexpr uint32_t P = Tr::kPerm;
@@ -888,7 +894,11 @@ __device__ __forceinline__ void process_page_narrow(
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float v = s[nt][e] * sscale;
-      if (need_mask && key0 + nt * 8 + (e ? tB : tA) > lim) v = -INFINITY;
+      if (need_mask) {
+        // visible: lim - win < key <= lim (the causal limit, the window)
+        const int key = key0 + nt * 8 + (e ? tB : tA);
+        if (key > lim || key <= lim - win) v = -INFINITY;
+      }
       s[nt][e] = v;
     }
   // online softmax (base 2) of query row r
@@ -1099,7 +1109,7 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
   float rscale[2];
   load_q<kKind, kRows16>(p, rm.q0, g, wrow0, wrows, lane, qa, rscale);
   int lim[2];
-  int my_min = INT_MAX;
+  int my_min = INT_MAX, my_max = -1;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     const int rr = rq + 8 * half;
@@ -1107,12 +1117,17 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
     if (rr < wrows) {
       lim[half] = rm.L - rm.n + (wrow0 + rr) / G;
       my_min = min(my_min, lim[half]);
+      my_max = max(my_max, lim[half]);
     }
   }
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1)
+  for (int d = 1; d < 32; d <<= 1) {
     my_min = min(my_min, __shfl_xor_sync(~0u, my_min, d));
+    my_max = max(my_max, __shfl_xor_sync(~0u, my_max, d));
+  }
   const int min_lim = min(my_min, rm.L - 1);
+  // keys at or below this are outside some row's window
+  const int win_edge = my_max - p.window;
   const float ss0 = p.score_scale * rscale[0];
   const float ss1 = p.score_scale * rscale[1];
 
@@ -1142,10 +1157,11 @@ __device__ void consume_item(const FastParams& p, const Smem& sm,
     }
     const int key0 = (ig.page0 + j) * kBS;
     const int valid = min(kBS, rm.L - key0);
-    const bool need_mask = key0 + kBS - 1 > min_lim;
+    const bool need_mask = key0 + kBS - 1 > min_lim || key0 <= win_edge;
     const uint32_t kb = sm.base + Ly::kRing + slot * Tr::kStageBytes;
     process_page<kKind, kRows16>(kb, kb + Tr::kPageBytes, qa, st, key0, valid,
-                                 need_mask, lim[0], lim[1], ss0, ss1, lane);
+                                 need_mask, lim[0], lim[1], p.window, ss0, ss1,
+                                 lane);
     __syncwarp();
     if (lane == 0) mbar_arrive_cnt(sm.empty(slot), decode ? kConsumerWarps : 1);
   }
@@ -1253,10 +1269,15 @@ __device__ void consume_item_narrow(const FastParams& p, const Smem& sm,
   load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
   const int lim = rq < rows ? rm.L - rm.n + rq / G : rm.L - 1;
   int min_lim = rq < rows ? lim : INT_MAX;
+  int max_lim = rq < rows ? lim : -1;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1)
+  for (int d = 1; d < 32; d <<= 1) {
     min_lim = min(min_lim, __shfl_xor_sync(~0u, min_lim, d));
+    max_lim = max(max_lim, __shfl_xor_sync(~0u, max_lim, d));
+  }
   min_lim = min(min_lim, rm.L - 1);
+  // keys at or below this are outside some row's window
+  const int win_edge = max_lim - p.window;
   const float ss = p.score_scale * rscale[0];
 
   NarrowState st;
@@ -1282,10 +1303,10 @@ __device__ void consume_item_narrow(const FastParams& p, const Smem& sm,
     }
     const int key0 = (ig.page0 + j) * kBS;
     const int valid = min(kBS, rm.L - key0);
-    const bool need_mask = key0 + kBS - 1 > min_lim;
+    const bool need_mask = key0 + kBS - 1 > min_lim || key0 <= win_edge;
     const uint32_t kb = sm.base + Ly::kRing + slot * Tr::kStageBytes;
     process_page_narrow<kKind>(kb, kb + Tr::kPageBytes, qa, st, key0, valid,
-                               need_mask, lim, ss, lane);
+                               need_mask, lim, p.window, ss, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive_cnt(sm.empty(slot), kConsumerWarps);
   }
@@ -1877,10 +1898,15 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
   load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
   const int lim = rq < rows ? rm.L - rm.n + rq / G : rm.L - 1;
   int min_lim = rq < rows ? lim : INT_MAX;
+  int max_lim = rq < rows ? lim : -1;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1)
+  for (int d = 1; d < 32; d <<= 1) {
     min_lim = min(min_lim, __shfl_xor_sync(~0u, min_lim, d));
+    max_lim = max(max_lim, __shfl_xor_sync(~0u, max_lim, d));
+  }
   min_lim = min(min_lim, rm.L - 1);
+  // keys at or below this are outside some row's window
+  const int win_edge = max_lim - p.window;
   const float ss = p.score_scale * rscale[0];
 
   NarrowState st;
@@ -1901,10 +1927,10 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
     }
     const int key0 = (page0 + j) * kBS;
     const int valid = min(kBS, rm.L - key0);
-    const bool need_mask = key0 + kBS - 1 > min_lim;
+    const bool need_mask = key0 + kBS - 1 > min_lim || key0 <= win_edge;
     const uint32_t kb = ring + s * Ly::kStageBytes + warp * Ly::kPageBytes;
     process_page_narrow<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
-                               valid, need_mask, lim, ss, lane);
+                               valid, need_mask, lim, p.window, ss, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (S + s));
   }
@@ -2004,6 +2030,7 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
     uint32_t c = 0;  // stages issued
     int go = 1;
     int4 rec0, rec1;
+    const long long skip = skipped_copy();
     while (go && src.next(rec0, rec1)) {
       const int32_t* bt =
           p.block_tables + (int64_t)rec0.x * p.max_blocks_per_seq + rec1.x;
@@ -2040,7 +2067,7 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
               go = 0;
               break;
             }
-            if (mine) {
+            if (mine && (long long)cc != skip) {
               int blk = cur[jj + kk];
               if (blk < 0 || (int64_t)blk >= p.num_blocks) {
                 if (kv == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
@@ -2357,8 +2384,9 @@ bool fast_path_supported(const AttnArgs& a) {
 
 AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                    int head_dim, int num_seqs, int max_query_len,
-                   int max_seq_len, int num_sms) {
+                   int max_seq_len, int num_sms, int window) {
   AttnPlan pl{};
+  pl.window = window > 0 && window < max_seq_len ? window : 0;
   pl.group = num_q_heads / num_kv_heads;
   pl.has_prefill = (int64_t)max_query_len * pl.group > kDecodeMaxRows;
   pl.has_decode = pl.group <= kDecodeMaxRows;
@@ -2389,8 +2417,87 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
   if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * head_dim * 4);
   pl.off_ml = off;
   if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * 2 * 4);
+  // a request's keys through the window start in the block holding key
+  // L - n - window + 1: at most n + window - 1 + 15 keys from there
+  pl.off_win_sl = pl.off_win_bt = off;
+  if (pl.window > 0) {
+    pl.win_max_seq_len =
+        (int)std::min<int64_t>(max_seq_len, (int64_t)max_query_len + pl.window + 14);
+    pl.win_blocks = (pl.win_max_seq_len + kBS - 1) / kBS;
+    off = up(off + (size_t)num_seqs * 4);
+    pl.off_win_bt = off;
+    off = up(off + (size_t)num_seqs * pl.win_blocks * 4);
+  }
   pl.total_bytes = off;
   return pl;
+}
+
+namespace {
+
+struct WindowArgs {
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int64_t num_tokens;
+  int num_seqs, max_query_len, max_seq_len, max_blocks_per_seq, window;
+  int32_t* bt_out;
+  int32_t* sl_out;
+  int blocks_out;
+};
+
+// One warp per request.  A request whose metadata fails the checks gets a
+// key count of -1, which every kernel of the step then flags and skips.
+__global__ void __launch_bounds__(256) window_view_kernel(WindowArgs w) {
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= w.num_seqs) return;
+  const ReqMeta m = load_req(w.qsl, w.seq_lens, r, w.num_tokens, w.max_query_len,
+                             w.max_seq_len, w.max_blocks_per_seq);
+  if (!m.ok) {
+    if (lane == 0) w.sl_out[r] = -1;
+    return;
+  }
+  const int lo = m.L - m.n - w.window + 1;  // first query's first key
+  const int p0 = lo > 0 ? lo / kBS : 0;
+  const int Lw = m.L - p0 * kBS;
+  const int nbw = min((Lw + kBS - 1) / kBS, w.blocks_out);
+  if (lane == 0) w.sl_out[r] = Lw;
+  const int32_t* src = w.block_tables + (int64_t)r * w.max_blocks_per_seq + p0;
+  int32_t* dst = w.bt_out + (int64_t)r * w.blocks_out;
+  for (int k = lane; k < nbw; k += 32) dst[k] = __ldg(src + k);
+}
+
+}  // namespace
+
+cudaError_t set_pipeline_hooks_fast(uint64_t wait_limit_ns, long long skip_copy) {
+  cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns,
+                                     sizeof(wait_limit_ns));
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbol(g_skip_copy, &skip_copy, sizeof(skip_copy));
+  return e;
+}
+
+cudaError_t launch_window_view(const AttnArgs& a, const AttnPlan& plan,
+                               cudaStream_t stream) {
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  WindowArgs w{};
+  w.block_tables = a.block_tables;
+  w.seq_lens = a.seq_lens;
+  w.qsl = a.query_start_loc;
+  w.num_tokens = a.num_tokens;
+  w.num_seqs = a.num_seqs;
+  w.max_query_len = a.max_query_len;
+  w.max_seq_len = a.max_seq_len;
+  w.max_blocks_per_seq = a.max_blocks_per_seq;
+  w.window = plan.window;
+  w.bt_out = reinterpret_cast<int32_t*>(ws + plan.off_win_bt);
+  w.sl_out = reinterpret_cast<int32_t*>(ws + plan.off_win_sl);
+  w.blocks_out = plan.win_blocks;
+  const unsigned grid = (unsigned)((a.num_seqs + 7) / 8);
+  window_view_kernel<<<grid, 256, 0, stream>>>(w);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
@@ -2425,6 +2532,7 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.score_scale = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.0f);
   fp.out_scale = fp8 ? a.v_scale : 1.0f;
   fp.seg_heads = 1;
+  fp.window = a.window > 0 ? a.window : kNoWindow;
 
   PlanArgs pa{};
   pa.qsl = a.query_start_loc;

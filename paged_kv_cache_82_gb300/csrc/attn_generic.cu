@@ -5,7 +5,8 @@
 // Same definition as the fast path ("vLLM engine anatomy": paging through the
 // block table, Figure 2; GQA, Table 1; exact softmax attention computed
 // online, "Boundaries: FlashAttention ..."): query i of request r sees keys
-// 0 .. L - n + i, query head h reads KV head h / group.
+// 0 .. L - n + i (with a sliding window of W keys only L - n + i - W + 1 ..
+// L - n + i), query head h reads KV head h / group.
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -27,6 +28,7 @@ struct GenericParams {
   int num_q_heads, num_kv_heads, group;
   int max_query_len, max_seq_len;
   float scale, k_scale, v_scale;
+  int window;  // sliding window in keys (kNoWindow: none)
 };
 
 template <typename TC>
@@ -63,6 +65,7 @@ attn_generic_kernel(GenericParams p) {
   }
   const int i = (int)(t - rm.q0);
   const int lim = rm.L - rm.n + i;
+  const int first = max(0, lim - p.window + 1);  // keys first .. lim
   const int g = h / p.group;
   const TQ* qp = static_cast<const TQ*>(p.q) + row * kD;
   float qv[kPer];
@@ -72,7 +75,7 @@ attn_generic_kernel(GenericParams p) {
 #pragma unroll
   for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
   const int32_t* bt = p.block_tables + (int64_t)r * p.max_blocks_per_seq;
-  for (int j = 0; j <= lim; ++j) {
+  for (int j = first; j <= lim; ++j) {
     int blk = __ldg(bt + j / kBS);
     if (blk < 0 || (int64_t)blk >= p.num_blocks) {
       if (lane == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
@@ -139,6 +142,7 @@ cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream) {
   gp.scale = a.scale;
   gp.k_scale = fp8 ? a.k_scale : 1.0f;
   gp.v_scale = fp8 ? a.v_scale : 1.0f;
+  gp.window = a.window > 0 ? a.window : kNoWindow;
   switch (a.cache_dtype) {
     case PA_F32:
       return launch_t<float, float>(gp, a.head_dim, stream);

@@ -163,11 +163,13 @@ struct TcParams {
   int max_query_len, max_seq_len;
   int tokens_per_tile;   // 128 / group
   float score_scale;     // softmax scale * log2(e)
+  int window;            // sliding window in keys (kNoWindow: none)
 };
 
-// one tile, as every role of the CTA sees it
+// one tile, as every role of the CTA sees it: its keys are the pages
+// p0 .. p0 + pages - 1 of the request (p0 > 0 only with a sliding window)
 struct TcTile {
-  int r, g, q0, n, L, i0, ntok, pages, nc;
+  int r, g, q0, n, L, i0, ntok, p0, pages, nc;
   bool ok;
 };
 
@@ -208,8 +210,12 @@ __device__ __forceinline__ TcTile tc_tile(const TcParams& p, const int* pre,
   t.i0 = tt * p.tokens_per_tile;
   t.ntok = min(p.tokens_per_tile, m.n - t.i0);
   t.ok = m.ok && tt >= 0 && t.ntok > 0;
-  // keys up to the last token's limit L - n + i0 + ntok - 1
-  t.pages = t.ok ? (t.L - t.n + t.i0 + t.ntok - 1) / kBS + 1 : 0;
+  // keys up to the last token's limit L - n + i0 + ntok - 1, from the first
+  // token's first key inside the window (L - n + i0 - window + 1)
+  const int end = t.ok ? (t.L - t.n + t.i0 + t.ntok - 1) / kBS + 1 : 0;
+  const int lo = t.L - t.n + t.i0 - p.window + 1;
+  t.p0 = t.ok && lo > 0 ? lo / kBS : 0;
+  t.pages = end - t.p0;
   t.nc = (t.pages + kTcPages - 1) / kTcPages;
   return t;
 }
@@ -283,6 +289,7 @@ __device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTil
   slot[8] = t.pages;
   slot[9] = t.nc;
   slot[10] = t.ok ? 1 : 0;
+  slot[11] = t.p0;
 }
 
 // The k-th tile of a warp that does not draw tiles, from slot k % 2; the
@@ -305,6 +312,7 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
   t.pages = sl[8];
   t.nc = sl[9];
   t.ok = sl[10] != 0;
+  t.p0 = sl[11];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
   return li;
@@ -412,7 +420,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     int row = 0;
     const int pg = grp * 32 + lane;
     if (pg < t.pages) {
-      int blk = __ldg(p.block_tables + (int64_t)t.r * p.max_blocks_per_seq + pg);
+      int blk = __ldg(p.block_tables + (int64_t)t.r * p.max_blocks_per_seq + t.p0 + pg);
       if (blk < 0 || blk >= p.num_blocks) {
         flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
         blk = 0;
@@ -445,6 +453,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
     uint32_t u = 0, qt = 0;
     uint32_t used[kKStages] = {};  // loads issued into each stage
+    const long long skip = skipped_copy();
     bool go = true;
     for (int k = 0; go; ++k) {
       // draw the next tile (longest first: from the step-wide counter, else
@@ -505,6 +514,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           go = false;
           break;
         }
+        if ((long long)u == skip) continue;  // testing hook: never issued
         load_chunk(&tmap_k, base + TcLayout::kK + st * kTileBytes,
                    bars + 8 * (kKFull + st), np, row);
         ++used[st];
@@ -612,8 +622,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
-      const int last = (t.L - 1) / kBS;  // page holding the last key
-      const int tail = t.L % kBS;        // its keys (0: a full page)
+      const int last = (t.L - 1) / kBS - t.p0;  // tile page holding the last key
+      const int tail = t.L % kBS;               // its keys (0: a full page)
       bool go = true;
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
@@ -714,14 +724,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         tc_ld32(t_b + 32, sr[1]);
         tc_wait_ld_dep(sr);
         // partial row max of the raw scores (the scale is positive); keys
-        // past the row's limit (only in chunks that reach the diagonal)
-        // become -inf
-        const int vis = lim - c * kTcKeys - half * 64;  // columns 0 .. vis
+        // past the row's limit (only in chunks that reach the diagonal) and
+        // keys at or before lim - window (only in chunks that reach the
+        // window's edge) become -inf
+        const int vis = lim - t.p0 * kBS - c * kTcKeys - half * 64;  // columns .. vis
+        const int wlo = vis - p.window;                             // columns .. wlo out
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (__any_sync(~0u, vis < 63)) {
+        if (__any_sync(~0u, vis < 63 || wlo >= 0)) {
 #pragma unroll
           for (int j = 0; j < 64; ++j)
-            if (j > vis) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
+            if (j > vis || j <= wlo) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
         for (int j = 0; j < 64; j += 2)
@@ -767,7 +779,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // 16k+8 .. 16k+15 (lo parts), key pairs packed low key first
         // (key pairs in packed fp32x2 arithmetic)
         const float2 scale2 = make_float2(p.score_scale, p.score_scale);
-        const float2 neg_m2 = make_float2(-m_ref, -m_ref);
+        // a row that has seen no key yet (a chunk wholly before its window)
+        // keeps m_ref = -inf: its scores are all -inf and give P = 0
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        const float2 neg_m2 = make_float2(-m_use, -m_use);
         float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -844,6 +859,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
 
 template <bool kBF16>
 cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
+                      cudaStream_t stream);
+
+}  // namespace
+
+cudaError_t set_pipeline_hooks_tc(uint64_t wait_limit_ns, long long skip_copy) {
+  cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_ns, &wait_limit_ns,
+                                     sizeof(wait_limit_ns));
+  if (e == cudaSuccess)
+    e = cudaMemcpyToSymbol(g_skip_copy, &skip_copy, sizeof(skip_copy));
+  return e;
+}
+
+namespace {
+
+template <bool kBF16>
+cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
                       cudaStream_t stream) {
   static bool configured[64] = {false};
   int dev = 0;
@@ -913,6 +944,7 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
   p.max_seq_len = a.max_seq_len;
   p.tokens_per_tile = kTcRows / p.group;
   p.score_scale = a.scale * 1.4426950408889634f;
+  p.window = a.window > 0 ? a.window : kNoWindow;
   int grid = max_atoms < num_sms ? max_atoms : num_sms;
   if (grid < 1) grid = 1;
   return a.cache_dtype == PA_BF16 ? launch_tc<true>(p, maps, grid, stream)

@@ -102,6 +102,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// the values last given to pa_set_wait_limit_ns / pa_test_skip_copy (both
+// are written together into every pipelined translation unit)
+std::mutex g_hooks_mutex;
+uint64_t g_hook_wait_ns = kWaitLimitNs;
+long long g_hook_skip = -1;
+
 thread_local ProfileEvents t_profile;
 thread_local uint64_t t_launches = 0;
 
@@ -286,35 +292,41 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype cache_dtype,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status pa_attention_workspace_size(int64_t num_tokens, int num_q_heads,
-                                      int num_kv_heads, int head_dim,
-                                      int num_seqs, int max_query_len,
-                                      int max_seq_len, size_t* bytes) {
+}  // extern "C"
+
+namespace {
+
+pa_status workspace_size_impl(int64_t num_tokens, int num_q_heads,
+                              int num_kv_heads, int head_dim, int num_seqs,
+                              int max_query_len, int max_seq_len, int window,
+                              size_t* bytes) {
   if (!bytes) return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-      num_q_heads % num_kv_heads != 0 || max_query_len < 0 || max_seq_len < 0)
+      num_q_heads % num_kv_heads != 0 || max_query_len < 0 || max_seq_len < 0 ||
+      window < 0)
     return PA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   const DeviceInfo* di = device_info();
   if (!di) return PA_ERR_CUDA;
   const AttnPlan pl = make_plan(num_tokens, num_q_heads, num_kv_heads, head_dim,
                                 num_seqs, max_query_len, max_seq_len,
-                                di->num_sms);
+                                di->num_sms, window);
   *bytes = pl.total_bytes;
   return PA_OK;
 }
 
-pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
-                       const void* v_cache, pa_dtype cache_dtype,
-                       int64_t num_blocks, int block_size, int num_q_heads,
-                       int num_kv_heads, int head_dim,
-                       const int32_t* block_tables, int max_blocks_per_seq,
-                       const int32_t* seq_lens,
-                       const int32_t* query_start_loc, int num_seqs,
-                       int64_t num_tokens, int max_query_len, int max_seq_len,
-                       float scale, float k_scale, float v_scale, void* out,
-                       void* workspace, size_t workspace_bytes,
-                       pa_stream_t stream) {
+pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
+                         const void* v_cache, pa_dtype cache_dtype,
+                         int64_t num_blocks, int block_size, int num_q_heads,
+                         int num_kv_heads, int head_dim,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* seq_lens,
+                         const int32_t* query_start_loc, int num_seqs,
+                         int64_t num_tokens, int max_query_len, int max_seq_len,
+                         float scale, float k_scale, float v_scale, int window,
+                         void* out, void* workspace, size_t workspace_bytes,
+                         pa_stream_t stream) {
+  if (window < 0) return PA_ERR_INVALID_ARG;
   if (!valid_dtype(q_dtype) || !valid_dtype(cache_dtype))
     return PA_ERR_INVALID_ARG;
   if (pa_status st = cache_shape_status(num_blocks, block_size, num_kv_heads,
@@ -351,7 +363,7 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
   if (!di) return PA_ERR_CUDA;
   const AttnPlan plan = make_plan(num_tokens, num_q_heads, num_kv_heads,
                                   head_dim, num_seqs, max_query_len,
-                                  max_seq_len, di->num_sms);
+                                  max_seq_len, di->num_sms, window);
   AttnArgs a{};
   a.q = q;
   a.q_dtype = q_dtype;
@@ -376,6 +388,7 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
   a.out = out;
   a.workspace = workspace;
   a.err = di->err;
+  a.window = plan.window;
   const bool fast = fast_path_supported(a);
   if (fast) {
     if (workspace_bytes < plan.total_bytes) return PA_ERR_INVALID_ARG;
@@ -389,6 +402,17 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
     return PA_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (fast && plan.window > 0) {
+    // the kernels of the step see each request through the window: its
+    // blocks from the one holding its first visible key (workspace)
+    e = launch_window_view(a, plan, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.block_tables = reinterpret_cast<const int32_t*>(ws + plan.off_win_bt);
+    a.seq_lens = reinterpret_cast<const int32_t*>(ws + plan.off_win_sl);
+    a.max_blocks_per_seq = plan.win_blocks;
+    a.max_seq_len = plan.win_max_seq_len;
+  }
   if (fast) {
     // prefill tiles go to the tensor-core kernel where it takes the step's
     // types (else the attention kernel runs them on the warp-level MMA)
@@ -404,6 +428,88 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
     e = launch_attention_generic(a, s);
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_attention_workspace_size(int64_t num_tokens, int num_q_heads,
+                                      int num_kv_heads, int head_dim,
+                                      int num_seqs, int max_query_len,
+                                      int max_seq_len, size_t* bytes) {
+  return workspace_size_impl(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                             num_seqs, max_query_len, max_seq_len, 0, bytes);
+}
+
+pa_status pa_attention_window_workspace_size(int64_t num_tokens,
+                                             int num_q_heads, int num_kv_heads,
+                                             int head_dim, int num_seqs,
+                                             int max_query_len, int max_seq_len,
+                                             int sliding_window, size_t* bytes) {
+  return workspace_size_impl(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                             num_seqs, max_query_len, max_seq_len,
+                             sliding_window, bytes);
+}
+
+pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
+                       const void* v_cache, pa_dtype cache_dtype,
+                       int64_t num_blocks, int block_size, int num_q_heads,
+                       int num_kv_heads, int head_dim,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* seq_lens,
+                       const int32_t* query_start_loc, int num_seqs,
+                       int64_t num_tokens, int max_query_len, int max_seq_len,
+                       float scale, float k_scale, float v_scale, void* out,
+                       void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
+  return attention_impl(q, q_dtype, k_cache, v_cache, cache_dtype, num_blocks,
+                        block_size, num_q_heads, num_kv_heads, head_dim,
+                        block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_tokens, max_query_len,
+                        max_seq_len, scale, k_scale, v_scale, 0, out, workspace,
+                        workspace_bytes, stream);
+}
+
+pa_status pa_attention_window(const void* q, pa_dtype q_dtype,
+                              const void* k_cache, const void* v_cache,
+                              pa_dtype cache_dtype, int64_t num_blocks,
+                              int block_size, int num_q_heads, int num_kv_heads,
+                              int head_dim, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int num_seqs,
+                              int64_t num_tokens, int max_query_len,
+                              int max_seq_len, float scale, float k_scale,
+                              float v_scale, int sliding_window, void* out,
+                              void* workspace, size_t workspace_bytes,
+                              pa_stream_t stream) {
+  return attention_impl(q, q_dtype, k_cache, v_cache, cache_dtype, num_blocks,
+                        block_size, num_q_heads, num_kv_heads, head_dim,
+                        block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_tokens, max_query_len,
+                        max_seq_len, scale, k_scale, v_scale, sliding_window,
+                        out, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) ns = kWaitLimitNs;
+  if (ns < 100000ull || ns > 60000000000ull) return PA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_hooks_mutex);
+  if (set_pipeline_hooks_fast(ns, g_hook_skip) != cudaSuccess ||
+      set_pipeline_hooks_tc(ns, g_hook_skip) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_hook_wait_ns = ns;
+  return PA_OK;
+}
+
+pa_status pa_test_skip_copy(int64_t stage) {
+  if (stage < -1) return PA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_hooks_mutex);
+  if (set_pipeline_hooks_fast(g_hook_wait_ns, stage) != cudaSuccess ||
+      set_pipeline_hooks_tc(g_hook_wait_ns, stage) != cudaSuccess)
+    return PA_ERR_CUDA;
+  g_hook_skip = stage;
+  return PA_OK;
 }
 
 pa_status pa_set_debug_bounds(int enable) {

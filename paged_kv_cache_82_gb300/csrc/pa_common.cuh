@@ -132,19 +132,34 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait: gives up after ~kWaitLimitNs of wall time.  A pipeline whose
-// wait gives up records PA_DEV_ERR_TIMEOUT and unwinds; it never spins
-// forever.
+// Bounded wait: gives up after g_wait_limit_ns of wall time (2 s unless
+// pa_set_wait_limit_ns says otherwise).  A pipeline whose wait gives up
+// records PA_DEV_ERR_TIMEOUT and unwinds; it never spins forever.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Per translation unit (static), per device; written by the unit's
+// set_pipeline_hooks() on the host.
+//  g_wait_limit_ns -- the longest one bounded wait spins, in ns;
+//  g_skip_copy     -- testing hook: the pipeline stage whose copy CTA 0 of
+//                     the unit's pipelined kernels never issues (-1: none),
+//                     so that the waits on that stage can only run out.
+static __device__ uint64_t g_wait_limit_ns = kWaitLimitNs;
+static __device__ long long g_skip_copy = -1;
 
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar,
                                                   uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = g_wait_limit_ns;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > limit) return false;
   }
+}
+
+// The stage CTA 0 of this grid leaves out (testing hook), -1 elsewhere.
+__device__ __forceinline__ long long skipped_copy() {
+  return blockIdx.x == 0 ? g_skip_copy : -1;
 }
 
 // ----------------------------------------------------------------------------

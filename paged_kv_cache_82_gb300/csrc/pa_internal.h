@@ -14,6 +14,12 @@ namespace pa {
 // launch site calls count_launch() once its launch has been accepted.
 void count_launch();
 
+// Bounded-wait limit and the skipped-copy testing hook of the pipelined
+// kernels, for the current device: attn_fast.cu and attn_prefill_tc.cu each
+// hold their own copy (cudaMemcpyToSymbol, synchronous).
+cudaError_t set_pipeline_hooks_fast(uint64_t wait_limit_ns, long long skip_copy);
+cudaError_t set_pipeline_hooks_tc(uint64_t wait_limit_ns, long long skip_copy);
+
 // ---- cache kernels (cache_kernels.cu) --------------------------------------
 cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      pa_dtype kv_dtype, int64_t num_tokens,
@@ -47,6 +53,10 @@ constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
 #endif
 constexpr int kMaxCtasPerSm = PA_CTAS_PER_SM;  // grid bound of the attention kernels
 
+// "No sliding window" inside the kernels: a row with causal limit lim sees
+// keys lim - window + 1 .. lim, so a window this wide never cuts.
+constexpr int kNoWindow = 1 << 30;
+
 // Rows of one split-K partial slot (a head group's 4 KV heads x 8 rows) and
 // the partial-result bytes make_plan reserves per SM whatever the step's
 // size: two slots per resident attention CTA, each rows x head_dim 128 fp32
@@ -67,13 +77,20 @@ struct AttnPlan {
   size_t off_atoms, off_atom_start, off_req_dec0, off_req_declen, off_req_rows,
       off_items,
       off_cta_begin, off_seg_info, off_split, off_pref, off_acc, off_ml,
-      total_bytes;
+      off_win_sl, off_win_bt, total_bytes;
+  // sliding window (0: none): each request's view from the block holding its
+  // first query's first key in the window -- block-table rows of win_blocks
+  // entries and key counts of at most win_max_seq_len
+  int window, win_blocks, win_max_seq_len;
 };
 
 // Host planning from host-known sizes only (no device read-back).
+// window: the sliding window in keys (0: none; a window of at least
+// max_seq_len keys cuts nothing and counts as none).
 AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                    int head_dim, int num_seqs, int max_query_len,
-                   int max_seq_len, int num_sms);
+                   int max_seq_len, int num_sms, int window = 0);
+
 
 struct AttnArgs {
   const void* q;
@@ -94,10 +111,18 @@ struct AttnArgs {
   void* out;
   void* workspace;
   unsigned* err;
+  int window;  // sliding window in keys (0: none)
 };
 
 // true if the TMA + tensor-core kernel covers these types / shapes
 bool fast_path_supported(const AttnArgs& a);
+
+// The step's view through a sliding window (plan.window > 0): for every
+// request, its block-table row from the block that holds its first query's
+// first key inside the window, and its key count from that block on, into
+// the workspace at plan.off_win_bt / off_win_sl.
+cudaError_t launch_window_view(const AttnArgs& a, const AttnPlan& plan,
+                               cudaStream_t stream);
 
 // events recorded around the main attention launch (measurement hook)
 struct ProfileEvents {

@@ -37,12 +37,17 @@ def gpu_step(wl, device="cuda", out=None, workspace=None):
             torch.from_numpy(md["slot_mapping"]).to(device),
             k_scale=wl.k_scale, v_scale=wl.v_scale, cache_dtype=cdt)
     q = wl.q.to(device)
-    res = pa.pa_attention(
-        q, kc, vc, torch.from_numpy(md["block_tables"]).to(device),
-        torch.from_numpy(md["seq_lens"]).to(device),
-        torch.from_numpy(md["query_start_loc"]).to(device),
-        md["max_query_len"], md["max_seq_len"], wl.scale, wl.k_scale,
-        wl.v_scale, out=out, workspace=workspace, cache_dtype=cdt)
+    meta = (torch.from_numpy(md["block_tables"]).to(device),
+            torch.from_numpy(md["seq_lens"]).to(device),
+            torch.from_numpy(md["query_start_loc"]).to(device),
+            md["max_query_len"], md["max_seq_len"], wl.scale)
+    if wl.sliding_window:
+        res = pa.pa_attention_window(
+            q, kc, vc, *meta, wl.sliding_window, wl.k_scale, wl.v_scale,
+            out=out, workspace=workspace, cache_dtype=cdt)
+    else:
+        res = pa.pa_attention(q, kc, vc, *meta, wl.k_scale, wl.v_scale,
+                              out=out, workspace=workspace, cache_dtype=cdt)
     flags = pa.pa_get_device_error()
     return res, kc, vc, md, flags
 

@@ -75,6 +75,7 @@ class Workload:
     block_size: int = BLOCK_SIZE
     shared_blocks: List[int] = field(default_factory=list)
     description: str = ""
+    sliding_window: int = 0  # keys a query sees through a window (0: all)
 
     @property
     def num_tokens(self) -> int:
