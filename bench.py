@@ -431,8 +431,14 @@ def run_ours(args):
         make = {"decode": workloads.config2, "mixed": workloads.config4,
                 "prefill": workloads.prefill_chunk, "mha": workloads.config3,
                 "fp8long": workloads.config5}[args.only]
-        # a smaller batch of the same decode shape (profiler captures)
-        wl = make(batch=args.batch) if args.batch else make()
+        # a smaller batch of the same shape (profiler captures); the mixed
+        # step keeps its shared prefix and chunk, with fewer decodes and a
+        # pool sized to them
+        if args.batch and args.only == "mixed":
+            wl = make(num_decodes=args.batch,
+                      num_blocks=200 + args.batch * 520 + 64)
+        else:
+            wl = make(batch=args.batch) if args.batch else make()
         d = _device_inputs(wl, dev)
         step_ms, kern_ms, _ = _time_steps(pa, wl, d, args.steps, args.warmup,
                                           flush)
@@ -671,8 +677,8 @@ def main():
                     help="profiling runs: time just one step kind, no JSON "
                          "line")
     ap.add_argument("--batch", type=int, default=0,
-                    help="with --only decode/mha/fp8long: that many requests "
-                         "instead of the workload's own batch")
+                    help="with --only decode/mha/fp8long/mixed: that many "
+                         "(decode) requests instead of the workload's own")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
