@@ -35,8 +35,9 @@ _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 # element type codes of pa_oracle.c
-F32, F16, BF16, E4M3 = 0, 1, 2, 3
-_DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3}
+F32, F16, BF16, E4M3, INT4, NVFP4 = 0, 1, 2, 3, 4, 5
+_DT_NAMES = {"f32": F32, "f16": F16, "bf16": BF16, "e4m3": E4M3,
+             "int4": INT4, "nvfp4": NVFP4}
 _ELEM_BYTES = {F32: 4, F16: 2, BF16: 2, E4M3: 1}
 
 _lock = threading.Lock()
@@ -70,6 +71,12 @@ def _bind(lib):
     lib.orc_e4m3_to_double.restype = f64
     lib.orc_e4m3_encode.argtypes = [f32]
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
+    lib.orc_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_to_double.restype = f64
+    lib.orc_e2m1_encode.argtypes = [f32]
+    lib.orc_e2m1_encode.restype = ctypes.c_uint8
+    lib.orc_int4_encode.argtypes = [f32]
+    lib.orc_int4_encode.restype = i32
     lib.orc_reshape_and_cache.argtypes = [P, P, i32, i64, i64, i64, P, P,
                                           i32, i64, i32, i32, i32, P, f32,
                                           f32]
@@ -186,6 +193,41 @@ def e4m3_encode(y: float) -> int:
     return int(_load().orc_e4m3_encode(float(np.float32(y))))
 
 
+def e2m1_to_double(code: int) -> float:
+    return _load().orc_e2m1_to_double(code & 0xF)
+
+
+def e2m1_encode(y: float) -> int:
+    """E2M1 code nearest to the fp32 value y (ties to even, saturating)."""
+    return int(_load().orc_e2m1_encode(float(np.float32(y))))
+
+
+def int4_encode(y: float) -> int:
+    """Nearest integer to the fp32 value y (ties to even) in [-7, 7]."""
+    return int(_load().orc_int4_encode(float(np.float32(y))))
+
+
+def page_bytes_4bit(cache_dtype, head_dim: int, block_size: int = 16) -> int:
+    """Bytes of one (block, KV head) page of a 4-bit cache: the codes, then
+    one fp32 scale per token (int4) or one E4M3 scale per 16 elements
+    (nvfp4)."""
+    codes = block_size * head_dim // 2
+    dt = _dt(cache_dtype, None)
+    return codes + (4 * block_size if dt == INT4 else
+                    block_size * head_dim // 16)
+
+
+def _geometry(cache, head_dim=None, block_size=16):
+    """(num_blocks, kv_heads, block_size, head_dim) of a cache array:
+    [NB, Hkv, bs, D] elements, or [NB, Hkv, page_bytes] for the 4-bit
+    formats (head_dim given)."""
+    if cache.ndim == 4:
+        return cache.shape
+    if head_dim is None:
+        raise OracleError("a 4-bit cache needs head_dim")
+    return cache.shape[0], cache.shape[1], block_size, head_dim
+
+
 def kv_bytes_per_token(elem_bytes: int, layers: int, kv_heads: int,
                        head_dim: int) -> int:
     """Table 1 of "vLLM engine anatomy": 2 x elem bytes x layers x KV heads x
@@ -256,17 +298,18 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, *,
     cdt = _dt(cache_dtype, None)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     T = sm.shape[0]
-    NB, Hkv, bs, D = k_cache.shape
+    NB, Hkv, bs, D = _geometry(k_cache, k.shape[-1], block_size)
     _check(_load().orc_reshape_and_cache(
         _ptr(k), _ptr(v), kdt, T, Hkv * D, Hkv * D, _ptr(k_cache),
         _ptr(v_cache), cdt, NB, bs, Hkv, D, _ptr(sm), k_scale, v_scale),
         "reshape_and_cache")
 
 
-def copy_blocks(k_cache, v_cache, block_mapping, *, cache_dtype):
+def copy_blocks(k_cache, v_cache, block_mapping, *, cache_dtype,
+                head_dim=None):
     """In-place block copies; block_mapping int64 [P, 2] of (src, dst)."""
     bm = np.ascontiguousarray(block_mapping, dtype=np.int64).reshape(-1, 2)
-    NB, Hkv, bs, D = k_cache.shape
+    NB, Hkv, bs, D = _geometry(k_cache, head_dim)
     _check(_load().orc_copy_blocks(
         _ptr(k_cache), _ptr(v_cache), _dt(cache_dtype, None), NB, bs, Hkv, D,
         _ptr(bm), bm.shape[0]), "copy_blocks")
@@ -284,7 +327,7 @@ def paged_attention(q, k_cache, v_cache, block_tables, seq_lens,
     qdt = _dt(q_dtype, qdt)
     cdt = _dt(cache_dtype, kcdt)
     T, Hq, D = qa.shape
-    NB, Hkv, bs, _ = kc.shape
+    NB, Hkv, bs, _ = _geometry(kc, D)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
@@ -310,7 +353,7 @@ def paged_attention_row(q, k_cache, v_cache, block_tables, seq_lens,
     qdt = _dt(q_dtype, qdt)
     cdt = _dt(cache_dtype, kcdt)
     T, Hq, D = qa.shape
-    NB, Hkv, bs, _ = kc.shape
+    NB, Hkv, bs, _ = _geometry(kc, D)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
@@ -336,7 +379,7 @@ def run_step(wl, num_threads=None):
     cdt = _DT_NAMES[wl.cache_dtype]
     if wl.copy_pairs:
         copy_blocks(kc, vc, np.asarray(wl.copy_pairs, dtype=np.int64),
-                    cache_dtype=cdt)
+                    cache_dtype=cdt, head_dim=wl.head_dim)
     if wl.write_new:
         reshape_and_cache(wl.key, wl.value, kc, vc, md["slot_mapping"],
                           cache_dtype=cdt, k_scale=wl.k_scale,

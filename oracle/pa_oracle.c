@@ -34,6 +34,21 @@
  *    --kv-cache-dtype fp8 stores KV in 1-byte FP8.  The E4M3 "FN" format
  *    (bias 7, no infinities, S.1111.111 = NaN, max 448) is taken from the
  *    OCP 8-bit floating point specification.
+ *  - same table: lower-bit KV formats, nvfp4 and int4_per_token_head, whose
+ *    accuracy is left to the user to evaluate.  NVFP4 is NVIDIA's published
+ *    4-bit format: FP4 E2M1 elements (the OCP Microscaling specification's
+ *    E2M1: 1 sign, 2 exponent bits with bias 1, 1 mantissa bit; values 0,
+ *    0.5, 1, 1.5, 2, 3, 4, 6; no infinities or NaN), one E4M3 scale per 16
+ *    consecutive elements and one fp32 scale per tensor.  int4_per_token_head
+ *    is read here as signed 4-bit integers with one fp32 scale per (token,
+ *    KV head), chosen at write time as max |x| / 7.
+ *
+ *  Page layout of the 4-bit formats (one page = one (block, KV head); block
+ *  size bs, head dim D): bs * D / 2 bytes of codes, token by token, element
+ *  2i in the low nibble of byte i of its token; then the scales: bs fp32
+ *  (INT4, one per token) or bs * D / 16 E4M3 bytes (NVFP4, token by token,
+ *  one per 16 elements).  Value: INT4 scale * code (two's complement);
+ *  NVFP4 tensor_scale * e4m3(block scale) * e2m1(code).
  *
  * Everything is computed in double from the stored bytes; no blocking,
  * fusion or reordering beyond the definitions.
@@ -46,7 +61,16 @@
 
 /* element type codes (same numbering as the product header, written out
  * independently here) */
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3, ORC_INT4 = 4,
+       ORC_NVFP4 = 5 };
+
+static int is_4bit(int dt) { return dt == ORC_INT4 || dt == ORC_NVFP4; }
+
+/* bytes of one (block, KV head) page of a 4-bit cache */
+static int64_t page_bytes_4bit(int dt, int bs, int D) {
+  const int64_t codes = (int64_t)bs * (D / 2);
+  return dt == ORC_INT4 ? codes + 4 * (int64_t)bs : codes + (int64_t)bs * (D / 16);
+}
 
 enum { ORC_OK = 0, ORC_BAD_ARG = 1, ORC_BAD_INDEX = 2 };
 
@@ -106,6 +130,14 @@ double orc_e4m3_to_double(uint8_t c) {
   } else {
     v = ldexp(1.0 + (double)m / 8.0, e - 7);
   }
+  return sign ? -v : v;
+}
+
+/* E2M1 (OCP Microscaling): sign bit 3, exponent bits 2-1 (bias 1),
+ * mantissa bit 0; exponent 0 is subnormal (m * 0.5). */
+double orc_e2m1_to_double(uint8_t c) {
+  const int sign = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
   return sign ? -v : v;
 }
 
@@ -170,6 +202,96 @@ static float div_f32(float x, float scale) {
   return q;
 }
 
+/* E2M1 code nearest to y, by exhaustive search over the 8 magnitudes; a
+ * tie goes to the code whose mantissa bit is 0; |y| beyond 6 saturates to
+ * 6; the sign bit follows y's sign (so -0 -> 0x8). */
+uint8_t orc_e2m1_encode(float y) {
+  uint8_t sign = signbit(y) ? 0x8 : 0x0;
+  double a = fabs((double)y);
+  if (a >= 6.0) return (uint8_t)(sign | 0x7);
+  int best = 0;
+  double best_err = INFINITY;
+  for (int c = 0; c <= 7; ++c) {
+    double err = fabs(a - orc_e2m1_to_double((uint8_t)c));
+    if (err < best_err || (err == best_err && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      best_err = err;
+    }
+  }
+  return (uint8_t)(sign | best);
+}
+
+/* INT4 code of y: the integer nearest to y (ties to even), clamped to
+ * [-7, 7]. */
+int orc_int4_encode(float y) {
+  double r = rint((double)y); /* the default rounding mode: ties to even */
+  if (r > 7.0) r = 7.0;
+  if (r < -7.0) r = -7.0;
+  return (int)r;
+}
+
+/* Quantise the D values of one (token, KV head), src[0 .. D) of type
+ * src_dt, into slot o of a 4-bit page (layout above).  INT4: s = fl32(max |x|
+ * / 7), code = int4(fl32(x / s)) (all codes 0 when s = 0).  NVFP4, per block
+ * of 16: b = e4m3(fl32(fl32(max |x| / 6) / tensor_scale)), then with
+ * r = fl32(e4m3 value of b * tensor_scale) code = e2m1(fl32(x / r)) (all
+ * codes 0 when r = 0). */
+static void quantize_4bit(const void* src, int64_t src0, int src_dt,
+                          uint8_t* page, int o, int bs, int D, int dt,
+                          float tensor_scale) {
+  uint8_t* codes = page + (int64_t)o * (D / 2);
+  for (int i = 0; i < D / 2; ++i) codes[i] = 0;
+  if (dt == ORC_INT4) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+      float x = fabsf(load_elem_f32(src, src0 + d, src_dt));
+      if (x > amax) amax = x;
+    }
+    float sc = amax > 0.0f ? div_f32(amax, 7.0f) : 0.0f;
+    memcpy(page + (int64_t)bs * (D / 2) + 4 * (int64_t)o, &sc, 4);
+    for (int d = 0; d < D; ++d) {
+      int c = sc > 0.0f ? orc_int4_encode(div_f32(load_elem_f32(src, src0 + d, src_dt), sc)) : 0;
+      codes[d / 2] |= (uint8_t)((c & 0xF) << (4 * (d & 1)));
+    }
+    return;
+  }
+  uint8_t* scales = page + (int64_t)bs * (D / 2) + (int64_t)o * (D / 16);
+  for (int blk = 0; blk < D / 16; ++blk) {
+    float amax = 0.0f;
+    for (int d = 16 * blk; d < 16 * blk + 16; ++d) {
+      float x = fabsf(load_elem_f32(src, src0 + d, src_dt));
+      if (x > amax) amax = x;
+    }
+    uint8_t b = orc_e4m3_encode(div_f32(div_f32(amax, 6.0f), tensor_scale));
+    scales[blk] = b;
+    float r = (float)(orc_e4m3_to_double(b) * (double)tensor_scale);
+    for (int d = 16 * blk; d < 16 * blk + 16; ++d) {
+      uint8_t c = r > 0.0f ? orc_e2m1_encode(div_f32(load_elem_f32(src, src0 + d, src_dt), r)) : 0;
+      codes[d / 2] |= (uint8_t)(c << (4 * (d & 1)));
+    }
+  }
+}
+
+/* Value of element i of a cache indexed as [block][head][offset][d] (i =
+ * ((block * heads + head) * bs + offset) * D + d), decoded exactly; for the
+ * 4-bit formats the element is found in its (block, head) page, and the
+ * per-tensor scale is left to the caller. */
+static double load_kv(const void* cache, int64_t i, int dt, int bs, int D) {
+  if (!is_4bit(dt)) return load_elem(cache, i, dt);
+  const int64_t page = i / ((int64_t)bs * D);
+  const int o = (int)((i / D) % bs), d = (int)(i % D);
+  const uint8_t* pg = (const uint8_t*)cache + page * page_bytes_4bit(dt, bs, D);
+  const uint8_t byte = pg[(int64_t)o * (D / 2) + d / 2];
+  const int nib = (d & 1) ? (byte >> 4) : (byte & 0xF);
+  if (dt == ORC_INT4) {
+    float sc;
+    memcpy(&sc, pg + (int64_t)bs * (D / 2) + 4 * (int64_t)o, 4);
+    return (double)sc * (double)(nib >= 8 ? nib - 16 : nib);
+  }
+  const uint8_t b = pg[(int64_t)bs * (D / 2) + (int64_t)o * (D / 16) + d / 16];
+  return orc_e4m3_to_double(b) * orc_e2m1_to_double((uint8_t)nib);
+}
+
 /* ---------------------------------------------------------------------- */
 /* reshape_and_cache: write each new token's K and V into its slot.        */
 /* Cache layout [num_blocks][num_kv_heads][block_size][head_dim]; slot s   */
@@ -184,15 +306,29 @@ int orc_reshape_and_cache(const void* key, const void* value, int kv_dtype,
                           const int64_t* slot_mapping, float k_scale,
                           float v_scale) {
   int eb = elem_bytes(cache_dtype);
-  if (eb == 0 || elem_bytes(kv_dtype) == 0 || kv_dtype == ORC_E4M3)
+  if ((eb == 0 && !is_4bit(cache_dtype)) || elem_bytes(kv_dtype) == 0 ||
+      kv_dtype == ORC_E4M3)
     return ORC_BAD_ARG;
-  if (cache_dtype != kv_dtype && cache_dtype != ORC_E4M3) return ORC_BAD_ARG;
+  if (cache_dtype != kv_dtype && cache_dtype != ORC_E4M3 && !is_4bit(cache_dtype))
+    return ORC_BAD_ARG;
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
     if (slot < 0) continue;
     int64_t b = slot / block_size;
     int64_t o = slot % block_size;
     if (b >= num_blocks) return ORC_BAD_INDEX;
+    if (is_4bit(cache_dtype)) {
+      const int64_t pb = page_bytes_4bit(cache_dtype, block_size, head_dim);
+      for (int h = 0; h < num_kv_heads; ++h) {
+        uint8_t* kp = (uint8_t*)k_cache + (b * num_kv_heads + h) * pb;
+        uint8_t* vp = (uint8_t*)v_cache + (b * num_kv_heads + h) * pb;
+        quantize_4bit(key, t * key_stride + (int64_t)h * head_dim, kv_dtype, kp,
+                      (int)o, block_size, head_dim, cache_dtype, k_scale);
+        quantize_4bit(value, t * value_stride + (int64_t)h * head_dim, kv_dtype,
+                      vp, (int)o, block_size, head_dim, cache_dtype, v_scale);
+      }
+      continue;
+    }
     for (int h = 0; h < num_kv_heads; ++h) {
       for (int d = 0; d < head_dim; ++d) {
         int64_t src_k = t * key_stride + (int64_t)h * head_dim + d;
@@ -223,8 +359,11 @@ int orc_copy_blocks(void* k_cache, void* v_cache, int cache_dtype,
                     int head_dim, const int64_t* block_mapping,
                     int64_t num_pairs) {
   int eb = elem_bytes(cache_dtype);
-  if (eb == 0) return ORC_BAD_ARG;
-  int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * eb;
+  if (eb == 0 && !is_4bit(cache_dtype)) return ORC_BAD_ARG;
+  int64_t block_bytes =
+      is_4bit(cache_dtype)
+          ? num_kv_heads * page_bytes_4bit(cache_dtype, block_size, head_dim)
+          : (int64_t)num_kv_heads * block_size * head_dim * eb;
   for (int64_t p = 0; p < num_pairs; ++p) {
     int64_t src = block_mapping[2 * p], dst = block_mapping[2 * p + 1];
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
@@ -319,8 +458,8 @@ static int attend_one(attn_job* J, int r, int h) {
       int64_t base = (((int64_t)b * J->num_kv_heads + g) * bs + j % bs) * D;
       double dot = 0.0;
       for (int d = 0; d < D; ++d)
-        dot += qv[d] * (J->k_scale * load_elem(J->k_cache, base + d,
-                                               J->cache_dtype));
+        dot += qv[d] * (J->k_scale * load_kv(J->k_cache, base + d,
+                                             J->cache_dtype, bs, D));
       s[j] = J->scale * dot;
       if (s[j] > smax) smax = s[j];
     }
@@ -336,7 +475,7 @@ static int attend_one(attn_job* J, int r, int h) {
       int64_t base = (((int64_t)b * J->num_kv_heads + g) * bs + j % bs) * D;
       for (int d = 0; d < D; ++d)
         o[d] += s[j] * (J->v_scale *
-                        load_elem(J->v_cache, base + d, J->cache_dtype));
+                        load_kv(J->v_cache, base + d, J->cache_dtype, bs, D));
     }
     for (int d = 0; d < D; ++d) o[d] /= denom;
   }
@@ -378,7 +517,8 @@ int orc_paged_attention(const void* q, int q_dtype, const void* k_cache,
                         double* out, int num_threads, int window) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
       block_size <= 0 || elem_bytes(q_dtype) == 0 ||
-      elem_bytes(cache_dtype) == 0 || window < 0)
+      (elem_bytes(cache_dtype) == 0 && !is_4bit(cache_dtype)) ||
+      (is_4bit(cache_dtype) && head_dim % 16 != 0) || window < 0)
     return ORC_BAD_ARG;
   attn_job J;
   memset(&J, 0, sizeof J);
@@ -398,8 +538,8 @@ int orc_paged_attention(const void* q, int q_dtype, const void* k_cache,
   J.query_start_loc = query_start_loc;
   J.num_seqs = num_seqs;
   J.scale = scale;
-  J.k_scale = (cache_dtype == ORC_E4M3) ? k_scale : 1.0;
-  J.v_scale = (cache_dtype == ORC_E4M3) ? v_scale : 1.0;
+  J.k_scale = (cache_dtype == ORC_E4M3 || cache_dtype == ORC_NVFP4) ? k_scale : 1.0;
+  J.v_scale = (cache_dtype == ORC_E4M3 || cache_dtype == ORC_NVFP4) ? v_scale : 1.0;
   J.window = window;
   J.out = out;
   J.next_item = 0;
@@ -437,8 +577,8 @@ int orc_paged_attention_row(const void* q, int q_dtype, const void* k_cache,
   const int n = query_start_loc[r + 1] - query_start_loc[r];
   const int L = seq_lens[r];
   if (i < 0 || i >= n || L < n || window < 0) return ORC_BAD_ARG;
-  const double ks = (cache_dtype == ORC_E4M3) ? k_scale : 1.0;
-  const double vs = (cache_dtype == ORC_E4M3) ? v_scale : 1.0;
+  const double ks = (cache_dtype == ORC_E4M3 || cache_dtype == ORC_NVFP4) ? k_scale : 1.0;
+  const double vs = (cache_dtype == ORC_E4M3 || cache_dtype == ORC_NVFP4) ? v_scale : 1.0;
   const int64_t t = query_start_loc[r] + i;
   const int visible = L - n + i + 1;
   const int first = first_visible_key(L - n + i, window);
@@ -455,7 +595,7 @@ int orc_paged_attention_row(const void* q, int q_dtype, const void* k_cache,
     double dot = 0.0;
     for (int d = 0; d < D; ++d)
       dot += load_elem(q, (t * num_q_heads + h) * (int64_t)D + d, q_dtype) *
-             (ks * load_elem(k_cache, base + d, cache_dtype));
+             (ks * load_kv(k_cache, base + d, cache_dtype, bs, D));
     s[j] = scale * dot;
     if (s[j] > smax) smax = s[j];
   }
@@ -469,7 +609,7 @@ int orc_paged_attention_row(const void* q, int q_dtype, const void* k_cache,
     int32_t b = block_tables[(int64_t)r * max_blocks_per_seq + j / bs];
     int64_t base = (((int64_t)b * num_kv_heads + g) * bs + j % bs) * D;
     for (int d = 0; d < D; ++d)
-      out_row[d] += s[j] * (vs * load_elem(v_cache, base + d, cache_dtype));
+      out_row[d] += s[j] * (vs * load_kv(v_cache, base + d, cache_dtype, bs, D));
   }
   for (int d = 0; d < D; ++d) out_row[d] /= denom;
   free(s);

@@ -34,6 +34,11 @@ MUTANTS = {
     # sliding window one key wide too many (keys p - W .. p)
     "window_off_by_one": (["  int first = position - window + 1;"],
                           ["  int first = position - window;"]),
+    # NVFP4 codes written high nibble first
+    "nvfp4_nibble_order": (["      codes[d / 2] |= (uint8_t)(c << (4 * (d & 1)));"],
+                           ["      codes[d / 2] |= (uint8_t)(c << (4 - 4 * (d & 1)));"]),
+    # INT4 scale max |x| / 8 instead of / 7
+    "int4_scale": (["div_f32(amax, 7.0f)"], ["div_f32(amax, 8.0f)"]),
     # ties to odd
     "ties_to_odd": (["(c & 1) == 0 && (best & 1) == 1"],
                     ["(c & 1) == 1 && (best & 1) == 0"]),
@@ -57,6 +62,8 @@ CATCHERS = {
     "scale_swap": pins.test_paged_bf16_and_fp8_match_sdpa_on_decoded_values,
     "ties_to_odd": pins.test_e4m3_encode_roundtrip_and_ties,
     "window_off_by_one": pins.test_window_of_one_key_is_the_own_value,
+    "nvfp4_nibble_order": pins.test_nvfp4_write_properties,
+    "int4_scale": pins.test_int4_write_properties,
     "layout_swap": pins.test_fig2_reshape_writes_only_the_new_slots,
     "copy_k_only": pins.test_copy_blocks_copies_whole_blocks_only,
 }

@@ -641,3 +641,180 @@ def test_window_row_function_equals_full_step():
             row = oracle.paged_attention_row(*args, r, i, h, scale=0.4,
                                              window=9)
             assert np.array_equal(row, out[md["query_start_loc"][r] + i, h])
+
+
+# ---------------------------------------------------------------------------
+# lower-bit KV caches ("01. vLLM", KV cache options table: nvfp4 and
+# int4_per_token_head).  Pages of one (block, KV head): 16 * D / 2 bytes of
+# codes (element 2i in the low nibble of byte i of its token), then the
+# scales: 16 fp32 (int4, one per token) or 16 * D / 16 E4M3 (nvfp4).
+# ---------------------------------------------------------------------------
+E2M1 = json.load(open(os.path.join(GOLDEN, "e2m1_values.json")))["values"]
+
+
+def _parse_page(page, fmt, D, bs=16):
+    """Independent reading of one 4-bit page: [bs, D] decoded values
+    (without the per-tensor scale), the codes, and the scales."""
+    page = np.asarray(page, dtype=np.uint8)
+    codes_b = page[:bs * D // 2].reshape(bs, D // 2)
+    nib = np.stack([codes_b & 0xF, codes_b >> 4], axis=-1).reshape(bs, D)
+    if fmt == "int4":
+        sc = page[bs * D // 2:].view(np.float32)
+        assert sc.shape == (bs,)
+        signed = np.where(nib >= 8, nib.astype(np.int64) - 16, nib)
+        return sc.astype(np.float64)[:, None] * signed, signed, sc
+    bsc = page[bs * D // 2:].reshape(bs, D // 16)
+    bval = torch.from_numpy(bsc.copy()).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+    vals = np.asarray(E2M1, dtype=np.float64)[nib]
+    return np.repeat(bval, 16, axis=1) * vals, nib, bsc
+
+
+def test_e2m1_decode_matches_the_spec_table():
+    for c in range(16):
+        v = oracle.e2m1_to_double(c)
+        assert v == E2M1[c] and np.signbit(v) == np.signbit(E2M1[c])
+
+
+def test_e2m1_encode_nearest_ties_to_even_saturating():
+    for c in range(16):
+        assert oracle.e2m1_encode(E2M1[c]) == c               # round trip
+    # midpoints go to the code whose mantissa bit is 0
+    for y, c in ((0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4),
+                 (3.5, 6), (5.0, 6), (-0.75, 10), (-5.0, 14)):
+        assert oracle.e2m1_encode(y) == c, y
+    for y, c in ((0.2501, 1), (0.7499, 1), (4.99, 6), (5.01, 7), (6.5, 7),
+                 (1e30, 7), (-1e30, 15)):
+        assert oracle.e2m1_encode(y) == c, y
+
+
+def test_int4_encode_nearest_ties_to_even_clamped():
+    for y, c in ((0.5, 0), (1.5, 2), (2.5, 2), (-0.5, 0), (-1.5, -2),
+                 (6.5, 6), (7.4, 7), (7.6, 7), (-9.0, -7), (3.49, 3)):
+        assert oracle.int4_encode(y) == c, y
+
+
+def _write_4bit(fmt, x, D, scale=1.0):
+    """Write tokens x [T, Hkv, D] (float32) into slots 0..T-1 of a fresh
+    4-bit cache with the oracle; returns the cache."""
+    T, Hkv, _ = x.shape
+    nb = -(-T // 16)
+    pb = oracle.page_bytes_4bit(fmt, D)
+    kc = np.full((nb, Hkv, pb), 0xA5, dtype=np.uint8)
+    vc = kc.copy()
+    oracle.reshape_and_cache(x, x, kc, vc, np.arange(T), cache_dtype=fmt,
+                             k_scale=scale, v_scale=scale)
+    assert np.array_equal(kc, vc)
+    return kc
+
+
+def test_int4_write_properties():
+    rng = np.random.default_rng(71)
+    D = 64
+    x = (rng.standard_normal((16, 2, D)) * rng.uniform(0.01, 100, (16, 2, 1))
+         ).astype(np.float32)
+    x[3, 1] = 0.0                                  # an all-zero token-head
+    x[5, 0, :15] = 0.5 * np.arange(-7, 8)          # multiples of amax / 7
+    x[5, 0, 15:] = 0.0
+    kc = _write_4bit("int4", x, D)
+    for h in range(2):
+        deq, codes, sc = _parse_page(kc[0, h], "int4", D)
+        for t in range(16):
+            amax = float(np.abs(x[t, h]).max())
+            if amax == 0.0:
+                assert sc[t] == 0 and (codes[t] == 0).all()
+                continue
+            assert sc[t] == np.float32(amax) / np.float32(7.0)
+            assert np.abs(codes[t]).max() == 7          # the extreme element
+            err = np.abs(deq[t] - x[t, h].astype(np.float64))
+            assert (err <= 0.5 * float(sc[t]) * (1 + 1e-6)).all()
+            neg = _write_4bit("int4", -x[t:t + 1, h:h + 1], D)
+            assert np.array_equal(_parse_page(neg[0, 0], "int4", D)[1][0],
+                                  -codes[t])           # sign symmetric
+    deq, _, _ = _parse_page(kc[0, 0], "int4", D)
+    np.testing.assert_array_equal(deq[5], x[5, 0])
+
+
+def test_nvfp4_write_properties():
+    rng = np.random.default_rng(72)
+    D, g = 128, 2.0 ** -6
+    x = (rng.standard_normal((16, 1, D)) * rng.uniform(0.01, 5, (16, 1, 1))
+         ).astype(np.float32)
+    # a token whose values are on the grid: decoded exactly
+    grid = np.asarray(E2M1[:8], dtype=np.float32)
+    x[7, 0] = (g * 2.0 * grid[np.arange(D) % 8]).astype(np.float32)
+    kc = _write_4bit("nvfp4", x, D, scale=g)
+    deq, codes, bsc = _parse_page(kc[0, 0], "nvfp4", D)
+    for t in range(16):
+        for b in range(D // 16):
+            blk = x[t, 0, 16 * b:16 * b + 16]
+            amax = float(np.abs(blk).max())
+            want = torch.tensor((np.float32(amax) / np.float32(6.0)) /
+                                np.float32(g)).to(torch.float8_e4m3fn)
+            assert bsc[t, b] == int(want.view(torch.uint8))
+            r = np.float32(float(want.to(torch.float64)) * g)
+            # each element decodes to the grid point nearest to x / r (a
+            # tie may go either way here; the encoder pin fixes ties)
+            y = blk / r
+            got = deq[t, 16 * b:16 * b + 16] / float(want.to(torch.float64))
+            dist = np.abs(np.abs(y)[:, None] - grid[None, :])
+            nearest = grid[np.argmin(dist, axis=1)] * np.sign(y)
+            assert (np.abs(np.abs(got) - np.abs(nearest)) <=
+                    (np.sort(dist, 1)[:, 1] - np.sort(dist, 1)[:, 0] < 1e-6)
+                    * 2.0 + 1e-12).all()
+    np.testing.assert_allclose(deq[7] * g, x[7, 0], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4"])
+def test_4bit_attention_equals_sdpa_on_decoded_values(fmt):
+    rng = np.random.default_rng(73)
+    Hq, Hkv, D, NB = 8, 2, 32, 20
+    shapes = [(1, 45), (4, 33), (2, 16), (9, 40)]
+    q, kc_f, vc_f, reqs, qs, ks, vs = random_paged_step(rng, shapes, Hq, Hkv,
+                                                        D, NB)
+    md = oracle.step_metadata(reqs)
+    g = 0.01 if fmt == "nvfp4" else 1.0
+    pb = oracle.page_bytes_4bit(fmt, D)
+    kc = np.zeros((NB, Hkv, pb), dtype=np.uint8)
+    vc = np.zeros((NB, Hkv, pb), dtype=np.uint8)
+    kk = np.concatenate(ks, 0)
+    vv = np.concatenate(vs, 0)
+    slots = np.concatenate([[oracle.slot_of(r.block_ids, j) for j in
+                             range(r.num_computed + r.num_new)] for r in reqs])
+    oracle.reshape_and_cache(kk, vv, kc, vc, slots, cache_dtype=fmt,
+                             k_scale=g, v_scale=g)
+    out = oracle.paged_attention(q, kc, vc, md["block_tables"],
+                                 md["seq_lens"], md["query_start_loc"],
+                                 scale=0.3, cache_dtype=fmt, k_scale=g,
+                                 v_scale=g)
+
+    def decoded(cache, r):
+        L = r.num_computed + r.num_new
+        rows = []
+        for j in range(L):
+            b, o = r.block_ids[j // 16], j % 16
+            rows.append([_parse_page(cache[b, h], fmt, D)[0][o] for h in
+                         range(Hkv)])
+        return np.asarray(rows) * g
+
+    ref = sdpa_reference([x.astype(np.float64) for x in qs],
+                         [decoded(kc, r) for r in reqs],
+                         [decoded(vc, r) for r in reqs], Hq // Hkv, 0.3)
+    np.testing.assert_allclose(out, np.concatenate(ref, 0), rtol=0,
+                               atol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nvfp4"])
+def test_4bit_copy_blocks_copies_whole_pages(fmt):
+    rng = np.random.default_rng(74)
+    pb = oracle.page_bytes_4bit(fmt, 128)
+    kc = rng.integers(0, 256, size=(9, 4, pb), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(9, 4, pb), dtype=np.uint8)
+    k0, v0 = kc.copy(), vc.copy()
+    oracle.copy_blocks(kc, vc, np.array([[2, 7], [0, 5]]), cache_dtype=fmt,
+                       head_dim=128)
+    np.testing.assert_array_equal(kc[7], k0[2])
+    np.testing.assert_array_equal(vc[5], v0[0])
+    keep = [0, 1, 2, 3, 4, 6, 8]
+    np.testing.assert_array_equal(kc[keep], k0[keep])
+    np.testing.assert_array_equal(vc[keep], v0[keep])
