@@ -68,8 +68,27 @@ typedef enum {
   PA_F32 = 0,
   PA_F16 = 1,
   PA_BF16 = 2,
-  PA_FP8_E4M3 = 3 /* OCP FP8 E4M3 "FN": bias 7, max 448, no inf, 0x7f NaN */
+  PA_FP8_E4M3 = 3, /* OCP FP8 E4M3 "FN": bias 7, max 448, no inf, 0x7f NaN */
+  PA_INT4 = 4,     /* cache only: int4_per_token_head (4-bit pages below)  */
+  PA_NVFP4 = 5     /* cache only: NVFP4 (4-bit pages below)                */
 } pa_dtype;
+
+/*
+ * 4-bit KV caches ([Overview], KV cache options table, --kv-cache-dtype:
+ * nvfp4, int4_per_token_head).  k_cache and v_cache are then byte arrays of
+ * [num_blocks][num_kv_heads][PA_PAGE_BYTES(dtype, head_dim)], one page per
+ * (block, KV head), 16-byte aligned:
+ *   - codes: 16 tokens x head_dim / 2 bytes, token by token; element 2i of a
+ *     token in the low nibble of its byte i, element 2i + 1 in the high one;
+ *   - then the scales: PA_INT4, 16 fp32 (one per token); PA_NVFP4, 16 x
+ *     head_dim / 16 E4M3 bytes (token by token, one per 16 elements).
+ * Values: PA_INT4: scale_t * code (two's complement, -8 .. 7); PA_NVFP4:
+ * tensor_scale * e4m3(block scale) * e2m1(code), with the E2M1 element of
+ * the OCP Microscaling specification (values 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+ * their negatives) and tensor_scale = k_scale for K, v_scale for V.
+ */
+#define PA_PAGE_BYTES(dtype, head_dim)                                     \
+  ((dtype) == PA_INT4 ? 8 * (head_dim) + 64 : 9 * (head_dim))
 
 /* Device-side error flags (bit mask) reported by pa_get_device_error. */
 #define PA_DEV_ERR_SLOT 0x1u      /* slot >= num_blocks * block_size        */
@@ -112,7 +131,15 @@ const char* pa_status_string(pa_status status);
  *                 PA_FP8_E4M3: the code is the E4M3 value nearest to
  *                 fl32(x / scale) (one correctly rounded fp32 division),
  *                 ties to even, saturating to +-448; scale = k_scale for K
- *                 and v_scale for V, both finite and > 0.
+ *                 and v_scale for V, both finite and > 0.  Or a 4-bit cache
+ *                 (layout above), each (token, KV head) quantised on its own:
+ *                 PA_INT4: s = fl32(max|x| / 7), code = nearest integer to
+ *                 fl32(x / s) (ties to even) in [-7, 7] (s = 0: codes 0;
+ *                 k_scale, v_scale unused); PA_NVFP4, per 16 elements: block
+ *                 scale b = E4M3 code of fl32(fl32(max|x| / 6) / scale) as
+ *                 above, r = fl32(e4m3(b) * scale), code = E2M1 value
+ *                 nearest to fl32(x / r), ties to even, saturating at 6
+ *                 (r = 0: codes 0); scale = k_scale / v_scale, finite, > 0.
  * Two tokens must not map to the same slot (the order of such writes is
  * unspecified).
  */
@@ -142,7 +169,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
  *                 and no dst may also appear as a src (the pairs run in
  *                 parallel).  An id outside [0, num_blocks) is skipped and
  *                 flagged PA_DEV_ERR_BLOCK_ID.
- * The copy is bit-exact for every cache dtype.
+ * The copy is bit-exact for every cache dtype (4-bit pages: codes and
+ * scales together).
  */
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype cache_dtype,
                          int64_t num_blocks, int block_size, int num_kv_heads,
@@ -209,7 +237,9 @@ pa_status pa_attention_workspace_size(int64_t num_tokens, int num_q_heads,
  *
  * Supported: head_dim 64 or 128; block_size 16; num_q_heads a multiple of
  * num_kv_heads; caches bf16/fp16 (with q of the same type), fp32 (with fp32
- * q), FP8 E4M3 (with bf16 or fp16 q).
+ * q), FP8 E4M3, INT4 or NVFP4 (with bf16 or fp16 q).  For a 4-bit cache,
+ * k_j and v_j are the decoded values of the layout above (NVFP4: times
+ * k_scale, v_scale).
  */
 pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
                        const void* v_cache, pa_dtype cache_dtype,

@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE = \
     range(5)
-PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3, PA_INT4, PA_NVFP4 = range(6)
 PA_DEV_ERR_SLOT, PA_DEV_ERR_BLOCK_ID, PA_DEV_ERR_METADATA, \
     PA_DEV_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 BLOCK_SIZE = 16
@@ -41,7 +41,35 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_copy_blocks",
             "pa_attention_window_workspace_size", "pa_set_wait_limit_ns",
             "pa_test_skip_copy")
 
-_DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3}
+_DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3,
+       "int4": PA_INT4, "nvfp4": PA_NVFP4}
+
+
+def page_bytes_4bit(cache_dtype: str, head_dim: int) -> int:
+    """PA_PAGE_BYTES of pa.h: bytes of one (block, KV head) page of a 4-bit
+    cache (int4: codes + 16 fp32 scales; nvfp4: codes + E4M3 block scales)."""
+    return 8 * head_dim + (64 if cache_dtype == "int4" else head_dim)
+
+
+def _cache_geometry(cache: torch.Tensor, cache_dtype: Optional[str],
+                    head_dim: Optional[int] = None):
+    """(num_blocks, kv_heads, block_size, head_dim) of a cache tensor:
+    [NB, Hkv, 16, D] elements, or [NB, Hkv, page_bytes] uint8 for the 4-bit
+    formats (head_dim from the page size when not given)."""
+    if cache_dtype in ("int4", "nvfp4"):
+        if cache.dim() != 3 or cache.dtype != torch.uint8:
+            raise ValueError("a 4-bit cache is a uint8 [NB, Hkv, page_bytes] "
+                             "tensor")
+        NB, H, pb = cache.shape
+        D = (pb - 64) // 8 if cache_dtype == "int4" else pb // 9
+        if head_dim is not None and head_dim != D:
+            raise ValueError("head_dim does not match the cache's pages")
+        if page_bytes_4bit(cache_dtype, D) != pb:
+            raise ValueError("page size matches no head_dim")
+        return NB, H, BLOCK_SIZE, D
+    if cache.dim() != 4:
+        raise ValueError("the caches must be [NB, Hkv, 16, D]")
+    return tuple(cache.shape)
 _lib = None
 
 
@@ -144,15 +172,15 @@ def _check(status: int, what: str) -> None:
 
 
 def _step_shapes(q, k_cache, v_cache, block_tables, seq_lens,
-                 query_start_loc, out):
+                 query_start_loc, out, cache_dtype=None):
     """Check the tensors of one attention step the way the C ABI reads them
     (contiguous, int32 metadata, consistent sizes) and return (T, Hq, D, NB,
     Hkv, block_size, B).  Runs before any pointer is taken, so a strided q or
     an int64 length array is refused instead of being read as raw bytes."""
-    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
-        raise ValueError("q must be [T, Hq, D] and the caches [NB, Hkv, 16, D]")
+    if q.dim() != 3 or v_cache.shape != k_cache.shape:
+        raise ValueError("q must be [T, Hq, D] and both caches alike")
     T, Hq, D = q.shape
-    NB, Hkv, bs, Dc = k_cache.shape
+    NB, Hkv, bs, Dc = _cache_geometry(k_cache, cache_dtype)
     if Dc != D:
         raise ValueError("head_dim of q and of the caches differ")
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
@@ -185,7 +213,7 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor,
         raise ValueError("key/value must be [T, Hkv, D] with contiguous rows")
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
         raise ValueError("slot_mapping must be int64 [num_tokens]")
-    NB, Hc, bs, Dc = k_cache.shape
+    NB, Hc, bs, Dc = _cache_geometry(k_cache, cache_dtype, D)
     if (Hc, Dc) != (Hkv, D) or v_cache.shape != k_cache.shape:
         raise ValueError("cache shape does not match key/value")
     lib = _load()
@@ -204,7 +232,7 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
     """block_mapping int64 [P, 2] of (src, dst) pairs."""
     if block_mapping.dtype != torch.int64 or not block_mapping.is_contiguous():
         raise ValueError("block_mapping must be a contiguous int64 [P, 2]")
-    NB, Hkv, bs, D = k_cache.shape
+    NB, Hkv, bs, D = _cache_geometry(k_cache, cache_dtype)
     lib = _load()
     st = lib.pa_copy_blocks(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
                             _dtype_code(k_cache, cache_dtype), NB, bs, Hkv, D,
@@ -238,7 +266,8 @@ def pa_attention(q: torch.Tensor, k_cache: torch.Tensor,
     seq_lens int32 [B]; query_start_loc int32 [B+1].  Returns out [T, Hq, D]
     (allocated if not given; the workspace too)."""
     T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
-                                            seq_lens, query_start_loc, out)
+                                            seq_lens, query_start_loc, out,
+                                            cache_dtype)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -286,7 +315,8 @@ def pa_attention_window(q: torch.Tensor, k_cache: torch.Tensor,
     """pa_attention with a sliding window of `sliding_window` keys (each
     query sees its own key and the window - 1 keys before it; 0: none)."""
     T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
-                                            seq_lens, query_start_loc, out)
+                                            seq_lens, query_start_loc, out,
+                                            cache_dtype)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -370,7 +400,8 @@ def pa_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor,
     if out is None:
         raise ValueError("pa_attention_noalloc needs a caller-provided out")
     T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
-                                            seq_lens, query_start_loc, out)
+                                            seq_lens, query_start_loc, out,
+                                            cache_dtype)
     st = _load().pa_attention_noalloc(_dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
            _dev(v_cache, "v_cache"), _dtype_code(k_cache, cache_dtype), NB, bs,
            Hq, Hkv, D, _dev(block_tables, "block_tables"),

@@ -7,6 +7,8 @@
 // online, "Boundaries: FlashAttention ..."): query i of request r sees keys
 // 0 .. L - n + i (with a sliding window of W keys only L - n + i - W + 1 ..
 // L - n + i), query head h reads KV head h / group.
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -31,13 +33,30 @@ struct GenericParams {
   int window;  // sliding window in keys (kNoWindow: none)
 };
 
-template <typename TC>
-__device__ __forceinline__ float load_cache(const void* base, int64_t i) {
-  return to_f32(static_cast<const TC*>(base)[i]);
-}
-template <>
-__device__ __forceinline__ float load_cache<uint8_t>(const void* base, int64_t i) {
-  return e4m3_to_f32(static_cast<const uint8_t*>(base)[i]);
+// Element d of the token at offset o of the page of (blk, g); the 4-bit
+// formats decode from their pages (pa.h), without the per-tensor scale.
+struct Int4Page {};
+struct Nvfp4Page {};
+
+template <typename TC, int kD>
+__device__ __forceinline__ float load_cache(const void* base, int64_t page,
+                                            int o, int d) {
+  if constexpr (std::is_same<TC, uint8_t>::value) {
+    return e4m3_to_f32(static_cast<const uint8_t*>(base)[(page * kBS + o) * kD + d]);
+  } else if constexpr (std::is_same<TC, Int4Page>::value) {
+    const uint8_t* pg = static_cast<const uint8_t*>(base) + page * (8 * kD + 64);
+    const uint32_t byte = pg[o * (kD / 2) + d / 2];
+    const int nib = (int)((d & 1) ? (byte >> 4) : (byte & 15u));
+    const float sc = *reinterpret_cast<const float*>(pg + kBS * (kD / 2) + 4 * o);
+    return sc * (float)(nib >= 8 ? nib - 16 : nib);
+  } else if constexpr (std::is_same<TC, Nvfp4Page>::value) {
+    const uint8_t* pg = static_cast<const uint8_t*>(base) + page * (9 * kD);
+    const uint32_t byte = pg[o * (kD / 2) + d / 2];
+    const uint32_t nib = (d & 1) ? (byte >> 4) : (byte & 15u);
+    return e4m3_to_f32(pg[kBS * (kD / 2) + o * (kD / 16) + d / 16]) * e2m1_to_f32(nib);
+  } else {
+    return to_f32(static_cast<const TC*>(base)[(page * kBS + o) * kD + d]);
+  }
 }
 
 template <typename TQ, typename TC, int kD>
@@ -81,12 +100,12 @@ attn_generic_kernel(GenericParams p) {
       if (lane == 0) flag_error(p.err, PA_DEV_ERR_BLOCK_ID);
       blk = 0;
     }
-    const int64_t base =
-        (((int64_t)blk * p.num_kv_heads + g) * kBS + (j % kBS)) * kD;
+    const int64_t page = (int64_t)blk * p.num_kv_heads + g;
+    const int o = j % kBS;
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
-      dot += qv[k] * load_cache<TC>(p.k_cache, base + lane + 32 * k);
+      dot += qv[k] * load_cache<TC, kD>(p.k_cache, page, o, lane + 32 * k);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) dot += __shfl_xor_sync(~0u, dot, d);
     const float mnew = fmaxf(m, dot);
@@ -95,7 +114,7 @@ attn_generic_kernel(GenericParams p) {
     l = l * alpha + pj;
 #pragma unroll
     for (int k = 0; k < kPer; ++k)
-      acc[k] = acc[k] * alpha + pj * load_cache<TC>(p.v_cache, base + lane + 32 * k);
+      acc[k] = acc[k] * alpha + pj * load_cache<TC, kD>(p.v_cache, page, o, lane + 32 * k);
     m = mnew;
   }
   TQ* op = static_cast<TQ*>(p.out) + row * kD;
@@ -138,7 +157,7 @@ cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream) {
   gp.group = a.num_q_heads / a.num_kv_heads;
   gp.max_query_len = a.max_query_len;
   gp.max_seq_len = a.max_seq_len;
-  const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
+  const bool fp8 = a.cache_dtype == PA_FP8_E4M3 || a.cache_dtype == PA_NVFP4;
   gp.scale = a.scale;
   gp.k_scale = fp8 ? a.k_scale : 1.0f;
   gp.v_scale = fp8 ? a.v_scale : 1.0f;
@@ -154,6 +173,14 @@ cudaError_t launch_attention_generic(const AttnArgs& a, cudaStream_t stream) {
       if (a.q_dtype == PA_BF16)
         return launch_t<__nv_bfloat16, uint8_t>(gp, a.head_dim, stream);
       return launch_t<__half, uint8_t>(gp, a.head_dim, stream);
+    case PA_INT4:
+      if (a.q_dtype == PA_BF16)
+        return launch_t<__nv_bfloat16, Int4Page>(gp, a.head_dim, stream);
+      return launch_t<__half, Int4Page>(gp, a.head_dim, stream);
+    case PA_NVFP4:
+      if (a.q_dtype == PA_BF16)
+        return launch_t<__nv_bfloat16, Nvfp4Page>(gp, a.head_dim, stream);
+      return launch_t<__half, Nvfp4Page>(gp, a.head_dim, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -4,7 +4,8 @@
 //    written into its slot (block = slot / 16, offset = slot % 16), as
 //    "vLLM engine anatomy" describes under "Prefill, decode ..." and in
 //    Figure 2; an FP8 cache ("01. vLLM", --kv-cache-dtype fp8) stores the
-//    E4M3 code nearest to fl32(x / scale).
+//    E4M3 code nearest to fl32(x / scale); the 4-bit caches of the same
+//    table (nvfp4, int4_per_token_head) quantise each (token, KV head).
 //  * copy_blocks: block-granular copy-on-write of shared blocks ("vLLM
 //    engine anatomy", PagedAttention section; V0's blocks_to_copy in "vLLM
 //    V0 vs V1").
@@ -146,6 +147,80 @@ cudaError_t launch_reshape_t(const void* key, const void* value,
   return e;
 }
 
+// 4-bit caches: one warp per (token, KV head, K or V).  Lane l holds the
+// kE = head_dim / 32 consecutive elements l*kE ..; a 16-element NVFP4 block
+// is the 16 / kE lanes of one aligned group.  Quantisation follows the
+// page format of pa.h: INT4, s = fl32(max|x| / 7), code = nearest integer
+// to fl32(x / s) in [-7, 7]; NVFP4 per block, b = E4M3(fl32(fl32(max|x| / 6)
+// / scale)), r = fl32(e4m3(b) * scale), code = E2M1(fl32(x / r)).
+template <typename Tin, bool kNvfp4, int kD>
+__global__ void __launch_bounds__(kThreads)
+reshape_4bit_kernel(const Tin* __restrict__ key, const Tin* __restrict__ value,
+                    int64_t num_tokens, int64_t key_stride,
+                    int64_t value_stride, uint8_t* __restrict__ k_cache,
+                    uint8_t* __restrict__ v_cache, int64_t num_slots,
+                    int num_kv_heads, const int64_t* __restrict__ slot_mapping,
+                    float k_scale, float v_scale, unsigned* err) {
+  constexpr int kE = kD / 32;
+  constexpr int kPage = kNvfp4 ? 9 * kD : 8 * kD + 64;
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  if (w >= num_tokens * 2 * num_kv_heads) return;
+  const int64_t t = w / (2 * num_kv_heads);
+  const int rem = (int)(w - t * 2 * num_kv_heads);
+  const int which = rem / num_kv_heads, h = rem - which * num_kv_heads;
+  const int64_t slot = __ldg(slot_mapping + t);
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (rem == 0 && lane == 0) flag_error(err, PA_DEV_ERR_SLOT);
+    return;
+  }
+  const Tin* src = (which ? value + t * value_stride : key + t * key_stride) +
+                   (int64_t)h * kD + lane * kE;
+  float x[kE];
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    x[e] = to_f32(src[e]);
+    amax = fmaxf(amax, fabsf(x[e]));
+  }
+  const int64_t b = slot / kBS;
+  const int o = (int)(slot - b * kBS);
+  uint8_t* page = (which ? v_cache : k_cache) + (b * num_kv_heads + h) * kPage;
+  uint32_t code[kE];
+  if constexpr (!kNvfp4) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, d));
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 7.0f) : 0.f;
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      int c = sc > 0.f ? __float2int_rn(__fdiv_rn(x[e], sc)) : 0;
+      c = max(-7, min(7, c));
+      code[e] = (uint32_t)c & 0xFu;
+    }
+    if (lane == 0)
+      *reinterpret_cast<float*>(page + kBS * (kD / 2) + 4 * o) = sc;
+  } else {
+    constexpr int kLanes = 16 / kE;  // lanes of one 16-element block
+#pragma unroll
+    for (int d = 1; d < kLanes; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, d));
+    const float g = which ? v_scale : k_scale;
+    const float u = __fdiv_rn(__fdiv_rn(amax, 6.0f), g);
+    const uint8_t bs =
+        static_cast<uint8_t>(__nv_cvt_float_to_fp8(u, __NV_SATFINITE, __NV_E4M3));
+    const float r = __fmul_rn(e4m3_to_f32(bs), g);
+#pragma unroll
+    for (int e = 0; e < kE; ++e) code[e] = r > 0.f ? e2m1_encode(__fdiv_rn(x[e], r)) : 0u;
+    if (lane % kLanes == 0)
+      page[kBS * (kD / 2) + o * (kD / 16) + (lane * kE) / 16] = bs;
+  }
+  // kE / 2 bytes of codes: element 2i in the low nibble of byte i
+  uint8_t* dst = page + o * (kD / 2) + lane * (kE / 2);
+#pragma unroll
+  for (int i = 0; i < kE / 2; ++i)
+    dst[i] = static_cast<uint8_t>(code[2 * i] | (code[2 * i + 1] << 4));
+}
+
 // Copy whole blocks: blockIdx.y walks the pairs, x-threads stripe the
 // block's bytes in 16-byte units (K and V).
 __global__ void __launch_bounds__(kThreads)
@@ -206,6 +281,46 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
       return cudaErrorInvalidValue;
   }
 #undef PA_RESHAPE
+}
+
+cudaError_t launch_reshape_4bit(const void* key, const void* value,
+                                pa_dtype kv_dtype, int64_t num_tokens,
+                                int64_t key_stride, int64_t value_stride,
+                                void* k_cache, void* v_cache,
+                                pa_dtype cache_dtype, int64_t num_blocks,
+                                int num_kv_heads, int head_dim,
+                                const int64_t* slot_mapping, float k_scale,
+                                float v_scale, unsigned* err,
+                                cudaStream_t stream) {
+  const int64_t warps = num_tokens * 2 * num_kv_heads;
+  const int64_t blocks = (warps * 32 + kThreads - 1) / kThreads;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  const bool nv = cache_dtype == PA_NVFP4;
+  uint8_t* kc = static_cast<uint8_t*>(k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(v_cache);
+  const int64_t slots = num_blocks * kBS;
+#define PA_RESHAPE4(T, NV, D)                                                  \
+  reshape_4bit_kernel<T, NV, D><<<(unsigned)blocks, kThreads, 0, stream>>>(    \
+      static_cast<const T*>(key), static_cast<const T*>(value), num_tokens,    \
+      key_stride, value_stride, kc, vc, slots, num_kv_heads, slot_mapping,     \
+      k_scale, v_scale, err)
+#define PA_RESHAPE4_D(T)                                                       \
+  if (head_dim == 128) {                                                       \
+    if (nv) PA_RESHAPE4(T, true, 128); else PA_RESHAPE4(T, false, 128);        \
+  } else {                                                                     \
+    if (nv) PA_RESHAPE4(T, true, 64); else PA_RESHAPE4(T, false, 64);          \
+  }
+  switch (kv_dtype) {
+    case PA_F32: PA_RESHAPE4_D(float); break;
+    case PA_F16: PA_RESHAPE4_D(__half); break;
+    case PA_BF16: PA_RESHAPE4_D(__nv_bfloat16); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef PA_RESHAPE4_D
+#undef PA_RESHAPE4
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,

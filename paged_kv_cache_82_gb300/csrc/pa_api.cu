@@ -56,7 +56,13 @@ int elem_bytes(pa_dtype t) {
   return 0;
 }
 
-bool valid_dtype(int t) { return t >= PA_F32 && t <= PA_FP8_E4M3; }
+bool valid_dtype(int t) { return t >= PA_F32 && t <= PA_NVFP4; }
+
+// bytes of one (block, KV head) page of a cache of type t
+int64_t page_bytes(pa_dtype t, int head_dim) {
+  if (is_4bit(t)) return PA_PAGE_BYTES(t, head_dim);
+  return (int64_t)PA_BLOCK_SIZE * head_dim * elem_bytes(t);
+}
 
 bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
@@ -225,10 +231,11 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
   if (pa_status st = cache_shape_status(num_blocks, block_size, num_kv_heads,
                                         head_dim))
     return st;
-  if (kv_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
-  if (cache_dtype != kv_dtype && cache_dtype != PA_FP8_E4M3)
+  if (kv_dtype == PA_FP8_E4M3 || is_4bit(kv_dtype)) return PA_ERR_UNSUPPORTED;
+  if (cache_dtype != kv_dtype && cache_dtype != PA_FP8_E4M3 &&
+      !is_4bit(cache_dtype))
     return PA_ERR_UNSUPPORTED;
-  if (cache_dtype == PA_FP8_E4M3 &&
+  if ((cache_dtype == PA_FP8_E4M3 || cache_dtype == PA_NVFP4) &&
       !(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0 && v_scale > 0))
     return PA_ERR_INVALID_ARG;
   const int64_t row = (int64_t)num_kv_heads * head_dim;
@@ -236,12 +243,13 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
   if (!k_cache || !v_cache) return PA_ERR_INVALID_ARG;
   if (num_tokens == 0) return PA_OK;
   if (!key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
-  const int ib = elem_bytes(kv_dtype), cb = elem_bytes(cache_dtype);
+  const int ib = elem_bytes(kv_dtype);
+  const int cb = is_4bit(cache_dtype) ? 16 : elem_bytes(cache_dtype);
   if (!aligned(key, ib) || !aligned(value, ib) || !aligned(k_cache, cb) ||
       !aligned(v_cache, cb) || !aligned(slot_mapping, 8))
     return PA_ERR_INVALID_ARG;
-  const size_t cache_bytes = (size_t)num_blocks * num_kv_heads * PA_BLOCK_SIZE *
-                             head_dim * cb;
+  const size_t cache_bytes =
+      (size_t)num_blocks * num_kv_heads * page_bytes(cache_dtype, head_dim);
   const size_t in_bytes_k = ((size_t)(num_tokens - 1) * key_stride + row) * ib;
   const size_t in_bytes_v = ((size_t)(num_tokens - 1) * value_stride + row) * ib;
   if (overlaps(k_cache, cache_bytes, v_cache, cache_bytes) ||
@@ -252,6 +260,13 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
     return PA_ERR_INVALID_ARG;
   const DeviceInfo* di = device_info();
   if (!di) return PA_ERR_CUDA;
+  if (is_4bit(cache_dtype)) {
+    cudaError_t e4 = launch_reshape_4bit(
+        key, value, kv_dtype, num_tokens, key_stride, value_stride, k_cache,
+        v_cache, cache_dtype, num_blocks, num_kv_heads, head_dim, slot_mapping,
+        k_scale, v_scale, di->err, reinterpret_cast<cudaStream_t>(stream));
+    return e4 == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   // 8-element vectors: 16 bytes (16-bit) or 32 bytes (fp32) on the input
   // side, 8 / 16 / 32 bytes on the cache side
   const size_t va = 8 * (size_t)ib;
@@ -279,8 +294,8 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, pa_dtype cache_dtype,
   if (num_pairs == 0) return PA_OK;
   if (!block_mapping || !aligned(block_mapping, 8)) return PA_ERR_INVALID_ARG;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return PA_ERR_INVALID_ARG;
-  const int64_t block_bytes = (int64_t)num_kv_heads * PA_BLOCK_SIZE * head_dim *
-                              elem_bytes(cache_dtype);
+  const int64_t block_bytes =
+      (int64_t)num_kv_heads * page_bytes(cache_dtype, head_dim);
   if (overlaps(k_cache, (size_t)(num_blocks * block_bytes), v_cache,
                (size_t)(num_blocks * block_bytes)))
     return PA_ERR_INVALID_ARG;
@@ -334,12 +349,12 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
     return st;
   if (num_q_heads <= 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
-  if (q_dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
-  if (cache_dtype != PA_FP8_E4M3 && cache_dtype != q_dtype)
-    return PA_ERR_UNSUPPORTED;
-  if (cache_dtype == PA_FP8_E4M3 && q_dtype == PA_F32) return PA_ERR_UNSUPPORTED;
+  if (q_dtype == PA_FP8_E4M3 || is_4bit(q_dtype)) return PA_ERR_UNSUPPORTED;
+  const bool quantised = cache_dtype == PA_FP8_E4M3 || is_4bit(cache_dtype);
+  if (!quantised && cache_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
+  if (quantised && q_dtype == PA_F32) return PA_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
-  if (cache_dtype == PA_FP8_E4M3 &&
+  if ((cache_dtype == PA_FP8_E4M3 || cache_dtype == PA_NVFP4) &&
       !(isfinite(k_scale) && isfinite(v_scale) && k_scale > 0 && v_scale > 0))
     return PA_ERR_INVALID_ARG;
   if (num_seqs < 0 || num_tokens < 0 || max_query_len < 0 || max_seq_len < 0 ||
@@ -351,14 +366,14 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens ||
       !query_start_loc || !out)
     return PA_ERR_INVALID_ARG;
-  const int qb = elem_bytes(q_dtype), cb = elem_bytes(cache_dtype);
+  const int qb = elem_bytes(q_dtype);
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 128) ||
       !aligned(v_cache, 128) || !aligned(block_tables, 4) ||
       !aligned(seq_lens, 4) || !aligned(query_start_loc, 4))
     return PA_ERR_INVALID_ARG;
   const size_t qo_bytes = (size_t)num_tokens * num_q_heads * head_dim * qb;
   const size_t cache_bytes =
-      (size_t)num_blocks * num_kv_heads * PA_BLOCK_SIZE * head_dim * cb;
+      (size_t)num_blocks * num_kv_heads * page_bytes(cache_dtype, head_dim);
   const DeviceInfo* di = device_info();
   if (!di) return PA_ERR_CUDA;
   const AttnPlan plan = make_plan(num_tokens, num_q_heads, num_kv_heads,

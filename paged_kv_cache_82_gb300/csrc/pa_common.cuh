@@ -19,6 +19,10 @@ namespace pa {
 
 constexpr int kBS = PA_BLOCK_SIZE;  // tokens per physical block
 
+__host__ __device__ constexpr bool is_4bit(int t) {
+  return t == PA_INT4 || t == PA_NVFP4;
+}
+
 // ----------------------------------------------------------------------------
 // device error word (one per device, defined in pa_api.cu; kernels receive
 // its address)
@@ -310,6 +314,28 @@ __device__ __forceinline__ __half from_f32<__half>(float x) {
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
+}
+
+// E2M1 (OCP Microscaling FP4: sign bit 3, exponent bits 2-1 with bias 1,
+// mantissa bit 0; values 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+__device__ __forceinline__ float e2m1_to_f32(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float mag = e == 0 ? 0.5f * (float)m
+                           : (1.0f + 0.5f * (float)m) * (float)(1u << (e - 1));
+  return (c & 8u) ? -mag : mag;
+}
+
+// E2M1 code nearest to y: the magnitude code counts the midpoints between
+// grid values that |y| has passed; a midpoint itself goes to the code with
+// mantissa bit 0 (ties to even); beyond 6 it saturates.  The sign bit
+// follows y's sign.
+__device__ __forceinline__ uint32_t e2m1_encode(float y) {
+  const float a = fabsf(y);
+  const uint32_t mag = (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) +
+                       (uint32_t)(a > 1.25f) + (uint32_t)(a >= 1.75f) +
+                       (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+                       (uint32_t)(a > 5.0f);
+  return (signbit(y) ? 8u : 0u) | mag;
 }
 
 __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {

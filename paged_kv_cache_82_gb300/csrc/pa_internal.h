@@ -31,6 +31,17 @@ cudaError_t launch_reshape_and_cache(const void* key, const void* value,
                                      float v_scale, bool vector_ok,
                                      unsigned* err, cudaStream_t stream);
 
+// 4-bit caches (PA_INT4, PA_NVFP4): one warp per (token, KV head, K or V)
+cudaError_t launch_reshape_4bit(const void* key, const void* value,
+                                pa_dtype kv_dtype, int64_t num_tokens,
+                                int64_t key_stride, int64_t value_stride,
+                                void* k_cache, void* v_cache,
+                                pa_dtype cache_dtype, int64_t num_blocks,
+                                int num_kv_heads, int head_dim,
+                                const int64_t* slot_mapping, float k_scale,
+                                float v_scale, unsigned* err,
+                                cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks,
                                int64_t block_bytes,
                                const int64_t* block_mapping, int64_t num_pairs,

@@ -28,6 +28,14 @@ BLOCK_SIZE = 16
 
 _TORCH_DT = {"f32": torch.float32, "f16": torch.float16,
              "bf16": torch.bfloat16}
+FOUR_BIT = ("int4", "nvfp4")
+
+
+def page_bytes_4bit(cache_dtype: str, head_dim: int) -> int:
+    """Bytes of one (block, KV head) page of a 4-bit cache: 16 tokens x
+    head_dim / 2 bytes of codes, then 16 fp32 scales (int4) or 16 x
+    head_dim / 16 E4M3 block scales (nvfp4)."""
+    return 8 * head_dim + (64 if cache_dtype == "int4" else head_dim)
 # NaN bit patterns used to poison unowned cache slots
 _NAN_BITS = {"f32": 0x7FC00000, "f16": 0x7E00, "bf16": 0x7FC0, "e4m3": 0x7F}
 _ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
@@ -60,7 +68,7 @@ class Workload:
     head_dim: int
     num_blocks: int
     q_dtype: str            # "f32" | "f16" | "bf16"
-    cache_dtype: str        # "f32" | "f16" | "bf16" | "e4m3"
+    cache_dtype: str        # "f32" | "f16" | "bf16" | "e4m3" | "int4" | "nvfp4"
     scale: float
     k_scale: float
     v_scale: float
@@ -88,9 +96,13 @@ class Workload:
     def kv_bytes(self, unique: bool = True) -> int:
         """Bytes of K and V the step's attention must read: every key of
         every request once (a block shared by several requests counted once
-        when unique=True)."""
-        eb = _ELEM_BYTES[self.cache_dtype]
-        per_token = 2 * eb * self.num_kv_heads * self.head_dim
+        when unique=True); a 4-bit cache's scales included."""
+        if self.cache_dtype in FOUR_BIT:
+            per_token = 2 * self.num_kv_heads * page_bytes_4bit(
+                self.cache_dtype, self.head_dim) // BLOCK_SIZE
+        else:
+            per_token = (2 * _ELEM_BYTES[self.cache_dtype] *
+                         self.num_kv_heads * self.head_dim)
         if not unique:
             return per_token * sum(r.seq_len for r in self.requests)
         seen = {}
@@ -176,6 +188,42 @@ def _fill_cache(cache: torch.Tensor, filled: dict, dtype: str, seed: int,
         cache[torch.from_numpy(bsel)] = dst
 
 
+def _fill_cache_4bit(cache: torch.Tensor, filled: dict, fmt: str,
+                     head_dim: int, seed: int, stream: int) -> None:
+    """4-bit pages (see page_bytes_4bit): random codes in every token slot
+    of the listed blocks; scales random for the first n tokens of each block
+    (int4: 0.05 + 0.25 |N(0,1)|; nvfp4: E4M3 codes of 0.25 .. 0.94) and NaN
+    for the rest (int4: fp32 NaN; nvfp4: the E4M3 NaN code), so that a read
+    of an unwritten slot shows."""
+    if not filled:
+        return
+    NB, H, pb = cache.shape
+    cb = BLOCK_SIZE * head_dim // 2
+    blocks = np.fromiter(filled.keys(), dtype=np.int64, count=len(filled))
+    counts = np.fromiter(filled.values(), dtype=np.int64, count=len(filled))
+    step = max(1, (1 << 22) // (H * pb))
+    for s0 in range(0, len(blocks), step):
+        bsel = blocks[s0:s0 + step]
+        n = len(bsel)
+        rng = np.random.default_rng(np.random.SeedSequence([seed, stream, s0]))
+        pages = np.empty((n, H, pb), dtype=np.uint8)
+        pages[:, :, :cb] = rng.integers(0, 256, size=(n, H, cb), dtype=np.uint8)
+        keep = (np.arange(BLOCK_SIZE)[None, :] <
+                counts[s0:s0 + step][:, None])                  # [n, 16]
+        if fmt == "int4":
+            sc = (0.05 + 0.25 * np.abs(rng.standard_normal(
+                (n, H, BLOCK_SIZE)))).astype(np.float32)
+            sc = np.where(keep[:, None, :], sc, np.float32(np.nan))
+            pages[:, :, cb:] = sc.view(np.uint8).reshape(n, H, 4 * BLOCK_SIZE)
+        else:
+            nsc = BLOCK_SIZE * head_dim // 16
+            sc = rng.integers(0x28, 0x38, size=(n, H, BLOCK_SIZE, head_dim // 16),
+                              dtype=np.uint8)
+            sc = np.where(keep[:, None, :, None], sc, np.uint8(0x7F))
+            pages[:, :, cb:] = sc.reshape(n, H, nsc)
+        cache[torch.from_numpy(bsel)] = torch.from_numpy(pages)
+
+
 def make_workload(name: str, seed: int, *, num_q_heads: int,
                   num_kv_heads: int, head_dim: int, num_blocks: int,
                   q_dtype: str, cache_dtype: str, requests: Sequence[Request],
@@ -198,11 +246,28 @@ def make_workload(name: str, seed: int, *, num_q_heads: int,
                         q_dtype).view(T, num_kv_heads, head_dim)
         value = _to_dtype(normal_f32(seed, 3, T * num_kv_heads * head_dim),
                           q_dtype).view(T, num_kv_heads, head_dim)
-    shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim)
-    k_cache = _nan_tensor(shape, cache_dtype)
-    v_cache = _nan_tensor(shape, cache_dtype)
-    _fill_cache(k_cache, filled, cache_dtype, seed, 4, k_scale)
-    _fill_cache(v_cache, filled, cache_dtype, seed, 5, v_scale)
+    if cache_dtype in FOUR_BIT:
+        shape4 = (num_blocks, num_kv_heads,
+                  page_bytes_4bit(cache_dtype, head_dim))
+        k_cache = torch.zeros(shape4, dtype=torch.uint8)
+        v_cache = torch.zeros(shape4, dtype=torch.uint8)
+        # every slot starts unwritten: NaN scales
+        for c in (k_cache, v_cache):
+            view = c.view(num_blocks * num_kv_heads, -1)
+            cb = BLOCK_SIZE * head_dim // 2
+            if cache_dtype == "int4":
+                view[:, cb:] = torch.full((BLOCK_SIZE,), float("nan"),
+                                          dtype=torch.float32).view(torch.uint8)
+            else:
+                view[:, cb:] = 0x7F
+        _fill_cache_4bit(k_cache, filled, cache_dtype, head_dim, seed, 4)
+        _fill_cache_4bit(v_cache, filled, cache_dtype, head_dim, seed, 5)
+    else:
+        shape = (num_blocks, num_kv_heads, BLOCK_SIZE, head_dim)
+        k_cache = _nan_tensor(shape, cache_dtype)
+        v_cache = _nan_tensor(shape, cache_dtype)
+        _fill_cache(k_cache, filled, cache_dtype, seed, 4, k_scale)
+        _fill_cache(v_cache, filled, cache_dtype, seed, 5, v_scale)
     return Workload(name=name, seed=seed, num_q_heads=num_q_heads,
                     num_kv_heads=num_kv_heads, head_dim=head_dim,
                     num_blocks=num_blocks, q_dtype=q_dtype,
