@@ -184,16 +184,18 @@ def _step(pa, wl, d):
     writes, attention.  Returns the number of our kernel launches (the
     library's own count)."""
     n0 = pa.pa_launch_count()
+    cdt = wl.cache_dtype
     if wl.copy_pairs:
-        pa.pa_copy_blocks(d["kc"], d["vc"], d["pairs"])
+        pa.pa_copy_blocks(d["kc"], d["vc"], d["pairs"], cache_dtype=cdt)
     if wl.write_new:
         pa.pa_reshape_and_cache(d["key"], d["value"], d["kc"], d["vc"],
                                 d["slots"], k_scale=wl.k_scale,
-                                v_scale=wl.v_scale)
+                                v_scale=wl.v_scale, cache_dtype=cdt)
     md = d["md"]
     pa.pa_attention(d["q"], d["kc"], d["vc"], d["bt"], d["sl"], d["qsl"],
                     md["max_query_len"], md["max_seq_len"], wl.scale,
-                    wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"])
+                    wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"],
+                    cache_dtype=cdt)
     return pa.pa_launch_count() - n0
 
 
@@ -430,7 +432,10 @@ def run_ours(args):
     if args.only != "all":
         make = {"decode": workloads.config2, "mixed": workloads.config4,
                 "prefill": workloads.prefill_chunk, "mha": workloads.config3,
-                "fp8long": workloads.config5}[args.only]
+                "fp8long": workloads.config5,
+                "int4": lambda **k: workloads.config2(cache_dtype="int4", **k),
+                "nvfp4": lambda **k: workloads.config2(cache_dtype="nvfp4",
+                                                       **k)}[args.only]
         # a smaller batch of the same shape (profiler captures); the mixed
         # step keeps its shared prefix and chunk, with fewer decodes and a
         # pool sized to them
@@ -516,7 +521,11 @@ def run_ours(args):
     # ---- the other decode workloads of the scope (kernel and step TB/s)
     others = {}
     for name, make in (("mha_fp16_32x8192", workloads.config3),
-                       ("fp8_long_context_70b", workloads.config5)):
+                       ("fp8_long_context_70b", workloads.config5),
+                       ("int4_decode_llama31_8b",
+                        lambda: workloads.config2(cache_dtype="int4")),
+                       ("nvfp4_decode_llama31_8b",
+                        lambda: workloads.config2(cache_dtype="nvfp4"))):
         wlo = make()
         do = _device_inputs(wlo, dev)
         o_step, o_kern, _ = _time_steps(pa, wlo, do, max(3, args.steps // 10),
@@ -528,6 +537,8 @@ def run_ours(args):
         others[name] = {
             "workload": wlo.description,
             "bytes": ob,
+            "keys_per_s": sum(r.seq_len for r in wlo.requests) /
+                          (statistics.mean(o_step) * 1e-3),
             "kernel_tbs": ob / (statistics.mean(o_kern) * 1e-3) / 1e12,
             "step_tbs": ob / (statistics.mean(o_step) * 1e-3) / 1e12,
             "frac_of_measured_hbm": ob / (statistics.mean(o_kern) * 1e-3) / 1e9 / peak_gbs,
@@ -672,7 +683,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill",
-                                       "mha", "fp8long"],
+                                       "mha", "fp8long", "int4", "nvfp4"],
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
                          "line")

@@ -88,15 +88,27 @@ constexpr int kPlanThreads = 1024;
 // ---------------------------------------------------------------------------
 // compile-time traits of the four supported (cache, q) type pairs
 // ---------------------------------------------------------------------------
-enum : int { kKindBF16 = 0, kKindF16 = 1, kKindFp8BF16 = 2, kKindFp8F16 = 3 };
+enum : int {
+  kKindBF16 = 0, kKindF16 = 1, kKindFp8BF16 = 2, kKindFp8F16 = 3,
+  // 4-bit caches (head-group decode kernel only): INT4 / NVFP4, bf16 / f16 q
+  kKindI4BF16 = 4, kKindI4F16 = 5, kKindN4BF16 = 6, kKindN4F16 = 7
+};
 
 template <int kKind>
 struct Traits {
-  static constexpr bool kFp8 = kKind >= kKindFp8BF16;
+  // 0: none, 1: INT4 per token-head, 2: NVFP4 (pages of pa.h)
+  static constexpr int k4 = kKind >= kKindN4BF16 ? 2 : kKind >= kKindI4BF16 ? 1 : 0;
+  static constexpr bool kFp8 = kKind == kKindFp8BF16 || kKind == kKindFp8F16;
   static constexpr bool kMmaBF16 = kKind == kKindBF16;  // else f16 MMA
-  static constexpr bool kQBF16 = kKind == kKindBF16 || kKind == kKindFp8BF16;
-  static constexpr int kRowBytes = kFp8 ? 128 : 256;    // head_dim 128
-  static constexpr int kPageBytes = kBS * kRowBytes;    // one (block, head)
+  static constexpr bool kQBF16 = kKind == kKindBF16 || kKind == kKindFp8BF16 ||
+                                 kKind == kKindI4BF16 || kKind == kKindN4BF16;
+  // q is widened to f16 for a quantised cache (an exact decode to f16)
+  static constexpr bool kQToF16 = kFp8 || k4 != 0;
+  static constexpr int kRowBytes = k4 ? 64 : kFp8 ? 128 : 256;  // head_dim 128
+  // one (block, head) page; a 4-bit page ends with its scales
+  static constexpr int kPageBytes = k4 == 1 ? 16 * 64 + 16 * 4
+                                    : k4 == 2 ? 16 * 64 + 16 * 8
+                                              : kBS * kRowBytes;
   static constexpr int kStageBytes = 2 * kPageBytes;    // K page + V page
   static constexpr int kStages = kFp8 ? 2 * PA_STAGES_16BIT : PA_STAGES_16BIT;
   static constexpr int kRingBytes = kStages * kStageBytes;  // 64 KiB
@@ -108,7 +120,7 @@ struct Traits {
   // orders (0,5,2,7,4,1,6,3 for FP8, 0,2,1,3,6,4,7,5 for 16-bit) the 16-byte
   // fragment reads of K and V are free of bank conflicts; the transposing
   // V reads of the decode path are two-way.
-  static constexpr uint32_t kPerm = kFp8 ? 0x36147250u : 0x57463120u;
+  static constexpr uint32_t kPerm = k4 ? 0x76543210u : kFp8 ? 0x36147250u : 0x57463120u;
   // A decode item hands page i to warp i % 4 through slot i % kStages.  The
   // ring depth must be a multiple of the consumer count so that every slot
   // always serves the same warp: otherwise a fast warp can wait one full
@@ -160,6 +172,8 @@ struct FastParams {
                       // this one start only after its own wait)
   int window;         // sliding window in keys (kNoWindow: none): a row with
                       // causal limit lim sees keys lim - window + 1 .. lim
+  const uint8_t* k4;  // 4-bit caches: [block][head][page] bytes (bulk copies)
+  const uint8_t* v4;
 };
 
 // ---------------------------------------------------------------------------
@@ -870,7 +884,7 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&a)[4], uint32_t addr) {
 // head-dim index of O^T element e of tile mt for thread (r, c)
 template <int kKind>
 __device__ __forceinline__ int narrow_col(int mt, int e, int r) {
-  if constexpr (Traits<kKind>::kFp8) {
+  if constexpr (Traits<kKind>::kFp8 || Traits<kKind>::k4) {
     return 16 * r + 2 * mt + (e >> 1);
   } else {
     return 16 * mt + r + 8 * (e >> 1);
@@ -1865,6 +1879,298 @@ merge_self_kernel(FastParams p) {
 // the TMA instructions per byte of the one-head items; used for steps of
 // <= 8-row requests whose KV head count is a multiple of kHg.
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// 4-bit caches in the head-group decode kernel
+//
+// Every INT4 and NVFP4 value is exact in f16 (a 4-bit code; an E2M1 value
+// times an E4M3 block scale), so the contraction runs on f16 MMAs with q
+// widened to f16 as for FP8 caches.  INT4 per-token scales multiply the
+// scores (K) and the probabilities (V); NVFP4 block scales multiply the
+// decoded pairs; NVFP4's per-tensor scales are folded into the score and
+// output scales.
+//
+// Head-dim order: thread (r, c) supplies dims 32c + 4s .. 32c + 4s + 3 of
+// k-step s of Q.K^T (b0 the first two, b1 the last two): the 16-byte chunk
+// c of a key's 64 code bytes.  V^T tile mt row r is head dim 16r + 2mt and
+// row r + 8 is 16r + 2mt + 1: byte mt of the code bytes 8r .. 8r + 7.
+// ---------------------------------------------------------------------------
+// Q rows of a narrow item in that order; rows >= nrows are zero.
+template <int kKind>
+__device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
+                                        int nrows, int lane,
+                                        uint32_t (&qa)[8][4], float& rscale) {
+  using Tr = Traits<kKind>;
+  const int r = lane >> 2, c = lane & 3;
+  const int G = p.group;
+  const bool valid = r < nrows;
+  uint32_t w[16];
+  if (valid) {
+    const int i = r / G, h = g * G + (r - i * G);
+    const uint4* src = reinterpret_cast<const uint4*>(
+        static_cast<const uint16_t*>(p.q) + ((int64_t)(q0 + i) * p.num_q_heads + h) * 128 +
+        32 * c);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldg(src + k);
+      w[4 * k] = v.x;
+      w[4 * k + 1] = v.y;
+      w[4 * k + 2] = v.z;
+      w[4 * k + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k] = 0u;
+  }
+  rscale = 1.f;
+  if constexpr (Tr::kQBF16) {
+    // bf16 -> f16 with a per-row power-of-two shift that keeps the row's
+    // largest |q| inside the f16 range; the shift is undone on the scores
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xFFFF0000u)));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(~0u, amax, 2));
+    int e = 0;
+    if (amax > 16384.f) e = ilogbf(amax) - 13;
+    const float down = exp2f((float)-e);
+    rscale = exp2f((float)e);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      w[k] = pack2<false>(__uint_as_float(w[k] << 16) * down,
+                          __uint_as_float(w[k] & 0xFFFF0000u) * down);
+  }
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    qa[st][0] = w[2 * st];
+    qa[st][2] = w[2 * st + 1];
+    qa[st][1] = qa[st][3] = 0u;
+  }
+}
+
+// eight 4-bit codes (one word, element 2i in the low nibble of byte i) ->
+// four f16 pairs of consecutive elements (exact)
+template <int kK4>
+__device__ __forceinline__ void decode8(uint32_t w, uint32_t (&f)[4]) {
+  if constexpr (kK4 == 1) {
+    // two's complement -> offset binary (code + 8), then 1024 + n as f16
+    // bits 0x6400 | n, minus 1032
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t y = x >> 4;
+    const __half2 off = __floats2half2_rn(1032.f, 1032.f);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      // byte b's low nibble into the low half, its high nibble (the low
+      // nibble of byte b of y) into the high half
+      const uint32_t t = (__byte_perm(x, y, (uint32_t)(b | ((4 + b) << 8))) & 0x000F000Fu) |
+                         0x64006400u;
+      __half2 hv = __hsub2(*reinterpret_cast<const __half2*>(&t), off);
+      f[b] = *reinterpret_cast<uint32_t*>(&hv);
+    }
+  } else {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(f[0]), "=r"(f[1]), "=r"(f[2]), "=r"(f[3])
+        : "r"(w));
+  }
+}
+
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                      *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// two E4M3 bytes (low byte first) -> f16 pair
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 l;\n\tcvt.u16.u32 l, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t}"
+      : "=r"(r)
+      : "r"(two));
+  return r;
+}
+
+// one 4-bit page (16 keys) of a narrow item
+template <int kKind>
+__device__ __forceinline__ void process_page_4bit(
+    uint32_t k_base, uint32_t v_base, const uint32_t (&qa)[8][4],
+    NarrowState& st, int key0, int valid_keys, bool need_mask, int lim,
+    int win, float sscale, int lane) {
+  using Tr = Traits<kKind>;
+  constexpr int K4 = Tr::k4;
+  constexpr int kCodes = 16 * 64;  // the scales follow the codes
+  const int r = lane >> 2, c = lane & 3;
+  // ---- S = Q.K^T: key nt * 8 + r, dims 32c .. 32c + 31
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+    const int t = nt * 8 + r;
+    const uint4 kc = lds128(k_base + t * 64 + c * 16);
+    const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+    uint32_t bsc[2] = {0u, 0u};
+    if constexpr (K4 == 2) {
+      // block scales of dims 32c .. 32c + 15 and 32c + 16 .. 32c + 31
+      uint32_t two;
+      asm volatile("ld.shared.u16 %0, [%1];" : "=r"(two) : "r"(k_base + kCodes + t * 8 + 2 * c));
+      const uint32_t sp = e4m3x2_to_f16x2(two);
+      bsc[0] = __byte_perm(sp, sp, 0x1010);
+      bsc[1] = __byte_perm(sp, sp, 0x3232);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t f[4];
+      decode8<K4>(kw[j], f);
+      if constexpr (K4 == 2) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f[q] = hmul2u(f[q], bsc[j >> 1]);
+      }
+      mma_acc<false, false>(s[nt], qa[2 * j], f[0], f[1]);
+      mma_acc<false, false>(s2, qa[2 * j + 1], f[2], f[3]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
+  }
+  // keys (2c, 2c + 1) of tile nt for row r: INT4 key scales on the scores
+  float ks[2][2] = {{1.f, 1.f}, {1.f, 1.f}};
+  if constexpr (K4 == 1) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      float2 v;
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(v.x), "=f"(v.y)
+                   : "r"(k_base + kCodes + 4 * (nt * 8 + 2 * c)));
+      ks[nt][0] = v.x;
+      ks[nt][1] = v.y;
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float v = s[nt][e] * (sscale * ks[nt][e]);
+      const int key = key0 + nt * 8 + 2 * c + e;
+      // keys past the sequence end (their scales may be NaN), past the
+      // causal limit or outside the window
+      if ((need_mask && (key > lim || key <= lim - win)) || nt * 8 + 2 * c + e >= valid_keys)
+        v = -INFINITY;
+      s[nt][e] = v;
+    }
+  // ---- online softmax (base 2) of query row r
+  float mx = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(~0u, mx, 2));
+  const float mnew = fmaxf(st.m, mx);
+  const float muse = mnew == -INFINITY ? 0.f : mnew;
+  const float alpha = exp2f(st.m - muse);
+  st.m = mnew;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) s[nt][e] = exp2f(s[nt][e] - muse);
+  st.l = st.l * alpha + ((s[0][0] + s[0][1]) + (s[1][0] + s[1][1]));
+  const float a_lo = __shfl_sync(~0u, alpha, 8 * c);
+  const float a_hi = __shfl_sync(~0u, alpha, 8 * c + 4);
+  if (__any_sync(~0u, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      st.o[mt][0] *= a_lo;
+      st.o[mt][1] *= a_hi;
+      st.o[mt][2] *= a_lo;
+      st.o[mt][3] *= a_hi;
+    }
+  }
+  // ---- O^T += V^T.P^T; keys 2c, 2c + 1, 8 + 2c, 9 + 2c; INT4 value scales
+  // go into P (a key past the sequence end gets P = 0 whatever its scale)
+  const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+  float pv[4] = {s[0][0], s[0][1], s[1][0], s[1][1]};
+  if constexpr (K4 == 1) {
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+      float2 v;
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                   : "=f"(v.x), "=f"(v.y)
+                   : "r"(v_base + kCodes + 4 * tk[k]));
+      pv[k] = tk[k] < valid_keys ? pv[k] * v.x : 0.f;
+      pv[k + 1] = tk[k + 1] < valid_keys ? pv[k + 1] * v.y : 0.f;
+    }
+  }
+  const uint32_t b0 = pack2<false>(pv[0], pv[1]);
+  const uint32_t b1 = pack2<false>(pv[2], pv[3]);
+  uint2 vw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(vw[k].x), "=r"(vw[k].y)
+                 : "r"(v_base + tk[k] * 64 + 8 * r));
+  }
+  uint32_t vsc[2] = {0u, 0u};  // NVFP4: block r of keys (0, 1) and (2, 3)
+  if constexpr (K4 == 2) {
+    uint32_t sb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      asm volatile("ld.shared.u8 %0, [%1];" : "=r"(sb[k]) : "r"(v_base + kCodes + tk[k] * 8 + r));
+      if (tk[k] >= valid_keys) sb[k] = 0u;  // past the end: scale 0, not NaN
+    }
+    vsc[0] = e4m3x2_to_f16x2(sb[0] | (sb[1] << 8));
+    vsc[1] = e4m3x2_to_f16x2(sb[2] | (sb[3] << 8));
+  }
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int m = mt & 3;
+    const uint32_t sel = (uint32_t)(m | (m << 4) | ((4 + m) << 8) | ((4 + m) << 12));
+    const uint32_t wa = (mt >> 2) ? vw[0].y : vw[0].x;
+    const uint32_t wb = (mt >> 2) ? vw[1].y : vw[1].x;
+    const uint32_t wc = (mt >> 2) ? vw[2].y : vw[2].x;
+    const uint32_t wd = (mt >> 2) ? vw[3].y : vw[3].x;
+    // byte mt of keys (0, 1) in bytes 0 and 2, of keys (2, 3) likewise
+    const uint32_t xab = __byte_perm(wa, wb, sel);
+    const uint32_t xcd = __byte_perm(wc, wd, sel);
+    uint32_t a[4];
+    if constexpr (K4 == 1) {
+      const uint32_t u = xab ^ 0x00880088u, v = xcd ^ 0x00880088u;
+      const __half2 off = __floats2half2_rn(1032.f, 1032.f);
+      const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
+      const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
+      uint32_t t0 = (u & 0x000F000Fu) | 0x64006400u, t1 = (u & 0x00F000F0u) | 0x64006400u;
+      uint32_t t2 = (v & 0x000F000Fu) | 0x64006400u, t3 = (v & 0x00F000F0u) | 0x64006400u;
+      __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t0), off);
+      __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&t1), sixteenth, off16);
+      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&t2), off);
+      __half2 h3 = __hfma2(*reinterpret_cast<__half2*>(&t3), sixteenth, off16);
+      a[0] = *reinterpret_cast<uint32_t*>(&h0);
+      a[1] = *reinterpret_cast<uint32_t*>(&h1);
+      a[2] = *reinterpret_cast<uint32_t*>(&h2);
+      a[3] = *reinterpret_cast<uint32_t*>(&h3);
+    } else {
+      // nibble pairs (key 0, key 1) as one byte each, then E2M1 -> f16
+      const uint32_t lo = xab & 0x000F000Fu, hi = (xab >> 4) & 0x000F000Fu;
+      const uint32_t lo2 = xcd & 0x000F000Fu, hi2 = (xcd >> 4) & 0x000F000Fu;
+      // bytes: (key 0 | key 1 << 4) low nibbles, high nibbles, then keys 2, 3
+      const uint32_t packed =
+          __byte_perm(__byte_perm(lo | (lo >> 12), hi | (hi >> 12), 0x0040),
+                      __byte_perm(lo2 | (lo2 >> 12), hi2 | (hi2 >> 12), 0x0040),
+                      0x5410);
+      uint32_t f[4];
+      decode8<2>(packed, f);
+      a[0] = hmul2u(f[0], vsc[0]);
+      a[1] = hmul2u(f[1], vsc[0]);
+      a[2] = hmul2u(f[2], vsc[1]);
+      a[3] = hmul2u(f[3], vsc[1]);
+    }
+    mma16816<false>(st.o[mt], a, b0, b1);
+  }
+}
+
 template <int kKind>
 struct HgLayout {
   using Tr = Traits<kKind>;
@@ -1895,7 +2201,12 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
   const int G = p.group;
   uint32_t qa[8][4];
   float rscale[2];
-  load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
+  if constexpr (Traits<kKind>::k4) {
+    load_q4<kKind>(p, rm.q0, g, rows, lane, qa, rscale[0]);
+    rscale[1] = rscale[0];
+  } else {
+    load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
+  }
   const int lim = rq < rows ? rm.L - rm.n + rq / G : rm.L - 1;
   int min_lim = rq < rows ? lim : INT_MAX;
   int max_lim = rq < rows ? lim : -1;
@@ -1929,8 +2240,12 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
     const int valid = min(kBS, rm.L - key0);
     const bool need_mask = key0 + kBS - 1 > min_lim || key0 <= win_edge;
     const uint32_t kb = ring + s * Ly::kStageBytes + warp * Ly::kPageBytes;
-    process_page_narrow<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
+    if constexpr (Traits<kKind>::k4)
+      process_page_4bit<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
                                valid, need_mask, lim, p.window, ss, lane);
+    else
+      process_page_narrow<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
+                                 valid, need_mask, lim, p.window, ss, lane);
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (S + s));
   }
@@ -2023,7 +2338,7 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
-    if (lane == 0) {
+    if (lane == 0 && !Tr::k4) {
       tma_prefetch_desc(&tmap_k);
       tma_prefetch_desc(&tmap_v);
     }
@@ -2078,10 +2393,17 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    kv * kHg * Ly::kPageBytes;
               if (kv == 0) mbar_arrive_expect_tx(bars + 8 * s, Ly::kStageBytes);
               __syncwarp(__activemask());
-              if constexpr (Tr::kFp8)
+              if constexpr (Tr::k4) {
+                // the group's four pages (codes and scales) are contiguous
+                const uint8_t* src =
+                    (kv ? p.v4 : p.k4) +
+                    ((int64_t)blk * p.num_kv_heads + rec0.y * kHg) * Ly::kPageBytes;
+                bulk_load(dst, src, kHg * Ly::kPageBytes, bars + 8 * s);
+              } else if constexpr (Tr::kFp8) {
                 tma_load_2d(dst, map, bars + 8 * s, 0, row);
-              else
+              } else {
                 tma_load_3d(dst, map, bars + 8 * s, 0, 0, row);
+              }
             }
             c += min(PP, cnt - jj);
           }
@@ -2375,6 +2697,9 @@ int decode_box_rows(const AttnArgs& a, bool tc) {
 
 bool fast_path_supported(const AttnArgs& a) {
   if (a.head_dim != 128) return false;
+  // 4-bit caches: decode-only steps in KV-head groups
+  if (is_4bit(a.cache_dtype))
+    return (a.q_dtype == PA_BF16 || a.q_dtype == PA_F16) && use_head_groups(a, false);
   if (a.cache_dtype == PA_BF16 && a.q_dtype == PA_BF16) return true;
   if (a.cache_dtype == PA_F16 && a.q_dtype == PA_F16) return true;
   if (a.cache_dtype == PA_FP8_E4M3 && (a.q_dtype == PA_BF16 || a.q_dtype == PA_F16))
@@ -2528,9 +2853,13 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.group = plan.group;
   fp.max_query_len = a.max_query_len;
   fp.max_seq_len = a.max_seq_len;
-  const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
+  // FP8 and NVFP4 fold their per-tensor scales into the score and output
+  // scales (INT4 has per-token scales only)
+  const bool fp8 = a.cache_dtype == PA_FP8_E4M3 || a.cache_dtype == PA_NVFP4;
   fp.score_scale = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.0f);
   fp.out_scale = fp8 ? a.v_scale : 1.0f;
+  fp.k4 = static_cast<const uint8_t*>(a.k_cache);
+  fp.v4 = static_cast<const uint8_t*>(a.v_cache);
   fp.seg_heads = 1;
   fp.window = a.window > 0 ? a.window : kNoWindow;
 
@@ -2565,10 +2894,21 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
   if (use_head_groups(a, tc != nullptr)) {
     const TcMaps* t = plan.has_prefill ? tc : nullptr;
-    switch (a.cache_dtype == PA_BF16  ? kKindBF16
-            : a.cache_dtype == PA_F16 ? kKindF16
-            : a.q_dtype == PA_BF16    ? kKindFp8BF16
-                                      : kKindFp8F16) {
+    const bool qb = a.q_dtype == PA_BF16;
+    switch (a.cache_dtype == PA_BF16   ? kKindBF16
+            : a.cache_dtype == PA_F16  ? kKindF16
+            : a.cache_dtype == PA_INT4 ? (qb ? kKindI4BF16 : kKindI4F16)
+            : a.cache_dtype == PA_NVFP4 ? (qb ? kKindN4BF16 : kKindN4F16)
+            : qb                        ? kKindFp8BF16
+                                        : kKindFp8F16) {
+      case kKindI4BF16:
+        return launch_hg<kKindI4BF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindI4F16:
+        return launch_hg<kKindI4F16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindN4BF16:
+        return launch_hg<kKindN4BF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindN4F16:
+        return launch_hg<kKindN4F16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
       case kKindBF16:
         return launch_hg<kKindBF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
       case kKindF16:

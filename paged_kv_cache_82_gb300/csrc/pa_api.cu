@@ -125,6 +125,8 @@ void count_launch() { ++t_launches; }
 
 bool encode_cache_tensor_maps(const AttnArgs& a, CUtensorMap* tk,
                               CUtensorMap* tv, int box_rows) {
+  // 4-bit pages go by untiled bulk copies: no tensor map
+  if (is_4bit(a.cache_dtype)) return true;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const int eb = elem_bytes(a.cache_dtype);
@@ -434,7 +436,7 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
     TcMaps tc;
     const bool use_tc = plan.has_prefill && tc_prefill_supported(a) &&
                         encode_prefill_tensor_maps(a, &tc);
-    CUtensorMap tk, tv;
+    CUtensorMap tk{}, tv{};
     if (!encode_cache_tensor_maps(a, &tk, &tv, decode_box_rows(a, use_tc)))
       return PA_ERR_CUDA;
     e = launch_attention_fast(a, plan, tk, tv, use_tc ? &tc : nullptr,

@@ -12,7 +12,7 @@ import torch
 import oracle
 import paged_kv_cache_82_gb300 as pa
 import workloads
-from tests._gpu_step import gpu_step
+from tests._gpu_step import gpu_step, half_ulp
 from tests.test_gpu_parity import _check_step
 
 pytestmark = pytest.mark.gpu
@@ -103,6 +103,64 @@ def test_4bit_attention(fmt, case):
     else:
         wl = _lowbit([(100, 1), (50, 9)], 8, 2, fmt, D=64)
     _check_step(wl)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("case", ["g4_bf16", "g4_f16", "g8", "two_rows",
+                                  "window", "split_long", "mha"])
+def test_4bit_head_group_decode(fmt, case):
+    """Decode-only steps whose KV heads come in groups of 4 run the
+    head-group kernel on the 4-bit pages (bulk copies, f16 MMAs)."""
+    rng = np.random.default_rng([FMTS.index(fmt), len(case)])
+    lens = [int(L) for L in rng.integers(1, 3000, size=37)] + [1, 16, 17]
+    if case == "g4_bf16":
+        wl = _lowbit([(L, 1) for L in lens], 32, 8, fmt)
+    elif case == "g4_f16":
+        wl = _lowbit([(L, 1) for L in lens], 32, 8, fmt, dtype="f16")
+    elif case == "g8":
+        wl = _lowbit([(L, 1) for L in lens], 64, 8, fmt)
+    elif case == "two_rows":       # 1 + 1 draft token at 4 heads: 8 rows
+        wl = _lowbit([(max(L, 2), 2) for L in lens], 32, 8, fmt)
+    elif case == "window":
+        wl = _lowbit([(L, 1) for L in lens], 32, 8, fmt)
+        wl.sliding_window = 300
+    elif case == "split_long":     # one segment cut by dozens of CTAs
+        wl = _lowbit([(40000, 1), (5, 1)], 32, 8, fmt)
+    else:                          # 16 KV heads, one query head each
+        wl = _lowbit([(L, 1) for L in lens[:12]], 16, 16, fmt)
+    _check_step(wl)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_4bit_decode_full_size_sampled(fmt):
+    """The Llama-3.1-8B decode batch over a 4-bit cache (the bench's
+    workload): sampled rows against the oracle's row function.  The random
+    codes give outputs near 1, so the bar includes half an ulp of the bf16
+    output (its final rounding), as for the small steps."""
+    wl = workloads.config2(cache_dtype=fmt)
+    out, kc, vc, md, flags = gpu_step(wl)
+    assert flags == 0
+    g = out.float().cpu().double().numpy()
+    rng = np.random.default_rng(11)
+    for r in rng.choice(len(wl.requests), size=10, replace=False):
+        h = int(rng.integers(0, 32))
+        row = oracle.paged_attention_row(
+            wl.q, wl.k_cache, wl.v_cache, md["block_tables"], md["seq_lens"],
+            md["query_start_loc"], int(r), 0, h, scale=wl.scale,
+            cache_dtype=fmt, k_scale=wl.k_scale, v_scale=wl.v_scale)
+        err = np.abs(g[md["query_start_loc"][r], h] - row)
+        assert (err <= 2e-3 + half_ulp(row, "bf16")).all(), float(err.max())
+
+
+def test_4bit_routing():
+    """Decode-only steps in KV-head groups take the head-group kernel plus
+    its merge (2 launches); others the generic kernel (1 launch)."""
+    n0 = pa.pa_launch_count()
+    gpu_step(_lowbit([(300, 1), (40, 1)], 32, 8, "int4", write_new=False))
+    assert pa.pa_launch_count() - n0 == 2
+    n0 = pa.pa_launch_count()
+    gpu_step(_lowbit([(300, 1), (40, 1)], 12, 6, "int4", write_new=False))
+    assert pa.pa_launch_count() - n0 == 1
 
 
 @pytest.mark.parametrize("fmt", FMTS)
