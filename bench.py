@@ -433,6 +433,8 @@ def run_ours(args):
         make = {"decode": workloads.config2, "mixed": workloads.config4,
                 "prefill": workloads.prefill_chunk, "mha": workloads.config3,
                 "fp8long": workloads.config5,
+                "prefillfp8": lambda **k: workloads.prefill_chunk(
+                    cache_dtype="e4m3", **k),
                 "int4": lambda **k: workloads.config2(cache_dtype="int4", **k),
                 "nvfp4": lambda **k: workloads.config2(cache_dtype="nvfp4",
                                                        **k)}[args.only]
@@ -574,6 +576,28 @@ def run_ours(args):
     }
     del dp
 
+    # ---- the same chunk over an FP8 cache (tiles widened to f16 on chip)
+    wlp8 = workloads.prefill_chunk(cache_dtype="e4m3")
+    dp8 = _device_inputs(wlp8, dev)
+    p8_step, p8_kern, _ = _time_steps(pa, wlp8, dp8, max(3, args.steps // 4),
+                                      args.warmup, flush)
+    flags = pa.pa_get_device_error()
+    if flags:
+        raise RuntimeError(f"device error flags 0x{flags:x} (fp8 prefill)")
+    p8_km = statistics.mean(p8_kern)
+    p8_tflops = workloads.attention_flops(wlp8) / (p8_km * 1e-3) / 1e12
+    prefill_fp8 = {
+        "workload": ("Llama-3.1-8B shape, bf16 q, FP8 E4M3 KV: one request, "
+                     "4096-token chunk after 4096 cached tokens (causal)"),
+        "kernel": ("prefill_tc_kernel (FP8 pages widened to f16 in shared "
+                   "memory, f16 tcgen05) + the empty decode launch"),
+        "bound": "tensor", "achieved": p8_tflops, "peak": bf16_peak,
+        "unit": "TFLOP/s", "frac": p8_tflops / bf16_peak,
+        "peak_kind": bf16_kind + " (f16 rate = bf16 rate)",
+        "kernels_ms": p8_km, "flops": workloads.attention_flops(wlp8),
+    }
+    del dp8
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = _cpu_baseline(wl, alg_bytes)
@@ -606,6 +630,7 @@ def run_ours(args):
         "clocks": clocks,
         "mixed_step": mixed,
         "prefill_step": prefill,
+        "prefill_step_fp8": prefill_fp8,
         "other_decodes": others,
         "cpu_baseline": cpu,
     }
@@ -683,7 +708,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill",
-                                       "mha", "fp8long", "int4", "nvfp4"],
+                                       "mha", "fp8long", "int4", "nvfp4",
+                                       "prefillfp8"],
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
                          "line")

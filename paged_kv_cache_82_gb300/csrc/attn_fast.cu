@@ -2926,9 +2926,9 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
     return launch_kind<kKindF16>(a, fp, pa, plan, tmap_k, tmap_v, tc, num_sms,
                                  stream);
   if (a.q_dtype == PA_BF16)
-    return launch_kind<kKindFp8BF16>(a, fp, pa, plan, tmap_k, tmap_v, nullptr,
+    return launch_kind<kKindFp8BF16>(a, fp, pa, plan, tmap_k, tmap_v, tc,
                                      num_sms, stream);
-  return launch_kind<kKindFp8F16>(a, fp, pa, plan, tmap_k, tmap_v, nullptr,
+  return launch_kind<kKindFp8F16>(a, fp, pa, plan, tmap_k, tmap_v, tc,
                                   num_sms, stream);
 }
 

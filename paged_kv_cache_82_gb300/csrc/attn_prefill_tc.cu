@@ -110,12 +110,22 @@ enum : int {
   kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
   kQkDone = kXchg + 4,               // every S MMA has completed
   kPvDone2 = kQkDone + 1,            // every P.V MMA has completed
-  kNumBars = kPvDone2 + 1
+  // FP8 caches: the bf16 Q tile has landed (before its widening); the two
+  // half-chunk staging buffers of E4M3 K pages, then of V pages, have landed
+  kQRaw = kPvDone2 + 1,
+  kK8Full = kQRaw + 1,
+  kV8Full = kK8Full + 2,
+  kNumBars = kV8Full + 2
 };
 
 constexpr int kSlotInts = 12;  // a tile slot: its index, then the TcTile fields
 
-struct TcLayout {
+// FP8 caches: E4M3 pages are staged half a chunk (4 pages) at a time, two
+// buffers per cache, and widened to f16 into the K / V stages
+constexpr int kHalfChunk8 = 4 * kBS * 128;  // 4 pages of 128 E4M3 bytes a row
+
+template <bool kFp8>
+struct TcLayoutT {
   static constexpr int kK = 0;                               // K stages
   static constexpr int kV = kK + kKStages * kTileBytes;      // V stages
   static constexpr int kQ = kV + kVStages * kTileBytes;      // Q tiles
@@ -128,10 +138,16 @@ struct TcLayout {
   // tile (x heads) and the tile count; block-scan scratch
   static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
   static constexpr int kScan = kPlan + 2 * kTcMaxSeqs * 4;   // int[33]
-  static constexpr int kBytes = kScan + 33 * 4;
+  // FP8: staging (1024-aligned for the swizzled TMA boxes), then the Q rows'
+  // power-of-two shifts of the two tile slots (float[2][128])
+  static constexpr int kK8 = (kScan + 33 * 4 + 1023) & ~1023;
+  static constexpr int kV8 = kK8 + (kFp8 ? 2 * kHalfChunk8 : 0);
+  static constexpr int kShift = kV8 + (kFp8 ? 2 * kHalfChunk8 : 0);
+  static constexpr int kBytes = kShift + (kFp8 ? 2 * 128 * 4 : 0);
   static constexpr int kSmemBytes = kBytes + 1024;   // + alignment slack
 };
-static_assert(TcLayout::kSmemBytes <= 227 * 1024, "shared memory budget");
+using TcLayout = TcLayoutT<false>;
+static_assert(TcLayoutT<true>::kSmemBytes <= 227 * 1024, "shared memory budget");
 // Each CTA allocates all 512 tensor-memory columns: a second CTA of this
 // kernel on the same SM would wait in its allocation.  Its shared memory
 // keeps it off (228 KB per SM).
@@ -162,7 +178,8 @@ struct TcParams {
   int num_q_heads, num_kv_heads, group;
   int max_query_len, max_seq_len;
   int tokens_per_tile;   // 128 / group
-  float score_scale;     // softmax scale * log2(e)
+  float score_scale;     // softmax scale * log2(e) (* k_scale for FP8)
+  float out_scale;       // 1, or v_scale for FP8
   int window;            // sliding window in keys (kNoWindow: none)
 };
 
@@ -293,10 +310,14 @@ __device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTil
 }
 
 // The k-th tile of a warp that does not draw tiles, from slot k % 2; the
-// index is -1 when there are no more (or on a timeout).
+// index is -1 when there are no more (or on a timeout).  shifts (FP8
+// caches, softmax warps): the slot's per-row Q shifts, of which row's is
+// copied to *shift before the slot is released.
 __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
                                            volatile int* slots, int k,
-                                           volatile int* abort_flag, TcTile& t) {
+                                           volatile int* abort_flag, TcTile& t,
+                                           const volatile float* shifts = nullptr,
+                                           int row = 0, float* shift = nullptr) {
   const int s = k & 1;
   if (!warp_wait(bars + 8 * (kTileFull + s), (k >> 1) & 1, abort_flag, p.err))
     return -1;
@@ -313,6 +334,7 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
   t.nc = sl[9];
   t.ok = sl[10] != 0;
   t.p0 = sl[11];
+  if (shifts != nullptr) *shift = shifts[s * 128 + row];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
   return li;
@@ -364,13 +386,80 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-template <bool kBF16>
+// FP8 caches: widen np (<= 4) staged E4M3 pages -- 16 rows of 128 bytes
+// each, 16-byte chunk k of row t at chunk k ^ (t & 7) as the TMA wrote it --
+// to f16 rows p0 * 16 .. of a K / V stage (two 64-column halves of 128-byte
+// rows under the same swizzle), exactly.  One warp, 16-byte units.
+__device__ __forceinline__ void widen_pages(const uint8_t* src, uint8_t* stage,
+                                            int p0, int np, int lane) {
+  for (int u = lane; u < np * kBS * 8; u += 32) {
+    const int k = u & 7, t = (u >> 3) & 15, pg = u >> 7;
+    const uint4 v = *reinterpret_cast<const uint4*>(src + pg * (kBS * 128) + t * 128 +
+                                                     ((k ^ (t & 7)) << 4));
+    uint32_t f[8];
+    e4m3x4_to_f16x2x2(v.x, f[0], f[1]);
+    e4m3x4_to_f16x2x2(v.y, f[2], f[3]);
+    e4m3x4_to_f16x2x2(v.z, f[4], f[5]);
+    e4m3x4_to_f16x2x2(v.w, f[6], f[7]);
+    const int R = (p0 + pg) * kBS + t;           // row of the stage
+    const int hh = k >> 2, j0 = 2 * (k & 3);     // column half, 16-byte chunk
+    uint8_t* row = stage + hh * kHalf + R * 128;
+    *reinterpret_cast<uint4*>(row + ((j0 ^ (R & 7)) << 4)) =
+        make_uint4(f[0], f[1], f[2], f[3]);
+    *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (R & 7)) << 4)) =
+        make_uint4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+// FP8 caches, bf16 q: widen the Q tile (128 rows of two 64-column halves)
+// to f16 in place, each row scaled by 2^-e so that its largest |q| stays
+// inside the f16 range (e = 0 unless it exceeds 2^14); 2^e goes to
+// shifts[row], for the softmax to undo on the scores.  One warp.
+__device__ __forceinline__ void widen_q(uint8_t* q, float* shifts, int lane) {
+  for (int R = lane; R < 128; R += 32) {
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(q + (j >> 3) * kHalf + R * 128 +
+                                                      (((j & 7) ^ (R & 7)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+        amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+      }
+    }
+    int e = 0;
+    if (amax > 16384.f) e = ilogbf(amax) - 13;
+    const float down = exp2f((float)-e);
+    shifts[R] = exp2f((float)e);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      uint4* a = reinterpret_cast<uint4*>(q + (j >> 3) * kHalf + R * 128 +
+                                          (((j & 7) ^ (R & 7)) << 4));
+      const uint4 v = *a;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = pack2<false>(__uint_as_float(w[i] << 16) * down,
+                            __uint_as_float(w[i] & 0xFFFF0000u) * down);
+      *a = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// kBF16: q and out are bf16 (else f16).  kFp8: the caches hold E4M3, which
+// the producer warps widen to f16; the MMAs then run in f16 (Q widened too).
+template <bool kBF16, bool kFp8>
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v,
                   const __grid_constant__ TcParams p) {
   using TOut = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
+  using Ly = TcLayoutT<kFp8>;
+  constexpr bool kMma = kBF16 && !kFp8;  // bf16 MMA operands (else f16)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -444,6 +533,70 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     }
   };
 
+  // FP8 caches: stream a tile's chunks of E4M3 pages through the two
+  // half-chunk staging buffers (8-byte barriers at bar8, bar8 + 8): the next
+  // chunk's half is in flight while this half is widened into the f16 stage.
+  // n8i / n8c: loads issued into / consumed from each buffer so far.
+  // Returns false on a timeout.
+  auto stream_fp8 = [&](const TcTile& t, const CUtensorMap* map, uint32_t stage0,
+                        int nstages, uint32_t full0, uint32_t empty0,
+                        uint8_t* stg8, uint32_t bar8, uint32_t& u, uint32_t* used,
+                        uint32_t (&n8i)[2], uint32_t (&n8c)[2]) -> bool {
+    auto half_pages = [&](int c, int h) {
+      return max(0, min(4, t.pages - c * kTcPages - 4 * h));
+    };
+    auto issue = [&](int c, int h, int rows) {
+      const int np = half_pages(c, h);
+      if (np == 0) return;
+      if (lane == 0) mbar_arrive_expect_tx(bar8 + 8 * h, (uint32_t)np * kBS * 128u);
+      __syncwarp();
+      const int pg = lane & 7;
+      if (lane < 8 && pg >= 4 * h && pg < 4 * h + np)
+        tma_load_2d(smem_u32(stg8 + h * kHalfChunk8 + (pg - 4 * h) * (kBS * 128)), map,
+                    bar8 + 8 * h, 0, rows);
+      ++n8i[h];
+    };
+    int cur = group_rows(t, 0), nxt = t.nc > 4 ? group_rows(t, 1) : 0;
+    {
+      const int r0 = chunk_rows(cur, 0);
+      issue(0, 0, r0);
+      issue(0, 1, r0);
+    }
+    for (int c = 0; c < t.nc; ++c, ++u) {
+      if (c > 0 && (c & 3) == 0) {
+        cur = nxt;
+        nxt = c + 4 < t.nc ? group_rows(t, (c >> 2) + 1) : 0;
+      }
+      const int st = u % nstages;
+      if (u >= (uint32_t)nstages &&
+          !warp_wait(empty0 + 8 * st, ((u / nstages) & 1) ^ 1, abort_flag, p.err))
+        return false;
+      const int rows_next =
+          c + 1 < t.nc ? chunk_rows(((c + 1) & 3) == 0 ? nxt : cur, c + 1) : 0;
+      uint8_t* stage = sp + (stage0 - base) + st * kTileBytes;
+      for (int h = 0; h < 2; ++h) {
+        const int np = half_pages(c, h);
+        if (np == 0) continue;
+        if (!warp_wait(bar8 + 8 * h, n8c[h] & 1, abort_flag, p.err)) return false;
+        ++n8c[h];
+        widen_pages(stg8 + h * kHalfChunk8, stage, 4 * h, np, lane);
+        __syncwarp();  // the buffer is read: the next half may land in it
+        if (c + 1 < t.nc) issue(c + 1, h, rows_next);
+      }
+      fence_proxy_async_smem();  // the stage is read by the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full0 + 8 * st);
+      ++used[st];
+    }
+    return true;
+  };
+  // copies still in flight in the staging buffers (after a timeout)
+  auto drain_fp8 = [&](uint32_t bar8, const uint32_t (&n8i)[2], const uint32_t (&n8c)[2]) {
+    if (lane == 0)
+      for (int h = 0; h < 2; ++h)
+        if (n8i[h] > n8c[h]) mbar_wait_bounded(bar8 + 8 * h, (n8i[h] - 1) & 1);
+  };
+
   if (warp == kKWarp) {
     // ------------------------- producer: tiles, Q, K -------------------------
     if (lane == 0) {
@@ -451,8 +604,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       tma_prefetch_desc(&tmap_k);
     }
     const uint32_t q_bytes = 2u * 64u * (uint32_t)G * p.tokens_per_tile * 2u;
-    uint32_t u = 0, qt = 0;
+    uint32_t u = 0, qt = 0, nq_raw = 0;
     uint32_t used[kKStages] = {};  // loads issued into each stage
+    uint32_t n8i[2] = {0u, 0u}, n8c[2] = {0u, 0u};
     const long long skip = skipped_copy();
     bool go = true;
     for (int k = 0; go; ++k) {
@@ -476,16 +630,55 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
       TcTile t{};
       if (li >= 0) t = tc_tile(p, pre, ntl, li);
+      const uint32_t qb = qt % kQStages;
+      bool q_ready = false;
+      if constexpr (kFp8) {
+        // Q first, widened to f16 (with its rows' shifts, handed over in the
+        // tile slot) before the tile is published
+        if (li >= 0 && t.ok && !aborted(abort_flag)) {
+          if (qt >= (uint32_t)kQStages &&
+              !warp_wait(bars + 8 * (kQEmpty + qb), ((qt / kQStages) - 1) & 1, abort_flag,
+                         p.err))
+            break;
+          const uint32_t qd = base + TcLayout::kQ + qb * kTileBytes;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bars + 8 * kQRaw, q_bytes);
+            tma_load_3d(qd, &tmap_q, bars + 8 * kQRaw, 0, t.g * G, t.q0 + t.i0);
+            tma_load_3d(qd + kHalf, &tmap_q, bars + 8 * kQRaw, 64, t.g * G, t.q0 + t.i0);
+          }
+          ++nq_raw;
+          if (!warp_wait(bars + 8 * kQRaw, (nq_raw - 1) & 1, abort_flag, p.err)) break;
+          float* shifts = reinterpret_cast<float*>(sp + Ly::kShift) + s * 128;
+          if constexpr (kBF16) {
+            widen_q(sp + TcLayout::kQ + qb * kTileBytes, shifts, lane);
+          } else {
+            for (int R = lane; R < 128; R += 32) shifts[R] = 1.f;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          q_ready = true;
+        }
+      }
       if (lane == 0) {
         put_tile(slots + s * kSlotInts, li, t);
         mbar_arrive(bars + 8 * (kTileFull + s));
+        if (q_ready) mbar_arrive(bars + 8 * (kQFull + qb));
       }
       __syncwarp();
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
+      if constexpr (kFp8) {
+        ++qt;
+        if (!stream_fp8(t, &tmap_k, base + TcLayout::kK, kKStages, bars + 8 * kKFull,
+                        bars + 8 * kKEmpty, sp + Ly::kK8, bars + 8 * kK8Full, u, used, n8i,
+                        n8c)) {
+          go = false;
+          break;
+        }
+        continue;
+      }
       // Q of this CTA's tile qt into buffer qt % kQStages, once the S MMAs of
       // the tile that last used it have completed
-      const uint32_t qb = qt % kQStages;
       if (qt >= (uint32_t)kQStages &&
           !warp_wait(bars + 8 * (kQEmpty + qb), ((qt / kQStages) - 1) & 1, abort_flag,
                      p.err))
@@ -521,24 +714,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       }
     }
     // let every copy this warp issued land before the CTA may exit
-    for (int st = 0; st < kKStages; ++st)
-      if (used[st] > 0)
-        mbar_wait_bounded(bars + 8 * (kKFull + st), (used[st] - 1) & 1);
-    for (uint32_t qb = 0; qb < (uint32_t)kQStages; ++qb) {
-      const uint32_t n = qt > qb ? (qt - qb + kQStages - 1) / kQStages : 0;  // loads into qb
-      if (n > 0) mbar_wait_bounded(bars + 8 * (kQFull + qb), (n - 1) & 1);
+    if constexpr (kFp8) {
+      drain_fp8(bars + 8 * kK8Full, n8i, n8c);
+      if (lane == 0 && nq_raw > 0) mbar_wait_bounded(bars + 8 * kQRaw, (nq_raw - 1) & 1);
+    } else {
+      for (int st = 0; st < kKStages; ++st)
+        if (used[st] > 0)
+          mbar_wait_bounded(bars + 8 * (kKFull + st), (used[st] - 1) & 1);
+      for (uint32_t qb = 0; qb < (uint32_t)kQStages; ++qb) {
+        const uint32_t n = qt > qb ? (qt - qb + kQStages - 1) / kQStages : 0;  // loads into qb
+        if (n > 0) mbar_wait_bounded(bars + 8 * (kQFull + qb), (n - 1) & 1);
+      }
     }
   } else if (warp == kVWarp) {
     // ----------------------------- producer: V ------------------------------
     if (lane == 0) tma_prefetch_desc(&tmap_v);
     uint32_t u = 0;
     uint32_t used[kVStages] = {};
+    uint32_t n8i[2] = {0u, 0u}, n8c[2] = {0u, 0u};
     bool go = true;
     for (int k = 0; go; ++k) {
       TcTile t;
       const int li = follow_tile(p, bars, slots, k, abort_flag, t);
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
+      if constexpr (kFp8) {
+        if (!stream_fp8(t, &tmap_v, base + TcLayout::kV, kVStages, bars + 8 * kVFull,
+                        bars + 8 * kVEmpty, sp + Ly::kV8, bars + 8 * kV8Full, u, used, n8i,
+                        n8c))
+          go = false;
+        continue;
+      }
       int cur = group_rows(t, 0), nxt = t.nc > 4 ? group_rows(t, 1) : 0;
       for (int c = 0; c < t.nc; ++c, ++u) {
         if (c > 0 && (c & 3) == 0) {
@@ -559,9 +765,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         ++used[st];
       }
     }
-    for (int st = 0; st < kVStages; ++st)
-      if (used[st] > 0)
-        mbar_wait_bounded(bars + 8 * (kVFull + st), (used[st] - 1) & 1);
+    if constexpr (kFp8) {
+      drain_fp8(bars + 8 * kV8Full, n8i, n8c);
+    } else {
+      for (int st = 0; st < kVStages; ++st)
+        if (used[st] > 0)
+          mbar_wait_bounded(bars + 8 * (kVFull + st), (used[st] - 1) & 1);
+    }
   } else if (warp == kQkWarp) {
     // ----------------------------- S = Q.K^T ------------------------------
     // The two MMA streams are issued by two warps: a tcgen05.mma keeps its
@@ -596,7 +806,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         {
           // the whole warp: one elected lane issues the group
           const int np = min(kTcPages, t.pages - c * kTcPages);
-          const uint32_t idesc = tc_idesc_f16(kBF16, false, kTcRows, np * kBS);
+          const uint32_t idesc = tc_idesc_f16(kMma, false, kTcRows, np * kBS);
           const uint32_t k_s = base + TcLayout::kK + st * kTileBytes;
           tc_mma_ss_k128<kHalf>(tmem + b * 128, tc_desc_sw128(q_s, 16, 1024),
                                 tc_desc_sw128(k_s, 16, 1024), idesc);
@@ -615,7 +825,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_wait_bounded(bars + 8 * kQkDone, 0);
   } else if (warp == kPvWarp) {
     // ------------------------------ O += P.V ------------------------------
-    const uint32_t idesc_pv = tc_idesc_f16(kBF16, true, kTcRows, 128);
+    const uint32_t idesc_pv = tc_idesc_f16(kMma, true, kTcRows, 128);
     uint32_t u = 0;
     for (int k = 0;; ++k) {
       TcTile t;
@@ -699,11 +909,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       ++xk;
       return ok;
     };
+    const volatile float* qshifts =
+        kFp8 ? reinterpret_cast<const volatile float*>(sp + Ly::kShift) : nullptr;
     for (int k = 0;; ++k) {
       TcTile t;
-      const int li = follow_tile(p, bars, slots, k, abort_flag, t);
+      float qshift = 1.f;  // FP8 caches: 2^e of this row's Q widening
+      const int li = follow_tile(p, bars, slots, k, abort_flag, t, qshifts, row, &qshift);
       if (li < 0 || aborted(abort_flag)) break;
       if (!t.ok) continue;
+      const float sscale = p.score_scale * qshift;
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
       const bool valid = it < t.ntok;
@@ -746,7 +960,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           break;
         }
         mx = fmaxf(mx, mx_other);  // the same value in both halves
-        const float m_new = fmaxf(m_ref, mx * p.score_scale);
+        const float m_new = fmaxf(m_ref, mx * sscale);
         const bool grow = m_new > m_ref + kRescaleLog2;
         const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
         if (c > 0 && __any_sync(~0u, grow)) {
@@ -778,7 +992,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         // keys of MMA step k take columns 16k .. 16k+7 (hi parts) and
         // 16k+8 .. 16k+15 (lo parts), key pairs packed low key first
         // (key pairs in packed fp32x2 arithmetic)
-        const float2 scale2 = make_float2(p.score_scale, p.score_scale);
+        const float2 scale2 = make_float2(sscale, sscale);
         // a row that has seen no key yet (a chunk wholly before its window)
         // keeps m_ref = -inf: its scores are all -inf and give P = 0
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
@@ -795,7 +1009,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
             const float2 pr = make_float2(fast_exp2(x.x), fast_exp2(x.y));
             l2[k & 1] = __fadd2_rn(l2[k & 1], pr);
             const int slot = (k >> 3) * 16 + (k & 7);  // hi at slot, lo at slot + 8
-            split_pair<kBF16>(pr, w[slot], w[slot + 8]);
+            split_pair<kMma>(pr, w[slot], w[slot + 8]);
           }
           tc_st32(t_b + j * 32, w);
         }
@@ -815,7 +1029,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                      abort_flag, p.err))
         break;
       tc_fence_after();
-      const float inv = 1.f / l_tot;
+      const float inv = p.out_scale / l_tot;
       // each thread writes 128 contiguous bytes of its row: 32-byte stores
       // when the output allows them (row starts are 256-byte multiples apart)
       const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
@@ -857,7 +1071,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   }
 }
 
-template <bool kBF16>
+template <bool kBF16, bool kFp8>
 cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
                       cudaStream_t stream);
 
@@ -873,7 +1087,7 @@ cudaError_t set_pipeline_hooks_tc(uint64_t wait_limit_ns, long long skip_copy) {
 
 namespace {
 
-template <bool kBF16>
+template <bool kBF16, bool kFp8>
 cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
                       cudaStream_t stream) {
   static bool configured[64] = {false};
@@ -882,9 +1096,9 @@ cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16>,
+    e = cudaFuncSetAttribute(prefill_tc_kernel<kBF16, kFp8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             TcLayout::kSmemBytes);
+                             TcLayoutT<kFp8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -894,11 +1108,11 @@ cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = TcLayout::kSmemBytes;
+  cfg.dynamicSmemBytes = TcLayoutT<kFp8>::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kBF16>, m.q, m.k, m.v, p);
+  e = cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kBF16, kFp8>, m.q, m.k, m.v, p);
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -908,8 +1122,10 @@ cudaError_t launch_tc(const TcParams& p, const TcMaps& m, int grid,
 bool tc_prefill_supported(const AttnArgs& a) {
   const int G = a.num_q_heads / a.num_kv_heads;
   // (the row max is taken on raw scores: the scale must be positive)
-  return a.head_dim == 128 && G >= 1 && G <= kTcRows && a.scale > 0.f &&
-         (a.cache_dtype == PA_BF16 || a.cache_dtype == PA_F16) &&
+  if (!(a.head_dim == 128 && G >= 1 && G <= kTcRows && a.scale > 0.f)) return false;
+  if (a.cache_dtype == PA_FP8_E4M3)  // widened to f16 in shared memory
+    return a.q_dtype == PA_BF16 || a.q_dtype == PA_F16;
+  return (a.cache_dtype == PA_BF16 || a.cache_dtype == PA_F16) &&
          a.q_dtype == a.cache_dtype;
 }
 
@@ -943,12 +1159,18 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
   p.max_query_len = a.max_query_len;
   p.max_seq_len = a.max_seq_len;
   p.tokens_per_tile = kTcRows / p.group;
-  p.score_scale = a.scale * 1.4426950408889634f;
+  const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
+  p.score_scale = a.scale * 1.4426950408889634f * (fp8 ? a.k_scale : 1.0f);
+  p.out_scale = fp8 ? a.v_scale : 1.0f;
   p.window = a.window > 0 ? a.window : kNoWindow;
   int grid = max_atoms < num_sms ? max_atoms : num_sms;
   if (grid < 1) grid = 1;
-  return a.cache_dtype == PA_BF16 ? launch_tc<true>(p, maps, grid, stream)
-                                  : launch_tc<false>(p, maps, grid, stream);
+  const bool qb = a.q_dtype == PA_BF16;
+  if (fp8)
+    return qb ? launch_tc<true, true>(p, maps, grid, stream)
+              : launch_tc<false, true>(p, maps, grid, stream);
+  return qb ? launch_tc<true, false>(p, maps, grid, stream)
+            : launch_tc<false, false>(p, maps, grid, stream);
 }
 
 }  // namespace pa

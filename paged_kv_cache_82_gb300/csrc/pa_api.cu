@@ -185,15 +185,18 @@ bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* m) {
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
   }
-  // caches [row][128]: a box is 64 columns of one 16-row page
+  // caches [row][128]: a box is 64 columns of one 16-row page; FP8 caches
+  // [row][128 bytes]: a box is one whole page (widened in shared memory)
   const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.num_kv_heads * PA_BLOCK_SIZE;
   const void* ptrs[2] = {a.k_cache, a.v_cache};
   CUtensorMap* maps[2] = {&m->k, &m->v};
+  const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
   for (int k = 0; k < 2; ++k) {
     cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, PA_BLOCK_SIZE};
-    if (fn(maps[k], dt, 2, const_cast<void*>(ptrs[k]), dims, strides, box, es,
+    cuuint64_t strides[1] = {fp8 ? 128u : 256u};
+    cuuint32_t box[2] = {fp8 ? 128u : 64u, PA_BLOCK_SIZE};
+    if (fn(maps[k], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : dt, 2,
+           const_cast<void*>(ptrs[k]), dims, strides, box, es,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

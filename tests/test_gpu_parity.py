@@ -220,6 +220,33 @@ def test_prefill_tiles(Hq, Hkv, seq_q, dtype):
     _check_step(_custom(seq_q, Hq, Hkv, dtype=dtype, write_new=True))
 
 
+@pytest.mark.parametrize("Hq,Hkv,seq_q,dtype", [
+    (12, 4, [(1500, 300), (200, 1)], "bf16"),   # group 3: 126-row tiles
+    (32, 8, [(3022, 1022), (90, 1)], "bf16"),   # a 1022-token chunk
+    (8, 8, [(900, 257)], "f16"),                # MHA, f16 q
+    (64, 4, [(650, 90), (77, 77)], "bf16"),     # group 16: 8-token tiles
+    (24, 6, [(700, 300), (40, 2), (64, 1)], "bf16"),  # no head groups
+])
+def test_prefill_tiles_fp8_cache(Hq, Hkv, seq_q, dtype):
+    # FP8 caches: the tiles' E4M3 pages are widened to f16 in shared memory
+    # and run on the tensor cores with Q widened to f16
+    _check_step(_custom(seq_q, Hq, Hkv, dtype=dtype, cache_dtype="e4m3",
+                        write_new=True))
+
+
+def test_prefill_tiles_fp8_cache_large_queries():
+    # bf16 queries beyond the f16 range: their rows are shifted by a power of
+    # two when widened, and the shift is undone on the scores
+    wl = _custom([(1200, 400), (300, 1)], 32, 8, cache_dtype="e4m3",
+                 write_new=True)
+    big = torch.ones(wl.q.shape[0], 32, 1)
+    big[::3] = 3.0e5
+    big[1::7] = 7.0e4
+    wl.q = (wl.q.float() * big).to(torch.bfloat16)
+    wl.scale = wl.scale / 3.0e5
+    _check_step(wl)
+
+
 @pytest.mark.parametrize("cache_dtype,dtype", [("bf16", "bf16"), ("f16", "f16")])
 def test_mixed_step_routing_by_rows(cache_dtype, dtype):
     # KV heads a multiple of 4 with a long prefill: requests of <= 8 rows run
@@ -300,9 +327,17 @@ def test_launches_per_step_kind():
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (100, 64)], 32, 8, write_new=True))
     assert pa.pa_launch_count() - n0 == 5
-    # FP8 cache with prefill tiles: planner, attention kernel, merge
+    # FP8 cache with prefill tiles: the same five launches, the tiles on the
+    # tensor cores (E4M3 pages widened to f16 in shared memory)
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (100, 64)], 32, 8, cache_dtype="e4m3",
+                     write_new=True))
+    assert pa.pa_launch_count() - n0 == 5
+    # FP8 cache, 6 KV heads (no head groups): the write, the prefill tiles
+    # on the tensor cores, the one-head attention kernel, the merge (both
+    # attention kernels plan themselves)
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 1), (100, 64)], 24, 6, cache_dtype="e4m3",
                      write_new=True))
     assert pa.pa_launch_count() - n0 == 4
 

@@ -460,17 +460,23 @@ def config5(batch: int = 16, lo: int = 32768, hi: int = 131072,
                                     "FP8 E4M3 KV"))
 
 
-def prefill_chunk(ctx: int = 4096, new: int = 4096) -> Workload:
+def prefill_chunk(ctx: int = 4096, new: int = 4096,
+                  cache_dtype: str = "bf16") -> Workload:
     """One chunked prefill, Llama-3.1-8B shape (32q/8kv heads, head_dim 128,
-    bf16): `new` prompt tokens after `ctx` cached ones, already in the cache
-    (the step attends only).  Used to measure the prefill tiles alone."""
+    bf16 q): `new` prompt tokens after `ctx` cached ones, already in the cache
+    (the step attends only).  Used to measure the prefill tiles alone.  With
+    cache_dtype "e4m3" the cache is FP8 (scales 0.0125 / 0.015)."""
     seed = 82006
     L = ctx + new
+    fp8 = cache_dtype == "e4m3"
     return decode_step("prefill_chunk_llama31_8b", seed, seq_lens=[L],
                        q_lens=[new], num_q_heads=32, num_kv_heads=8,
                        head_dim=128, num_blocks=_blocks_for(L) + 8,
-                       dtype="bf16", cache_dtype="bf16", write_new=False,
-                       description=f"1 prefill chunk: {new} new after {ctx}")
+                       dtype="bf16", cache_dtype=cache_dtype, write_new=False,
+                       k_scale=0.0125 if fp8 else 1.0,
+                       v_scale=0.015 if fp8 else 1.0,
+                       description=(f"1 prefill chunk: {new} new after {ctx}, "
+                                    f"{cache_dtype} KV"))
 
 
 def attention_flops(wl: Workload) -> int:
