@@ -392,22 +392,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // rows under the same swizzle), exactly.  One warp, 16-byte units.
 __device__ __forceinline__ void widen_pages(const uint8_t* src, uint8_t* stage,
                                             int p0, int np, int lane) {
-  for (int u = lane; u < np * kBS * 8; u += 32) {
-    const int k = u & 7, t = (u >> 3) & 15, pg = u >> 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(src + pg * (kBS * 128) + t * 128 +
-                                                     ((k ^ (t & 7)) << 4));
-    uint32_t f[8];
-    e4m3x4_to_f16x2x2(v.x, f[0], f[1]);
-    e4m3x4_to_f16x2x2(v.y, f[2], f[3]);
-    e4m3x4_to_f16x2x2(v.z, f[4], f[5]);
-    e4m3x4_to_f16x2x2(v.w, f[6], f[7]);
-    const int R = (p0 + pg) * kBS + t;           // row of the stage
-    const int hh = k >> 2, j0 = 2 * (k & 3);     // column half, 16-byte chunk
-    uint8_t* row = stage + hh * kHalf + R * 128;
-    *reinterpret_cast<uint4*>(row + ((j0 ^ (R & 7)) << 4)) =
-        make_uint4(f[0], f[1], f[2], f[3]);
-    *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (R & 7)) << 4)) =
-        make_uint4(f[4], f[5], f[6], f[7]);
+  // lane: 16-byte chunk k = lane & 7 of rows t = lane / 8 + 4 i of each page;
+  // the chunk's column half and its f16 chunks are the same in every row
+  const int k = lane & 7, t0 = lane >> 3;
+  const int hh = k >> 2, j0 = 2 * (k & 3);
+  const uint8_t* s0 = src + t0 * 128;
+  uint8_t* d0 = stage + hh * kHalf + (p0 * kBS + t0) * 128;
+  for (int pg = 0; pg < np; ++pg) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + 4 * i;  // row in the page; (p0 + pg) * 16 + t in the stage
+      const uint4 v = *reinterpret_cast<const uint4*>(s0 + pg * (kBS * 128) + i * 512 +
+                                                       ((k ^ (t & 7)) << 4));
+      uint32_t f[8];
+      e4m3x4_to_f16x2x2(v.x, f[0], f[1]);
+      e4m3x4_to_f16x2x2(v.y, f[2], f[3]);
+      e4m3x4_to_f16x2x2(v.z, f[4], f[5]);
+      e4m3x4_to_f16x2x2(v.w, f[6], f[7]);
+      uint8_t* row = d0 + pg * (kBS * 128) + i * 512;
+      *reinterpret_cast<uint4*>(row + ((j0 ^ (t & 7)) << 4)) =
+          make_uint4(f[0], f[1], f[2], f[3]);
+      *reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (t & 7)) << 4)) =
+          make_uint4(f[4], f[5], f[6], f[7]);
+    }
   }
 }
 
