@@ -402,6 +402,61 @@ def _kernel_hash():
     return h.hexdigest()
 
 
+def _cache_ops(pa, dev, flush, steps, warmup, peak_gbs):
+    """HBM rate of pa_reshape_and_cache and pa_copy_blocks on their own:
+    algorithmic bytes (every element read once and written once) over the
+    device time of one call, the L2 flushed before each."""
+    import torch
+    T, Hkv, D, NB = 32768, 8, 128, 2 * 32768 // 16 + 8192
+    gen = torch.Generator(device="cpu").manual_seed(82007)
+    key = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(dev)
+    value = torch.randn(T, Hkv, D, generator=gen).to(torch.bfloat16).to(dev)
+    slots = torch.randperm(NB * 16, generator=gen)[:T].to(dev)
+    res = {}
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(steps):
+            flush.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for name, cdt, eb in (("reshape_and_cache_bf16", "bf16", 2),
+                          ("reshape_and_cache_bf16_to_fp8", "e4m3", 1)):
+        tdt = torch.bfloat16 if cdt == "bf16" else torch.uint8
+        kc = torch.zeros(NB, Hkv, 16, D, dtype=tdt, device=dev)
+        vc = torch.zeros_like(kc)
+        ms = timed(lambda: pa.pa_reshape_and_cache(
+            key, value, kc, vc, slots, k_scale=0.0125, v_scale=0.015,
+            cache_dtype=cdt))
+        byts = 2 * T * Hkv * D * (2 + eb)
+        res[name] = {"tokens": T, "bytes": byts, "ms": ms,
+                     "tbs": byts / (ms * 1e-3) / 1e12,
+                     "frac_of_measured_hbm": byts / (ms * 1e-3) / 1e9 / peak_gbs}
+        del kc, vc
+    kc = torch.zeros(NB, Hkv, 16, D, dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    perm = torch.randperm(NB, generator=gen)
+    pairs = torch.stack([perm[:4096], perm[4096:8192]], 1).to(dev)
+    ms = timed(lambda: pa.pa_copy_blocks(kc, vc, pairs))
+    byts = 2 * 2 * 4096 * Hkv * 16 * D * 2
+    res["copy_blocks_bf16"] = {"pairs": 4096, "bytes": byts, "ms": ms,
+                               "tbs": byts / (ms * 1e-3) / 1e12,
+                               "frac_of_measured_hbm":
+                                   byts / (ms * 1e-3) / 1e9 / peak_gbs}
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error flags (cache ops)")
+    return res
+
+
 def _headline_config(wl, ws):
     """The `config` object of the headline line, identical in both arms: the
     workload and its sizes (the reference arm attends a bounded sample of it,
@@ -527,7 +582,9 @@ def run_ours(args):
                        ("int4_decode_llama31_8b",
                         lambda: workloads.config2(cache_dtype="int4")),
                        ("nvfp4_decode_llama31_8b",
-                        lambda: workloads.config2(cache_dtype="nvfp4"))):
+                        lambda: workloads.config2(cache_dtype="nvfp4")),
+                       ("bf16_head_dim_64_decode",
+                        lambda: workloads.config2(head_dim=64))):
         wlo = make()
         do = _device_inputs(wlo, dev)
         o_step, o_kern, _ = _time_steps(pa, wlo, do, max(3, args.steps // 10),
@@ -546,6 +603,12 @@ def run_ours(args):
             "frac_of_measured_hbm": ob / (statistics.mean(o_kern) * 1e-3) / 1e9 / peak_gbs,
         }
         del do, wlo
+
+    # ---- the cache kernels alone at a size that fills the GPU: the K/V
+    # writes of a 32,768-token prefill (bf16 -> bf16, and bf16 -> FP8) and
+    # copy-on-write copies of 4,096 blocks (Llama-3.1-8B shape)
+    cache_ops = _cache_ops(pa, dev, flush, max(3, args.steps // 10),
+                           args.warmup, peak_gbs)
 
     # ---- prefill tiles alone: one long chunked prefill (tensor cores)
     wlp = workloads.prefill_chunk()
@@ -632,6 +695,7 @@ def run_ours(args):
         "prefill_step": prefill,
         "prefill_step_fp8": prefill_fp8,
         "other_decodes": others,
+        "cache_ops": cache_ops,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -91,20 +91,29 @@ constexpr int kPlanThreads = 1024;
 enum : int {
   kKindBF16 = 0, kKindF16 = 1, kKindFp8BF16 = 2, kKindFp8F16 = 3,
   // 4-bit caches (head-group decode kernel only): INT4 / NVFP4, bf16 / f16 q
-  kKindI4BF16 = 4, kKindI4F16 = 5, kKindN4BF16 = 6, kKindN4F16 = 7
+  kKindI4BF16 = 4, kKindI4F16 = 5, kKindN4BF16 = 6, kKindN4F16 = 7,
+  // head_dim 64, bf16 / f16 (head-group decode kernel only)
+  kKindBF16D64 = 8, kKindF16D64 = 9
 };
 
 template <int kKind>
 struct Traits {
   // 0: none, 1: INT4 per token-head, 2: NVFP4 (pages of pa.h)
-  static constexpr int k4 = kKind >= kKindN4BF16 ? 2 : kKind >= kKindI4BF16 ? 1 : 0;
+  static constexpr int k4 = kKind == kKindN4BF16 || kKind == kKindN4F16   ? 2
+                          : kKind == kKindI4BF16 || kKind == kKindI4F16 ? 1
+                                                                        : 0;
   static constexpr bool kFp8 = kKind == kKindFp8BF16 || kKind == kKindFp8F16;
-  static constexpr bool kMmaBF16 = kKind == kKindBF16;  // else f16 MMA
+  static constexpr int kD = kKind >= kKindBF16D64 ? 64 : 128;  // head_dim
+  static constexpr bool kMmaBF16 = kKind == kKindBF16 || kKind == kKindBF16D64;
   static constexpr bool kQBF16 = kKind == kKindBF16 || kKind == kKindFp8BF16 ||
-                                 kKind == kKindI4BF16 || kKind == kKindN4BF16;
+                                 kKind == kKindI4BF16 || kKind == kKindN4BF16 ||
+                                 kKind == kKindBF16D64;
+  // a page's rows are one 128-byte segment (FP8 at head_dim 128, 16-bit at
+  // head_dim 64): 2-D TMA boxes, the 128-byte-row token order below
+  static constexpr bool kRows128 = kFp8 || kD == 64;
   // q is widened to f16 for a quantised cache (an exact decode to f16)
   static constexpr bool kQToF16 = kFp8 || k4 != 0;
-  static constexpr int kRowBytes = k4 ? 64 : kFp8 ? 128 : 256;  // head_dim 128
+  static constexpr int kRowBytes = k4 ? 64 : kRows128 ? 128 : 256;
   // one (block, head) page; a 4-bit page ends with its scales
   static constexpr int kPageBytes = k4 == 1 ? 16 * 64 + 16 * 4
                                     : k4 == 2 ? 16 * 64 + 16 * 8
@@ -120,7 +129,9 @@ struct Traits {
   // orders (0,5,2,7,4,1,6,3 for FP8, 0,2,1,3,6,4,7,5 for 16-bit) the 16-byte
   // fragment reads of K and V are free of bank conflicts; the transposing
   // V reads of the decode path are two-way.
-  static constexpr uint32_t kPerm = k4 ? 0x76543210u : kFp8 ? 0x36147250u : 0x57463120u;
+  static constexpr uint32_t kPerm = k4         ? 0x76543210u
+                                    : kRows128 ? 0x36147250u
+                                               : 0x57463120u;
   // A decode item hands page i to warp i % 4 through slot i % kStages.  The
   // ring depth must be a multiple of the consumer count so that every slot
   // always serves the same warp: otherwise a fast warp can wait one full
@@ -174,6 +185,7 @@ struct FastParams {
                       // causal limit lim sees keys lim - window + 1 .. lim
   const uint8_t* k4;  // 4-bit caches: [block][head][page] bytes (bulk copies)
   const uint8_t* v4;
+  int head_dim;       // 128, or 64 (16-bit caches, head-group decode kernel)
 };
 
 // ---------------------------------------------------------------------------
@@ -578,17 +590,18 @@ __device__ __forceinline__ void load_q(const FastParams& p, int q0, int g,
       const int h = g * G + (R - i * G);
       src = reinterpret_cast<const uint4*>(
           static_cast<const uint16_t*>(p.q) +
-          ((int64_t)(q0 + i) * Hq + h) * 128);
+          ((int64_t)(q0 + i) * Hq + h) * Tr::kD);
     }
     uint4 ch[4];
     if constexpr (!Tr::kFp8) {
       // 16-bit cache: chunk 4j + c of the row (8 elements) feeds k-steps
       // 2j and 2j+1
+      constexpr int kJ = Tr::kD / 32;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < kJ; ++j)
         ch[j] = valid ? __ldg(src + 4 * j + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kJ; ++j) {
         qa[2 * j][half] = ch[j].x;
         qa[2 * j][2 + half] = ch[j].y;
         qa[2 * j + 1][half] = ch[j].z;
@@ -668,7 +681,16 @@ __device__ __forceinline__ void qk_page(uint32_t k_base,
 #pragma unroll
     for (int e = 0; e < 4; ++e) s[nt][e] = s2[nt][e] = 0.f;
     const int t = nt * 8 + perm_of(P, r);
-    if constexpr (!Tr::kFp8) {
+    if constexpr (!Tr::kFp8 && Tr::kD == 64) {
+      // 128-byte rows: chunk u of token t at u ^ (t & 7)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int u = (j << 2) | c;
+        const uint4 kv = lds128(k_base + t * 128 + ((u ^ (t & 7)) << 4));
+        mma_acc<kB, kRows16>(s[nt], qa[2 * j], kv.x, kv.y);
+        mma_acc<kB, kRows16>(s2[nt], qa[2 * j + 1], kv.z, kv.w);
+      }
+    } else if constexpr (!Tr::kFp8) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int dhi = j >> 1;
@@ -933,7 +955,7 @@ __device__ __forceinline__ void process_page_narrow(
   const float a_hi = __shfl_sync(~0u, alpha, 8 * c + 4);
   if (__any_sync(~0u, a_lo != 1.f || a_hi != 1.f)) {
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < Tr::kD / 16; ++mt) {
       st.o[mt][0] *= a_lo;
       st.o[mt][1] *= a_hi;
       st.o[mt][2] *= a_lo;
@@ -961,10 +983,11 @@ __device__ __forceinline__ void process_page_narrow(
     // chunk 2 * (mt & 3) + (g & 1) of segment mt >> 2
     const int g8 = lane >> 3, i8 = lane & 7;
     const int tok = ((g8 >> 1) << 3) + perm_of(P, i8);
-    const uint32_t row = v_base + tok * 256;
-    const int tx = (tok << 1) & 7, gb = g8 & 1;
+    constexpr int kRowB = Tr::kD == 64 ? 128 : 256;  // bytes of a token's row
+    const uint32_t row = v_base + tok * kRowB;
+    const int tx = Tr::kD == 64 ? (tok & 7) : ((tok << 1) & 7), gb = g8 & 1;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
+    for (int mt = 0; mt < Tr::kD / 16; ++mt) {
       uint32_t a[4];
       const int ch = 2 * (mt & 3) + gb;
       const int dhi = mt >> 2;
@@ -1772,6 +1795,8 @@ merge_self_kernel(FastParams p) {
     const int sh = p.seg_heads;
     const int part_rows = sh == 1 ? 16 : kHgPartRows;
     const int total = sh * rows[r];
+    const int D = p.head_dim;
+    const bool act = 4 * lane < D;  // lanes holding 4 of the row's D columns
     for (int x = (b - b0) * nwarps + (threadIdx.x >> 5); x < total;
          x += (b1 - b0) * nwarps) {
       const int w = x / rows[r], rr = x - w * rows[r];
@@ -1794,9 +1819,9 @@ merge_self_kernel(FastParams p) {
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           vpre[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (s < np) {
+          if (s < np && act) {
             const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-            vpre[s] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+            vpre[s] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane);
           }
         }
         float ms = -INFINITY, ls = 0.f;
@@ -1827,7 +1852,8 @@ merge_self_kernel(FastParams p) {
         for (int s = 4; s < np; ++s) {
           const float wgt = __shfl_sync(~0u, w, s);
           const int64_t pr = pr_head + (s - 1) * pr_step;
-          const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+          const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
           acc[0] += wgt * v.x;
           acc[1] += wgt * v.y;
           acc[2] += wgt * v.z;
@@ -1853,7 +1879,8 @@ merge_self_kernel(FastParams p) {
         for (int s = 0; s < np; ++s) {
           const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
           const float ms = __ldg(p.ws_ml + pr * 2);
-          const float4 v = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * 128) + lane);
+          const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
           const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
           acc[0] += wgt * v.x;
           acc[1] += wgt * v.y;
@@ -1862,9 +1889,11 @@ merge_self_kernel(FastParams p) {
         }
       }
       const float inv = p.out_scale / den;
-      TOut* o = static_cast<TOut*>(p.out) + row * 128 + 4 * lane;
+      TOut* o = static_cast<TOut*>(p.out) + row * D + 4 * lane;
+      if (act) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+        for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+      }
     }
   }  // boundaries
 }
@@ -2259,8 +2288,9 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
     lq[h] = __shfl_sync(~0u, st.l, (2 * c + h) * 4);
   }
   const int Hq = p.num_q_heads;
+  constexpr int kD = Traits<kKind>::kD;
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
+  for (int mt = 0; mt < kD / 16; ++mt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int qrow = 2 * c + (e & 1);
@@ -2270,11 +2300,11 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
         const int i = qrow / G;
         const int h = g * G + (qrow - i * G);
         const int64_t orow = (int64_t)(rm.q0 + i) * Hq + h;
-        store_out<OutT<kKind>>(p.out, orow * 128 + col,
+        store_out<OutT<kKind>>(p.out, orow * kD + col,
                                st.o[mt][e] / lq[e & 1] * p.out_scale);
       } else {
         const int64_t pr = (int64_t)slot * kHgPartRows + warp * 8 + qrow;
-        p.ws_acc[pr * 128 + col] = st.o[mt][e];
+        p.ws_acc[pr * kD + col] = st.o[mt][e];
         if (mt == 0 && (e >> 1) == 0 && rq == 0) {
           p.ws_ml[pr * 2 + 0] = mq[e & 1];
           p.ws_ml[pr * 2 + 1] = lq[e & 1];
@@ -2399,7 +2429,7 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     (kv ? p.v4 : p.k4) +
                     ((int64_t)blk * p.num_kv_heads + rec0.y * kHg) * Ly::kPageBytes;
                 bulk_load(dst, src, kHg * Ly::kPageBytes, bars + 8 * s);
-              } else if constexpr (Tr::kFp8) {
+              } else if constexpr (Tr::kRows128) {
                 tma_load_2d(dst, map, bars + 8 * s, 0, row);
               } else {
                 tma_load_3d(dst, map, bars + 8 * s, 0, 0, row);
@@ -2696,6 +2726,10 @@ int decode_box_rows(const AttnArgs& a, bool tc) {
 }
 
 bool fast_path_supported(const AttnArgs& a) {
+  // head_dim 64, bf16 / f16: decode-only steps in KV-head groups
+  if (a.head_dim == 64)
+    return (a.cache_dtype == PA_BF16 || a.cache_dtype == PA_F16) &&
+           a.q_dtype == a.cache_dtype && use_head_groups(a, false);
   if (a.head_dim != 128) return false;
   // 4-bit caches: decode-only steps in KV-head groups
   if (is_4bit(a.cache_dtype))
@@ -2860,6 +2894,7 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   fp.out_scale = fp8 ? a.v_scale : 1.0f;
   fp.k4 = static_cast<const uint8_t*>(a.k_cache);
   fp.v4 = static_cast<const uint8_t*>(a.v_cache);
+  fp.head_dim = a.head_dim;
   fp.seg_heads = 1;
   fp.window = a.window > 0 ? a.window : kNoWindow;
 
@@ -2895,12 +2930,17 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   if (use_head_groups(a, tc != nullptr)) {
     const TcMaps* t = plan.has_prefill ? tc : nullptr;
     const bool qb = a.q_dtype == PA_BF16;
-    switch (a.cache_dtype == PA_BF16   ? kKindBF16
-            : a.cache_dtype == PA_F16  ? kKindF16
+    const bool d64 = a.head_dim == 64;
+    switch (a.cache_dtype == PA_BF16   ? (d64 ? kKindBF16D64 : kKindBF16)
+            : a.cache_dtype == PA_F16  ? (d64 ? kKindF16D64 : kKindF16)
             : a.cache_dtype == PA_INT4 ? (qb ? kKindI4BF16 : kKindI4F16)
             : a.cache_dtype == PA_NVFP4 ? (qb ? kKindN4BF16 : kKindN4F16)
             : qb                        ? kKindFp8BF16
                                         : kKindFp8F16) {
+      case kKindBF16D64:
+        return launch_hg<kKindBF16D64>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
+      case kKindF16D64:
+        return launch_hg<kKindF16D64>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
       case kKindI4BF16:
         return launch_hg<kKindI4BF16>(a, fp, plan, tmap_k, tmap_v, t, num_sms, stream);
       case kKindI4F16:

@@ -280,6 +280,36 @@ def test_f16_and_fp8_f16_query():
                         cache_dtype="e4m3", write_new=True))
 
 
+@pytest.mark.parametrize("case", ["g4_bf16", "g4_f16", "g8", "two_rows",
+                                  "split_long", "window", "mha"])
+def test_head_dim_64_head_group_decode(case):
+    """head_dim 64, bf16 / f16, decode-only steps with KV heads in groups of
+    4: the head-group kernel on 128-byte page rows."""
+    rng = np.random.default_rng(len(case))
+    lens = [int(L) for L in rng.integers(1, 3000, size=37)] + [1, 16, 17]
+    if case == "g4_bf16":
+        wl = _custom([(L, 1) for L in lens], 32, 8, D=64)
+    elif case == "g4_f16":
+        wl = _custom([(L, 1) for L in lens], 16, 4, D=64, dtype="f16")
+    elif case == "g8":
+        wl = _custom([(L, 1) for L in lens], 64, 8, D=64)
+    elif case == "two_rows":
+        wl = _custom([(max(L, 2), 2) for L in lens], 32, 8, D=64,
+                     write_new=True)
+    elif case == "split_long":
+        wl = _custom([(40000, 1), (5, 1)], 32, 8, D=64, write_new=True)
+    elif case == "window":
+        wl = _custom([(L, 1) for L in lens], 32, 8, D=64)
+        wl.sliding_window = 100
+    else:
+        wl = _custom([(L, 1) for L in lens[:12]], 16, 16, D=64)
+    _check_step(wl)
+    # the head-group kernel and its merge
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 1), (40, 1)], 32, 8, D=64))
+    assert pa.pa_launch_count() - n0 == 2
+
+
 def test_head_dim_64_and_fp32_generic_path():
     _check_step(_custom([(100, 1), (50, 9)], 8, 2, D=64, write_new=True))
     _check_step(_custom([(100, 1), (50, 9)], 8, 2, D=64, dtype="f32",

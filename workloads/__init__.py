@@ -359,7 +359,8 @@ def config1() -> Workload:
 
 
 def config2(batch: int = 64, lo: int = 512, hi: int = 4096,
-            num_blocks: int = 20000, cache_dtype: str = "bf16") -> Workload:
+            num_blocks: int = 20000, cache_dtype: str = "bf16",
+            head_dim: int = 128) -> Workload:
     """Llama-3.1-8B-shaped decode: 32q/8kv heads, head_dim 128, bf16, batch
     64, context uniform in [512, 4096], 20,000-block permuted pool.  With
     cache_dtype "int4" / "nvfp4" the same batch over a 4-bit cache (NVFP4
@@ -369,12 +370,12 @@ def config2(batch: int = 64, lo: int = 512, hi: int = 4096,
     lens = rng.integers(lo, hi, size=batch, endpoint=True).tolist()
     nv = cache_dtype == "nvfp4"
     return decode_step("cfg2_llama31_8b_decode", seed, seq_lens=lens,
-                       num_q_heads=32, num_kv_heads=8, head_dim=128,
+                       num_q_heads=32, num_kv_heads=8, head_dim=head_dim,
                        num_blocks=num_blocks, dtype="bf16",
                        cache_dtype=cache_dtype,
                        k_scale=0.5 if nv else 1.0, v_scale=0.25 if nv else 1.0,
                        description=(f"{batch} decodes, L~U[{lo},{hi}], "
-                                    f"{cache_dtype} KV"))
+                                    f"{cache_dtype} KV, head_dim {head_dim}"))
 
 
 def config3(batch: int = 32, seq_len: int = 8192,
