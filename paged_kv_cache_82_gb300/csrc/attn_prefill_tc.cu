@@ -392,10 +392,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // rows under the same swizzle), exactly.  One warp, 16-byte units.
 __device__ __forceinline__ void widen_pages(const uint8_t* src, uint8_t* stage,
                                             int p0, int np, int lane) {
-  // lane: 16-byte chunk k = lane & 7 of rows t = lane / 8 + 4 i of each page;
-  // the chunk's column half and its f16 chunks are the same in every row
-  const int k = lane & 7, t0 = lane >> 3;
+  // lane: 16-byte chunk k = lane & 7 of rows t = t0 + 4 i of each page;
+  // the chunk's column half and its f16 chunks are the same in every row.
+  // The upper-half lanes take row t ^ 1: the two halves lie 16 KB apart (the
+  // same banks), and the swizzle of the neighbouring row puts the 8 lanes of
+  // each quarter-warp on 8 different bank groups, for the loads and for both
+  // stores (otherwise every store costs two wavefronts per quarter-warp)
+  const int k = lane & 7;
   const int hh = k >> 2, j0 = 2 * (k & 3);
+  const int t0 = (lane >> 3) ^ hh;
   const uint8_t* s0 = src + t0 * 128;
   uint8_t* d0 = stage + hh * kHalf + (p0 * kBS + t0) * 128;
   for (int pg = 0; pg < np; ++pg) {
