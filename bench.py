@@ -172,9 +172,14 @@ def _device_inputs(wl, dev):
         d["pairs"] = torch.tensor(wl.copy_pairs, dtype=torch.int64, device=dev)
     d["out"] = torch.empty_like(d["q"])
     import paged_kv_cache_82_gb300 as pa
-    nbytes = pa.pa_attention_workspace_size(
-        wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-        len(wl.requests), md["max_query_len"], md["max_seq_len"])
+    from paged_kv_cache_82_gb300.metadata import common_prefix_blocks
+    # a step whose requests share leading blocks runs as a cascade (the
+    # engine knows the shared prefix from its block manager)
+    d["casc"] = common_prefix_blocks(wl.requests)
+    size_fn = (pa.pa_attention_cascade_workspace_size if d["casc"] > 0
+               else pa.pa_attention_workspace_size)
+    nbytes = size_fn(wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+                     len(wl.requests), md["max_query_len"], md["max_seq_len"])
     d["ws"] = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     return d
 
@@ -192,10 +197,16 @@ def _step(pa, wl, d):
                                 d["slots"], k_scale=wl.k_scale,
                                 v_scale=wl.v_scale, cache_dtype=cdt)
     md = d["md"]
-    pa.pa_attention(d["q"], d["kc"], d["vc"], d["bt"], d["sl"], d["qsl"],
-                    md["max_query_len"], md["max_seq_len"], wl.scale,
-                    wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"],
-                    cache_dtype=cdt)
+    if d.get("casc", 0) > 0:
+        pa.pa_attention_cascade(d["q"], d["kc"], d["vc"], d["bt"], d["sl"],
+                                d["qsl"], md["max_query_len"], md["max_seq_len"],
+                                wl.scale, d["casc"], wl.k_scale, wl.v_scale,
+                                out=d["out"], workspace=d["ws"], cache_dtype=cdt)
+    else:
+        pa.pa_attention(d["q"], d["kc"], d["vc"], d["bt"], d["sl"], d["qsl"],
+                        md["max_query_len"], md["max_seq_len"], wl.scale,
+                        wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"],
+                        cache_dtype=cdt)
     return pa.pa_launch_count() - n0
 
 

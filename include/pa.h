@@ -298,6 +298,60 @@ pa_status pa_attention_window_workspace_size(int64_t num_tokens,
                                              int sliding_window, size_t* bytes);
 
 /*
+ * pa_attention_cascade -- pa_attention for a step whose requests all begin
+ * with the same cached blocks (a shared prefix).
+ *
+ * Defines: with prefix caching, requests that share a prompt prefix share
+ * its full blocks ([Overview], "KV cache management and prefix caching";
+ * [Anatomy], the automatic prefix caching section); cascade attention
+ * ([Overview], the attention-backend paragraph, which records its removal
+ * from vLLM in 0.32.0) computes the shared prefix's part of the attention
+ * once for all queries and merges it with each request's own part, by the
+ * same rule as the split-K merge ([Anatomy], "Boundaries: FlashAttention").
+ * The result is pa_attention's for the same arguments, up to the rounding
+ * order of the merge.
+ *
+ * Arguments and results as pa_attention, plus common_prefix_blocks = N >= 0
+ * (negative, or more than max_blocks_per_seq: PA_ERR_INVALID_ARG).  The
+ * caller states that every request's block-table row begins with the same
+ * N block ids, and that every request's queries come after those blocks'
+ * keys (L_r - n_r >= 16 N).  N = 0 is the plain step.  Where the step's
+ * types and shapes have a cascade path (head_dim 128, bf16 / f16 / FP8
+ * E4M3 caches, a positive scale, KV heads a multiple of 4, at most 512
+ * requests) the N prefix blocks are read once per KV head, for the query
+ * rows of every request of at most 8 rows per KV head, on the tensor
+ * cores; elsewhere N is not used.  The statement is checked on the device:
+ * a request whose block-table row or key count breaks it sets
+ * PA_DEV_ERR_METADATA (pa_get_device_error) and the step's output is then
+ * undefined.  The workspace must hold pa_attention_cascade_workspace_size
+ * bytes for the same sizes.
+ */
+pa_status pa_attention_cascade(const void* q, pa_dtype q_dtype,
+                               const void* k_cache, const void* v_cache,
+                               pa_dtype cache_dtype, int64_t num_blocks,
+                               int block_size, int num_q_heads, int num_kv_heads,
+                               int head_dim, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* query_start_loc, int num_seqs,
+                               int64_t num_tokens, int max_query_len,
+                               int max_seq_len, float scale, float k_scale,
+                               float v_scale, int common_prefix_blocks, void* out,
+                               void* workspace, size_t workspace_bytes,
+                               pa_stream_t stream);
+
+/*
+ * pa_attention_cascade_workspace_size -- bytes of device workspace
+ * pa_attention_cascade needs: pa_attention's, plus one partial row
+ * ((head_dim + 2) x 4 bytes) per token and q head for the shared prefix and
+ * 32 per request and group of 4 KV heads for the requests' own parts.
+ */
+pa_status pa_attention_cascade_workspace_size(int64_t num_tokens,
+                                              int num_q_heads, int num_kv_heads,
+                                              int head_dim, int num_seqs,
+                                              int max_query_len, int max_seq_len,
+                                              size_t* bytes);
+
+/*
  * pa_set_wait_limit_ns -- the longest one pipeline wait inside the attention
  * kernels may last (no counterpart on the pages; failure detection).  A
  * kernel whose wait runs out records PA_DEV_ERR_TIMEOUT (pa_get_device_error),

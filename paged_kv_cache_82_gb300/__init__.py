@@ -39,7 +39,8 @@ EXPORTED = ("pa_status_string", "pa_reshape_and_cache", "pa_copy_blocks",
             "pa_launch_count", "pa_attention_noalloc",
             "pa_set_debug_bounds", "pa_attention_window",
             "pa_attention_window_workspace_size", "pa_set_wait_limit_ns",
-            "pa_test_skip_copy")
+            "pa_test_skip_copy", "pa_attention_cascade",
+            "pa_attention_cascade_workspace_size")
 
 _DT = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16, "e4m3": PA_FP8_E4M3,
        "int4": PA_INT4, "nvfp4": PA_NVFP4}
@@ -120,6 +121,13 @@ def load_library(path: str = LIB_PATH):
     lib.pa_attention_window_workspace_size.argtypes = [
         i64, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
     lib.pa_attention_window_workspace_size.restype = i32
+    lib.pa_attention_cascade.argtypes = [P, i32, P, P, i32, i64, i32, i32, i32,
+                                         i32, P, i32, P, P, i32, i64, i32, i32,
+                                         f32, f32, f32, i32, P, P, sz, P]
+    lib.pa_attention_cascade.restype = i32
+    lib.pa_attention_cascade_workspace_size.argtypes = [
+        i64, i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.pa_attention_cascade_workspace_size.restype = i32
     lib.pa_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.pa_set_wait_limit_ns.restype = i32
     lib.pa_test_skip_copy.argtypes = [i64]
@@ -334,6 +342,54 @@ def pa_attention_window(q: torch.Tensor, k_cache: torch.Tensor,
         _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "pa_attention_window")
+    return out
+
+
+def pa_attention_cascade_workspace_size(num_tokens: int, num_q_heads: int,
+                                        num_kv_heads: int, head_dim: int,
+                                        num_seqs: int, max_query_len: int,
+                                        max_seq_len: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = _load().pa_attention_cascade_workspace_size(
+        num_tokens, num_q_heads, num_kv_heads, head_dim, num_seqs,
+        max_query_len, max_seq_len, ctypes.byref(out))
+    _check(st, "pa_attention_cascade_workspace_size")
+    return int(out.value)
+
+
+def pa_attention_cascade(q: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, block_tables: torch.Tensor,
+                         seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                         max_query_len: int, max_seq_len: int, scale: float,
+                         common_prefix_blocks: int, k_scale: float = 1.0,
+                         v_scale: float = 1.0,
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         cache_dtype: Optional[str] = None,
+                         stream=None) -> torch.Tensor:
+    """pa_attention for a step whose requests all begin with the same
+    `common_prefix_blocks` block ids (the shared prefix is read once per KV
+    head and merged with each request's own part)."""
+    T, Hq, D, NB, Hkv, bs, B = _step_shapes(q, k_cache, v_cache, block_tables,
+                                            seq_lens, query_start_loc, out,
+                                            cache_dtype)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = pa_attention_cascade_workspace_size(
+            T, Hq, Hkv, D, B, max_query_len, max_seq_len)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8,
+                                device=q.device)
+    st = _load().pa_attention_cascade(
+        _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dtype_code(k_cache, cache_dtype), NB, bs, Hq,
+        Hkv, D, _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(seq_lens, "seq_lens"), _dev(query_start_loc, "query_start_loc"),
+        B, T, int(max_query_len), int(max_seq_len), float(scale),
+        float(k_scale), float(v_scale), int(common_prefix_blocks),
+        _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_attention_cascade")
     return out
 
 

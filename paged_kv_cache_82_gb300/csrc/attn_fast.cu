@@ -191,6 +191,13 @@ struct FastParams {
   int head_dim;       // 128, or 64 (16-bit caches, head-group decode kernel)
   int l2_prefetch;    // 1: the head-group producer prefetches pages into L2
                       // PA_L2_PREFETCH_PAGES ahead of its loads
+  // shared-prefix (cascade) steps, head-group kernel: every request's first
+  // cascade_blocks pages are left to the prefix tiles (partial rows from
+  // casc_row0 on, one per token and q head); the decode segments cover the
+  // pages after them, and a segment that no range boundary cuts writes its
+  // partial to slot unc_slot0 + request * (KV heads / kHg) + head group.
+  int cascade_blocks;
+  int64_t unc_slot0, casc_row0;
 };
 
 // ---------------------------------------------------------------------------
@@ -1423,6 +1430,11 @@ struct ItemSource {
   const int* rows;
   long long cur, lo, hi;
   int r, B, H, b;
+  // cascade steps: pages start after the shared prefix, and an uncut piece
+  // goes to its own slot (the merge adds the prefix's part)
+  bool casc;
+  int pg_off;
+  int64_t unc_slot0;
 
   __device__ bool next(int4& rec0, int4& rec1) {
     if (!self) {
@@ -1450,9 +1462,10 @@ struct ItemSource {
     // its "tail" part (slot 2b + 1)
     const bool before = cur == lo && ss < lo;
     const bool after = pe == hi && se > hi;
-    const int slot = before ? 2 * b : (after ? 2 * b + 1 : -1);
+    const int slot = before ? 2 * b
+                            : (after ? 2 * b + 1 : (casc ? (int)(unc_slot0 + r * H + g) : -1));
     rec0 = make_int4(r, g, kItemDecode, slot);
-    rec1 = make_int4(pg_begin, pg_end, rows[r], 0);
+    rec1 = make_int4(pg_begin + pg_off, pg_end + pg_off, rows[r], 0);
     cur = pe;
     if (pe == se && g + 1 == H) ++r;
     return true;
@@ -1475,8 +1488,13 @@ __device__ long long plan_prefix(const FastParams& p, long long* dec0,
                                  p.max_query_len, p.max_seq_len,
                                  p.max_blocks_per_seq);
       if (m.ok && m.n > 0 && m.n * p.group <= p.dec_rows_max) {
-        dl = kSegCost + m.nb;
+        dl = kSegCost + m.nb - p.cascade_blocks;
         rw = m.n * p.group;
+        // a cascade step's shared prefix must lie before the queries
+        if (p.cascade_blocks > 0 && m.L - m.n < p.cascade_blocks * kBS) {
+          if (blockIdx.x == 0) flag_error(p.err, PA_DEV_ERR_METADATA);
+          dl = rw = 0;
+        }
       } else if (!m.ok && blockIdx.x == 0) {
         flag_error(p.err, PA_DEV_ERR_METADATA);
       }
@@ -1758,8 +1776,10 @@ merge_kernel(FastParams p) {
 #endif
 constexpr int kMergeThreads = PA_MERGE_THREADS;  // merge_self_kernel CTA
 
+// (at most 64 registers a thread: a merge CTA fits beside the two decode
+// CTAs of an SM, so that its plan runs while the attention kernel does)
 template <typename TOut>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 4)
 merge_self_kernel(FastParams p) {
   extern __shared__ long long mplan[];
   __shared__ long long scan[34];
@@ -1772,6 +1792,122 @@ merge_self_kernel(FastParams p) {
   const int g_eff = self_plan_grid(C, p.attn_grid);
   if (C <= 0) return;
   const int lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int D = p.head_dim;
+  const bool act = 4 * lane < D;  // lanes holding 4 of the row's D columns
+  // rows of every KV head of a segment (one head, or a head group whose
+  // partial slots hold kHg x 8 rows)
+  const int sh = p.seg_heads;
+  const int part_rows = sh == 1 ? 16 : kHgPartRows;
+  const bool casc = p.cascade_blocks > 0;
+  if (casc) {
+    // a cascade step's requests all start with request 0's first
+    // cascade_blocks block-table entries (checked while the attention runs)
+    const int64_t total = (int64_t)p.num_seqs * p.cascade_blocks;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+         x += (int64_t)gridDim.x * blockDim.x) {
+      const int r = (int)(x / p.cascade_blocks);
+      const int j = (int)(x - (int64_t)r * p.cascade_blocks);
+      if (r > 0 && __ldg(p.block_tables + (int64_t)r * p.max_blocks_per_seq + j) !=
+                       __ldg(p.block_tables + j))
+        flag_error(p.err, PA_DEV_ERR_METADATA);
+    }
+  }
+  // One output row from np partial rows (row_of(s): row index into ws_acc /
+  // ws_ml), combined in part order: M = max m_s, out = sum 2^(m_s - M) acc_s
+  // / sum 2^(m_s - M) l_s.  A part with m = -inf has no visible key.
+  auto combine = [&](int np, auto row_of, int64_t orow) {
+    float M = -INFINITY, den = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (np <= 32) {
+      // lane s holds part s's (m, l): one round trip gives M and the
+      // denominator; the weights go round by shuffle, so the numerator's
+      // loads are independent of each other.  The first four parts' rows
+      // are loaded together with (m, l).
+      float4 vpre[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        vpre[s] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s < np && act)
+          vpre[s] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + row_of(s) * D) + lane);
+      }
+      float ms = -INFINITY, ls = 0.f;
+      if (lane < np) {
+        const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ws_ml) + row_of(lane));
+        ms = ml.x;
+        ls = ml.y;
+      }
+      M = ms;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+      const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);
+      den = w * ls;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const float wgt = __shfl_sync(~0u, w, s);
+        if (s < np) {
+          acc[0] += wgt * vpre[s].x;
+          acc[1] += wgt * vpre[s].y;
+          acc[2] += wgt * vpre[s].z;
+          acc[3] += wgt * vpre[s].w;
+        }
+      }
+#pragma unroll 4
+      for (int s = 4; s < np; ++s) {
+        const float wgt = __shfl_sync(~0u, w, s);
+        const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + row_of(s) * D) + lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        acc[0] += wgt * v.x;
+        acc[1] += wgt * v.y;
+        acc[2] += wgt * v.z;
+        acc[3] += wgt * v.w;
+      }
+    } else {
+      // M and the denominator with the parts spread over the lanes
+      for (int s = lane; s < np; s += 32) M = fmaxf(M, __ldg(p.ws_ml + row_of(s) * 2));
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
+      for (int s = lane; s < np; s += 32) {
+        const int64_t pr = row_of(s);
+        const float ms = __ldg(p.ws_ml + pr * 2);
+        if (ms != -INFINITY) den += exp2f(ms - M) * __ldg(p.ws_ml + pr * 2 + 1);
+      }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
+      // the numerator in part order, loads of several parts in flight
+#pragma unroll 4
+      for (int s = 0; s < np; ++s) {
+        const int64_t pr = row_of(s);
+        const float ms = __ldg(p.ws_ml + pr * 2);
+        const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);
+        acc[0] += wgt * v.x;
+        acc[1] += wgt * v.y;
+        acc[2] += wgt * v.z;
+        acc[3] += wgt * v.w;
+      }
+    }
+    const float inv = p.out_scale / den;
+    TOut* o = static_cast<TOut*>(p.out) + orow * D + 4 * lane;
+    if (act) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
+    }
+  };
+  // the output row of segment row rr (kv head w of the segment's group)
+  struct SegRow {
+    int prow;
+    int64_t row;
+  };
+  auto seg_row = [&](int g, int x, int nrows, int q0) -> SegRow {
+    const int w = x / nrows, rr = x - w * nrows;
+    const int i = rr / p.group;
+    const int h = (g * sh + w) * p.group + (rr - i * p.group);
+    return SegRow{sh == 1 ? rr : w * 8 + rr, (int64_t)(q0 + i) * p.num_q_heads + h};
+  };
+  const int c0 = casc ? 1 : 0;  // the prefix's part comes first
   // this CTA takes range boundaries blockIdx.x, + gridDim.x, ...
   for (int b = blockIdx.x; b < g_eff; b += gridDim.x) {
     if (b == 0) continue;
@@ -1784,9 +1920,9 @@ merge_self_kernel(FastParams p) {
     const long long ss = dec0[r] + (long long)g * dl, se = ss + dl;
     if (ss >= lo_b) continue;  // boundary b does not cut a segment
     // the boundaries that cut this segment: b0 .. b1-1.  Its parts, in order:
-    // the tail piece of range b0-1 (slot 2(b0-1)+1), then the head pieces of
-    // ranges b0 .. b1-1 (slots 2k).  The b1-b0 CTAs of these boundaries share
-    // the segment's rows.
+    // (cascade steps: the shared prefix's,) the tail piece of range b0-1
+    // (slot 2(b0-1)+1), then the head pieces of ranges b0 .. b1-1 (slots
+    // 2k).  The b1-b0 CTAs of these boundaries share the segment's rows.
     int b0 = b;
     while (b0 > 1 && (long long)(b0 - 1) * C / g_eff > ss) --b0;
     int b1 = b + 1;
@@ -1795,112 +1931,49 @@ merge_self_kernel(FastParams p) {
     const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
                                 p.max_seq_len, p.max_blocks_per_seq);
     pdl_wait();  // the attention grid has finished writing the parts
-    // rows of every KV head of the segment (one head, or a head group whose
-    // partial slots hold kHg x 8 rows)
-    const int sh = p.seg_heads;
-    const int part_rows = sh == 1 ? 16 : kHgPartRows;
     const int total = sh * rows[r];
-    const int D = p.head_dim;
-    const bool act = 4 * lane < D;  // lanes holding 4 of the row's D columns
     for (int x = (b - b0) * nwarps + (threadIdx.x >> 5); x < total;
          x += (b1 - b0) * nwarps) {
-      const int w = x / rows[r], rr = x - w * rows[r];
-      const int prow = sh == 1 ? rr : w * 8 + rr;
-      const int i = rr / p.group;
-      const int h = (g * sh + w) * p.group + (rr - i * p.group);
-      const int64_t row = (int64_t)(rm.q0 + i) * p.num_q_heads + h;
-      // partial row of part s: slot 2(b0-1)+1 for s = 0, else slot 2(b0+s-1)
-      const int64_t pr_tail = (int64_t)(2 * (b0 - 1) + 1) * part_rows + prow;
-      const int64_t pr_head = (int64_t)(2 * b0) * part_rows + prow;
+      const SegRow sr = seg_row(g, x, rows[r], rm.q0);
+      const int64_t pr_tail = (int64_t)(2 * (b0 - 1) + 1) * part_rows + sr.prow;
+      const int64_t pr_head = (int64_t)(2 * b0) * part_rows + sr.prow;
       const int64_t pr_step = 2 * (int64_t)part_rows;
-      float M = -INFINITY, den = 0.f;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (np <= 32) {
-        // lane s holds part s's (m, l): one round trip gives M and the
-        // denominator; the weights go round by shuffle, so the numerator's
-        // loads are independent of each other.  The first four parts' rows
-        // are loaded together with (m, l).
-        float4 vpre[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          vpre[s] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (s < np && act) {
-            const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-            vpre[s] = __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane);
-          }
-        }
-        float ms = -INFINITY, ls = 0.f;
-        if (lane < np) {
-          const int64_t pr = lane == 0 ? pr_tail : pr_head + (lane - 1) * pr_step;
-          const float2 ml = __ldg(reinterpret_cast<const float2*>(p.ws_ml) + pr);
-          ms = ml.x;
-          ls = ml.y;
-        }
-        M = ms;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
-        const float w = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
-        den = w * ls;
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const float wgt = __shfl_sync(~0u, w, s);
-          if (s < np) {
-            acc[0] += wgt * vpre[s].x;
-            acc[1] += wgt * vpre[s].y;
-            acc[2] += wgt * vpre[s].z;
-            acc[3] += wgt * vpre[s].w;
-          }
-        }
-#pragma unroll 4
-        for (int s = 4; s < np; ++s) {
-          const float wgt = __shfl_sync(~0u, w, s);
-          const int64_t pr = pr_head + (s - 1) * pr_step;
-          const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-          acc[0] += wgt * v.x;
-          acc[1] += wgt * v.y;
-          acc[2] += wgt * v.z;
-          acc[3] += wgt * v.w;
-        }
-      } else {
-        // M and the denominator with the parts spread over the lanes
-        for (int s = lane; s < np; s += 32) {
-          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-          M = fmaxf(M, __ldg(p.ws_ml + pr * 2));
-        }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) M = fmaxf(M, __shfl_xor_sync(~0u, M, d));
-        for (int s = lane; s < np; s += 32) {
-          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-          const float ms = __ldg(p.ws_ml + pr * 2);
-          if (ms != -INFINITY) den += exp2f(ms - M) * __ldg(p.ws_ml + pr * 2 + 1);
-        }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(~0u, den, d);
-        // the numerator in part order, loads of several parts in flight
-#pragma unroll 4
-        for (int s = 0; s < np; ++s) {
-          const int64_t pr = s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
-          const float ms = __ldg(p.ws_ml + pr * 2);
-          const float4 v = act ? __ldg(reinterpret_cast<const float4*>(p.ws_acc + pr * D) + lane)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-          const float wgt = ms == -INFINITY ? 0.f : exp2f(ms - M);  // no visible key
-          acc[0] += wgt * v.x;
-          acc[1] += wgt * v.y;
-          acc[2] += wgt * v.z;
-          acc[3] += wgt * v.w;
-        }
-      }
-      const float inv = p.out_scale / den;
-      TOut* o = static_cast<TOut*>(p.out) + row * D + 4 * lane;
-      if (act) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = from_f32<TOut>(acc[k] * inv);
-      }
+      const int64_t pr_casc = p.casc_row0 + sr.row;
+      combine(np + c0,
+              [&](int s) -> int64_t {
+                if (s < c0) return pr_casc;
+                s -= c0;
+                return s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
+              },
+              sr.row);
     }
   }  // boundaries
+  if (casc) {
+    // cascade steps: a segment that no boundary cuts has one part of its
+    // own (its uncut slot), merged here with the prefix's
+    const int H = p.num_kv_heads / sh;
+    const int64_t npairs = (int64_t)p.num_seqs * H;
+    for (int64_t x = blockIdx.x; x < npairs; x += gridDim.x) {
+      const int r = (int)(x / H), g = (int)(x - (int64_t)r * H);
+      if (declen[r] == 0) continue;
+      const long long ss = dec0[r] + (long long)g * declen[r], se = ss + declen[r];
+      // the range holding unit ss; the segment is cut if the range ends
+      // before it does (handled above)
+      int k = (int)(ss * g_eff / C);
+      while (k + 1 < g_eff && (long long)(k + 1) * C / g_eff <= ss) ++k;
+      while (k > 0 && (long long)k * C / g_eff > ss) --k;
+      if ((long long)(k + 1) * C / g_eff < se) continue;
+      const ReqMeta rm = load_req(p.qsl, p.seq_lens, r, p.num_tokens, p.max_query_len,
+                                  p.max_seq_len, p.max_blocks_per_seq);
+      pdl_wait();
+      const int64_t unc = (p.unc_slot0 + (int64_t)r * H + g) * part_rows;
+      for (int y = threadIdx.x >> 5; y < sh * rows[r]; y += nwarps) {
+        const SegRow sr = seg_row(g, y, rows[r], rm.q0);
+        const int64_t pr_casc = p.casc_row0 + sr.row, pr_unc = unc + sr.prow;
+        combine(2, [&](int s) -> int64_t { return s == 0 ? pr_casc : pr_unc; }, sr.row);
+      }
+    }
+  }
 }
 
 
@@ -2370,6 +2443,9 @@ attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
   }
   src.cur = src.lo;
   src.r = p.num_seqs > 0 ? request_of(dec0, p.num_seqs, src.lo) : 0;
+  src.casc = p.cascade_blocks > 0;
+  src.pg_off = p.cascade_blocks;
+  src.unc_slot0 = p.unc_slot0;
 
   if (warp == kConsumerWarps) {
     // ------------------------------ producer ------------------------------
@@ -2587,12 +2663,26 @@ bool use_head_groups(const AttnArgs& a, bool tc) {
 // the tiles half their balanced share: the rest run behind the decode kernel
 // on every SM, which measured best (a 1022-token chunk beside 120 decodes:
 // 13 SMs, step 437 -> 428 us; 20 SMs or more were slower than none).
+//
+// Cascade steps: the decode segments lose the shared prefix (their keys
+// taken as max_seq_len - 16 N against the prefill rows' max_seq_len), and
+// the decode kernel, prefetching into L2 (l2_prefetch) and reading no
+// prefix from L2, keeps HBM busy on fewer SMs: the tiles get their whole
+// balanced share (the 120-decode mixed step after a 125-block prefix: 31
+// SMs; measured 13 -> 0.409 ms, 28 -> 0.387-0.392, 36-44 -> 0.394).
 int prefill_ctas_ahead(const AttnArgs& a, int num_sms) {
   const int64_t n_pf = a.num_tokens - a.num_seqs + 1;
   if (n_pf <= 0 || a.num_seqs <= 0 || num_sms < 16) return 0;
   const double G = (double)a.num_q_heads / a.num_kv_heads;
-  const double r = G * (double)n_pf / (double)a.num_seqs * 0.006;
-  int p = (int)(0.5 * num_sms * r / (1.0 + r) + 0.5);
+  double r = G * (double)n_pf / (double)a.num_seqs * 0.006;
+  double share = 0.5;
+  if (a.cascade_blocks > 0) {
+    const double K = (double)a.max_seq_len;
+    const double Kd = std::max(1.0, K - (double)a.cascade_blocks * kBS);
+    r *= K / Kd;
+    share = 1.0;
+  }
+  int p = (int)(share * num_sms * r / (1.0 + r) + 0.5);
   if (p < 4) p = 4;
   if (p > num_sms / 4) p = num_sms / 4;
   return p;
@@ -2655,9 +2745,12 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
     cfg.gridDim = dim3(grid);
   }
   if (pe.start) cudaEventRecord(pe.start, stream);
+  // (cascade steps: the shared-prefix tiles' partial rows)
+  float* casc_acc = f.cascade_blocks > 0 ? f.ws_acc + f.casc_row0 * 128 : nullptr;
+  float* casc_ml = f.cascade_blocks > 0 ? f.ws_ml + f.casc_row0 * 2 : nullptr;
   if (tc && pf_ctas > 0) {
     e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
-                          tile_ctr, false, pf_ctas, stream);
+                          tile_ctr, false, pf_ctas, stream, casc_acc, casc_ml);
     if (e != cudaSuccess) return e;
   }
   e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
@@ -2665,7 +2758,8 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   count_launch();
   if (tc) {
     e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
-                          tile_ctr, pe.start == nullptr, num_sms, stream);
+                          tile_ctr, pe.start == nullptr, num_sms, stream, casc_acc,
+                          casc_ml);
     if (e != cudaSuccess) return e;
   }
   if (pe.stop) cudaEventRecord(pe.stop, stream);
@@ -2761,6 +2855,11 @@ int decode_box_rows(const AttnArgs& a, bool tc) {
   return use_head_groups(a, tc) ? kHg * kBS : kBS;
 }
 
+bool cascade_supported(const AttnArgs& a) {
+  return a.cascade_blocks > 0 && a.window <= 0 && fast_path_supported(a) &&
+         tc_prefill_supported(a) && use_head_groups(a, true);
+}
+
 bool fast_path_supported(const AttnArgs& a) {
   // head_dim 64, bf16 / f16: decode-only steps in KV-head groups
   if (a.head_dim == 64)
@@ -2779,8 +2878,9 @@ bool fast_path_supported(const AttnArgs& a) {
 
 AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                    int head_dim, int num_seqs, int max_query_len,
-                   int max_seq_len, int num_sms, int window) {
+                   int max_seq_len, int num_sms, int window, bool cascade) {
   AttnPlan pl{};
+  pl.cascade = cascade && window <= 0 ? 1 : 0;
   pl.window = window > 0 && window < max_seq_len ? window : 0;
   pl.group = num_q_heads / num_kv_heads;
   pl.has_prefill = (int64_t)max_query_len * pl.group > kDecodeMaxRows;
@@ -2792,9 +2892,20 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                 ((num_tokens * pl.group + kPrefillTileRows - 1) / kPrefillTileRows +
                  num_seqs)
           : 0;
+  if (pl.cascade) {
+    // shared-prefix tiles: the step's tokens, per KV head, in tiles of
+    // 128 / group tokens (128 query rows)
+    const int64_t tpt = std::max(1, 128 / pl.group);
+    pl.max_atoms += (int64_t)num_kv_heads * ((num_tokens + tpt - 1) / tpt);
+  }
   pl.max_items = pl.max_atoms + (pl.has_decode ? (int64_t)num_seqs * num_kv_heads : 0) +
                  pl.grid_max;
   pl.max_slots = 2 * (int64_t)pl.grid_max;
+  pl.unc_slots = pl.cascade && pl.has_decode ? (int64_t)num_seqs * (num_kv_heads / kHg) : 0;
+  // partial rows: the slots', then (cascade) one per token and q head
+  pl.casc_row0 = (pl.max_slots + pl.unc_slots) * kHgPartRows;
+  const int64_t part_rows =
+      pl.has_decode ? pl.casc_row0 + (pl.cascade ? num_tokens * num_q_heads : 0) : 0;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   size_t off = 0;
   pl.off_atoms = off;       off = up(off + (size_t)pl.max_atoms * 16);
@@ -2809,9 +2920,9 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
   pl.off_pref = off;        off = up(off + 16);
   // partial slots of up to kHgPartRows rows (head-group items: kHg heads x 8)
   pl.off_acc = off;
-  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * head_dim * 4);
+  off = up(off + (size_t)part_rows * head_dim * 4);
   pl.off_ml = off;
-  if (pl.has_decode) off = up(off + (size_t)pl.max_slots * kHgPartRows * 2 * 4);
+  off = up(off + (size_t)part_rows * 2 * 4);
   // a request's keys through the window start in the block holding key
   // L - n - window + 1: at most n + window - 1 + 15 keys from there
   pl.off_win_sl = pl.off_win_bt = off;
@@ -2964,7 +3075,14 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
   pa.split_list = reinterpret_cast<int4*>(ws + plan.off_split + 16);
   pa.n_split = reinterpret_cast<int*>(ws + plan.off_split);
   if (use_head_groups(a, tc != nullptr)) {
-    const TcMaps* t = plan.has_prefill ? tc : nullptr;
+    const TcMaps* t = plan.has_prefill || plan.cascade ? tc : nullptr;
+    if (plan.cascade && t != nullptr && a.cascade_blocks > 0) {
+      // shared-prefix step: the prefix tiles' rows and the uncut suffix
+      // slots follow the split slots in the partial rows
+      fp.cascade_blocks = a.cascade_blocks;
+      fp.unc_slot0 = plan.max_slots;
+      fp.casc_row0 = plan.casc_row0;
+    }
     const bool qb = a.q_dtype == PA_BF16;
     const bool d64 = a.head_dim == 64;
     switch (a.cache_dtype == PA_BF16   ? (d64 ? kKindBF16D64 : kKindBF16)

@@ -118,7 +118,7 @@ enum : int {
   kNumBars = kV8Full + 2
 };
 
-constexpr int kSlotInts = 12;  // a tile slot: its index, then the TcTile fields
+constexpr int kSlotInts = 13;  // a tile slot: its index, then the TcTile fields
 
 // FP8 caches: E4M3 pages are staged half a chunk (4 pages) at a time, two
 // buffers per cache, and widened to f16 into the K / V stages
@@ -137,10 +137,10 @@ struct TcLayoutT {
   // the step's tile list when the kernel plans it: per request, the first
   // tile (x heads) and the tile count; block-scan scratch
   static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
-  static constexpr int kScan = kPlan + 2 * kTcMaxSeqs * 4;   // int[33]
+  static constexpr int kScan = kPlan + 2 * kTcMaxSeqs * 4;   // int[36]
   // FP8: staging (1024-aligned for the swizzled TMA boxes), then the Q rows'
   // power-of-two shifts of the two tile slots (float[2][128])
-  static constexpr int kK8 = (kScan + 33 * 4 + 1023) & ~1023;
+  static constexpr int kK8 = (kScan + 36 * 4 + 1023) & ~1023;
   static constexpr int kV8 = kK8 + (kFp8 ? 2 * kHalfChunk8 : 0);
   static constexpr int kShift = kV8 + (kFp8 ? 2 * kHalfChunk8 : 0);
   static constexpr int kBytes = kShift + (kFp8 ? 2 * 128 * 4 : 0);
@@ -181,21 +181,52 @@ struct TcParams {
   float score_scale;     // softmax scale * log2(e) (* k_scale for FP8)
   float out_scale;       // 1, or v_scale for FP8
   int window;            // sliding window in keys (kNoWindow: none)
+  // shared-prefix (cascade) steps: N > 0 leading block-table entries that
+  // every request shares.  The prefix tiles (after the prefill tiles in the
+  // list) take the tokens of the decode-class requests, all of whose keys
+  // 0 .. 16 N - 1 they see, and write partial rows (O unscaled, m, l) at
+  // casc_acc / casc_ml [token * num_q_heads + q head]
+  int cascade_blocks;
+  float* casc_acc;
+  float* casc_ml;
 };
 
 // one tile, as every role of the CTA sees it: its keys are the pages
-// p0 .. p0 + pages - 1 of the request (p0 > 0 only with a sliding window)
+// p0 .. p0 + pages - 1 of the request (p0 > 0 only with a sliding window).
+// A shared-prefix tile (casc) reads request 0's block-table row: tokens
+// i0 .. i0 + ntok - 1 of the step, every one of them seeing keys 0 .. L - 1.
 struct TcTile {
   int r, g, q0, n, L, i0, ntok, p0, pages, nc;
-  bool ok;
+  bool ok, casc;
 };
 
 // Tile li of the step's list, which runs request by request, tile index
 // ascending (causal limits growing), KV head fastest: from the planner's
-// list, or located in the kernel's own per-request prefix.
+// list, or located in the kernel's own per-request prefix.  Past the n_real
+// prefill tiles come the shared-prefix tiles of the first casc_tok tokens
+// (tile index, then KV head fastest).
 __device__ __forceinline__ TcTile tc_tile(const TcParams& p, const int* pre,
-                                          const int* ntl, int li) {
+                                          const int* ntl, int li, int n_real,
+                                          int casc_tok) {
   int r, g, tt;
+  if (li >= n_real) {
+    const int j = li - n_real;
+    TcTile t{};
+    t.casc = true;
+    tt = j / p.num_kv_heads;
+    t.g = j - tt * p.num_kv_heads;
+    t.r = 0;
+    t.q0 = 0;
+    t.n = casc_tok;
+    t.L = p.cascade_blocks * kBS;
+    t.i0 = tt * p.tokens_per_tile;
+    t.ntok = min(p.tokens_per_tile, casc_tok - t.i0);
+    t.p0 = 0;
+    t.pages = p.cascade_blocks;
+    t.nc = (t.pages + kTcPages - 1) / kTcPages;
+    t.ok = t.ntok > 0 && p.num_seqs > 0 && p.cascade_blocks <= p.max_blocks_per_seq;
+    return t;
+  }
   if (p.self_plan) {
     int lo = 0, hi = p.num_seqs - 1;  // last request with pre[r] <= li
     while (lo < hi) {
@@ -256,10 +287,14 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity,
 // The step's prefill tiles: per request (prefill-class: more than
 // dec_rows_max query rows), ceil(rows / tile rows) tiles per KV head; the
 // exclusive prefix of tiles x heads into pre[], the tile counts into ntl[].
-// All threads of the block take part; returns the total.
+// scan[33]: the tokens the shared-prefix tiles take (up to the last token of
+// the last decode-class request; 0 without a shared prefix).  All threads
+// of the block take part; returns the prefill tiles' total.
 __device__ int plan_tiles(const TcParams& p, int* pre, int* ntl, int* scan) {
   const int rows_per_tile = p.tokens_per_tile * p.group;
   int run = 0;
+  if (threadIdx.x == 0) scan[33] = 0;
+  __syncthreads();
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
     const int r = base + threadIdx.x;
     int tiles = 0;
@@ -269,6 +304,8 @@ __device__ int plan_tiles(const TcParams& p, int* pre, int* ntl, int* scan) {
                                  p.max_blocks_per_seq);
       if (m.ok && m.n * p.group > p.dec_rows_max)
         tiles = (m.n * p.group + rows_per_tile - 1) / rows_per_tile;
+      else if (m.ok && m.n > 0 && p.cascade_blocks > 0)
+        atomicMax(scan + 33, m.q0 + m.n);
     }
     const int ex = block_scan_excl<int>(tiles * p.num_kv_heads, scan + 32, scan);
     const int tot = scan[32];
@@ -307,6 +344,7 @@ __device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTil
   slot[9] = t.nc;
   slot[10] = t.ok ? 1 : 0;
   slot[11] = t.p0;
+  slot[12] = t.casc ? 1 : 0;
 }
 
 // The k-th tile of a warp that does not draw tiles, from slot k % 2; the
@@ -334,6 +372,7 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
   t.nc = sl[9];
   t.ok = sl[10] != 0;
   t.p0 = sl[11];
+  t.casc = sl[12] != 0;
   if (shifts != nullptr) *shift = shifts[s * 128 + row];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
@@ -507,9 +546,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
   volatile int* slots = reinterpret_cast<volatile int*>(sp + TcLayout::kTileSlot);
   int* const pre = reinterpret_cast<int*>(sp + TcLayout::kPlan);
   int* const ntl = pre + kTcMaxSeqs;
-  const int n_tiles =
+  const int n_real =
       p.self_plan ? plan_tiles(p, pre, ntl, reinterpret_cast<int*>(sp + TcLayout::kScan))
                   : min(*p.n_atoms, p.max_atoms);
+  // shared-prefix tiles after the prefill tiles (self-planned steps only)
+  const int casc_tok =
+      p.self_plan ? reinterpret_cast<const int*>(sp + TcLayout::kScan)[33] : 0;
+  const int n_tiles =
+      n_real + (casc_tok > 0 ? (casc_tok + p.tokens_per_tile - 1) / p.tokens_per_tile *
+                                   p.num_kv_heads
+                             : 0);
 
   // Cache rows of the tile's pages 32 G .. 32 G + 31 (four chunks), one
   // page per lane, checked against the pool.  The producers fetch the next
@@ -641,7 +687,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         li = snake_tile(k, n_tiles);
       }
       TcTile t{};
-      if (li >= 0) t = tc_tile(p, pre, ntl, li);
+      if (li >= 0) t = tc_tile(p, pre, ntl, li, n_real, casc_tok);
       const uint32_t qb = qt % kQStages;
       bool q_ready = false;
       if constexpr (kFp8) {
@@ -933,7 +979,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
       const bool valid = it < t.ntok;
-      const int lim = t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
+      // (a shared-prefix tile: every row sees all of its keys)
+      const int lim = t.casc ? t.L - 1 : t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
       float m_ref = -INFINITY, l = 0.f;
       bool go = true;
       for (int c = 0; c < t.nc; ++c) {
@@ -1048,12 +1095,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       TOut* o = static_cast<TOut*>(p.out) +
                 ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128 +
                 half * 64;
+      // a shared-prefix tile leaves its rows unnormalised, for the merge
+      const int64_t crow =
+          (int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh;
+      if (t.casc && valid && half == 0) {
+        p.casc_ml[crow * 2] = m_ref;
+        p.casc_ml[crow * 2 + 1] = l_tot;
+      }
 #pragma unroll 1
       for (int j = 0; j < 2; ++j) {
         uint32_t v[32];
         tc_ld32(t_o + j * 32, v);
         tc_wait_ld_dep(v);
-        if (valid) {
+        if (t.casc) {
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(p.casc_acc + crow * 128 + half * 64 + j * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                   __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]));
+          }
+        } else if (valid) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k)
@@ -1147,8 +1209,14 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
                               const int* n_atoms, int max_atoms,
                               int dec_rows_max, int* tile_ctr, bool after_decode,
-                              int num_sms, cudaStream_t stream) {
+                              int num_sms, cudaStream_t stream, float* casc_acc,
+                              float* casc_ml) {
   TcParams p{};
+  if (self_plan && a.cascade_blocks > 0 && casc_acc && casc_ml) {
+    p.cascade_blocks = a.cascade_blocks;
+    p.casc_acc = casc_acc;
+    p.casc_ml = casc_ml;
+  }
   p.out = a.out;
   p.block_tables = a.block_tables;
   p.seq_lens = a.seq_lens;

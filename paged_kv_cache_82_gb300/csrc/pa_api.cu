@@ -319,7 +319,7 @@ namespace {
 pa_status workspace_size_impl(int64_t num_tokens, int num_q_heads,
                               int num_kv_heads, int head_dim, int num_seqs,
                               int max_query_len, int max_seq_len, int window,
-                              size_t* bytes) {
+                              bool cascade, size_t* bytes) {
   if (!bytes) return PA_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads != 0 || max_query_len < 0 || max_seq_len < 0 ||
@@ -330,7 +330,7 @@ pa_status workspace_size_impl(int64_t num_tokens, int num_q_heads,
   if (!di) return PA_ERR_CUDA;
   const AttnPlan pl = make_plan(num_tokens, num_q_heads, num_kv_heads, head_dim,
                                 num_seqs, max_query_len, max_seq_len,
-                                di->num_sms, window);
+                                di->num_sms, window, cascade);
   *bytes = pl.total_bytes;
   return PA_OK;
 }
@@ -344,9 +344,9 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
                          const int32_t* query_start_loc, int num_seqs,
                          int64_t num_tokens, int max_query_len, int max_seq_len,
                          float scale, float k_scale, float v_scale, int window,
-                         void* out, void* workspace, size_t workspace_bytes,
-                         pa_stream_t stream) {
-  if (window < 0) return PA_ERR_INVALID_ARG;
+                         int cascade_blocks, void* out, void* workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+  if (window < 0 || cascade_blocks < 0) return PA_ERR_INVALID_ARG;
   if (!valid_dtype(q_dtype) || !valid_dtype(cache_dtype))
     return PA_ERR_INVALID_ARG;
   if (pa_status st = cache_shape_status(num_blocks, block_size, num_kv_heads,
@@ -366,7 +366,8 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
       max_blocks_per_seq < 0)
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PA_OK;
-  if ((int64_t)max_blocks_per_seq * PA_BLOCK_SIZE < max_seq_len)
+  if ((int64_t)max_blocks_per_seq * PA_BLOCK_SIZE < max_seq_len ||
+      cascade_blocks > max_blocks_per_seq)
     return PA_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens ||
       !query_start_loc || !out)
@@ -381,9 +382,9 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
       (size_t)num_blocks * num_kv_heads * page_bytes(cache_dtype, head_dim);
   const DeviceInfo* di = device_info();
   if (!di) return PA_ERR_CUDA;
-  const AttnPlan plan = make_plan(num_tokens, num_q_heads, num_kv_heads,
-                                  head_dim, num_seqs, max_query_len,
-                                  max_seq_len, di->num_sms, window);
+  AttnPlan plan = make_plan(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                            num_seqs, max_query_len, max_seq_len, di->num_sms,
+                            window);
   AttnArgs a{};
   a.q = q;
   a.q_dtype = q_dtype;
@@ -409,6 +410,15 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
   a.workspace = workspace;
   a.err = di->err;
   a.window = plan.window;
+  // a shared prefix runs as a cascade where the step's types and shapes
+  // allow it; elsewhere the hint is not used (the same attention, computed
+  // over every request's whole row)
+  a.cascade_blocks = cascade_blocks;
+  if (cascade_blocks > 0 && cascade_supported(a))
+    plan = make_plan(num_tokens, num_q_heads, num_kv_heads, head_dim, num_seqs,
+                     max_query_len, max_seq_len, di->num_sms, window, true);
+  else
+    a.cascade_blocks = 0;
   const bool fast = fast_path_supported(a);
   if (fast) {
     if (workspace_bytes < plan.total_bytes) return PA_ERR_INVALID_ARG;
@@ -437,7 +447,7 @@ pa_status attention_impl(const void* q, pa_dtype q_dtype, const void* k_cache,
     // prefill tiles go to the tensor-core kernel where it takes the step's
     // types (else the attention kernel runs them on the warp-level MMA)
     TcMaps tc;
-    const bool use_tc = plan.has_prefill && tc_prefill_supported(a) &&
+    const bool use_tc = (plan.has_prefill || plan.cascade) && tc_prefill_supported(a) &&
                         encode_prefill_tensor_maps(a, &tc);
     CUtensorMap tk{}, tv{};
     if (!encode_cache_tensor_maps(a, &tk, &tv, decode_box_rows(a, use_tc)))
@@ -459,7 +469,15 @@ pa_status pa_attention_workspace_size(int64_t num_tokens, int num_q_heads,
                                       int num_seqs, int max_query_len,
                                       int max_seq_len, size_t* bytes) {
   return workspace_size_impl(num_tokens, num_q_heads, num_kv_heads, head_dim,
-                             num_seqs, max_query_len, max_seq_len, 0, bytes);
+                             num_seqs, max_query_len, max_seq_len, 0, false, bytes);
+}
+
+pa_status pa_attention_cascade_workspace_size(int64_t num_tokens, int num_q_heads,
+                                              int num_kv_heads, int head_dim,
+                                              int num_seqs, int max_query_len,
+                                              int max_seq_len, size_t* bytes) {
+  return workspace_size_impl(num_tokens, num_q_heads, num_kv_heads, head_dim,
+                             num_seqs, max_query_len, max_seq_len, 0, true, bytes);
 }
 
 pa_status pa_attention_window_workspace_size(int64_t num_tokens,
@@ -469,7 +487,7 @@ pa_status pa_attention_window_workspace_size(int64_t num_tokens,
                                              int sliding_window, size_t* bytes) {
   return workspace_size_impl(num_tokens, num_q_heads, num_kv_heads, head_dim,
                              num_seqs, max_query_len, max_seq_len,
-                             sliding_window, bytes);
+                             sliding_window, false, bytes);
 }
 
 pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
@@ -487,8 +505,28 @@ pa_status pa_attention(const void* q, pa_dtype q_dtype, const void* k_cache,
                         block_size, num_q_heads, num_kv_heads, head_dim,
                         block_tables, max_blocks_per_seq, seq_lens,
                         query_start_loc, num_seqs, num_tokens, max_query_len,
-                        max_seq_len, scale, k_scale, v_scale, 0, out, workspace,
+                        max_seq_len, scale, k_scale, v_scale, 0, 0, out, workspace,
                         workspace_bytes, stream);
+}
+
+pa_status pa_attention_cascade(const void* q, pa_dtype q_dtype, const void* k_cache,
+                               const void* v_cache, pa_dtype cache_dtype,
+                               int64_t num_blocks, int block_size, int num_q_heads,
+                               int num_kv_heads, int head_dim,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* seq_lens,
+                               const int32_t* query_start_loc, int num_seqs,
+                               int64_t num_tokens, int max_query_len,
+                               int max_seq_len, float scale, float k_scale,
+                               float v_scale, int common_prefix_blocks, void* out,
+                               void* workspace, size_t workspace_bytes,
+                               pa_stream_t stream) {
+  return attention_impl(q, q_dtype, k_cache, v_cache, cache_dtype, num_blocks,
+                        block_size, num_q_heads, num_kv_heads, head_dim,
+                        block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_tokens, max_query_len,
+                        max_seq_len, scale, k_scale, v_scale, 0, common_prefix_blocks,
+                        out, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_attention_window(const void* q, pa_dtype q_dtype,
@@ -507,7 +545,7 @@ pa_status pa_attention_window(const void* q, pa_dtype q_dtype,
                         block_size, num_q_heads, num_kv_heads, head_dim,
                         block_tables, max_blocks_per_seq, seq_lens,
                         query_start_loc, num_seqs, num_tokens, max_query_len,
-                        max_seq_len, scale, k_scale, v_scale, sliding_window,
+                        max_seq_len, scale, k_scale, v_scale, sliding_window, 0,
                         out, workspace, workspace_bytes, stream);
 }
 

@@ -93,14 +93,22 @@ struct AttnPlan {
   // first query's first key in the window -- block-table rows of win_blocks
   // entries and key counts of at most win_max_seq_len
   int window, win_blocks, win_max_seq_len;
+  // shared-prefix (cascade) steps: partial rows after the max_slots slots --
+  // unc_slots more slots (one per decode request and head group, for the
+  // suffix of a segment that no range boundary cuts), then one row per
+  // (token, q head) for the shared prefix (casc_row0 onwards)
+  int cascade;
+  int64_t unc_slots, casc_row0;
 };
 
 // Host planning from host-known sizes only (no device read-back).
 // window: the sliding window in keys (0: none; a window of at least
 // max_seq_len keys cuts nothing and counts as none).
+// cascade: room for a shared-prefix step (pa_attention_cascade).
 AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                    int head_dim, int num_seqs, int max_query_len,
-                   int max_seq_len, int num_sms, int window = 0);
+                   int max_seq_len, int num_sms, int window = 0,
+                   bool cascade = false);
 
 
 struct AttnArgs {
@@ -123,7 +131,14 @@ struct AttnArgs {
   void* workspace;
   unsigned* err;
   int window;  // sliding window in keys (0: none)
+  int cascade_blocks;  // leading block-table entries all requests share,
+                       // computed once for the step (0: no cascade)
 };
+
+// true if a shared-prefix step of these types and shapes runs as a cascade
+// (prefix tiles on the tensor cores, suffixes on the head-group decode
+// kernel); otherwise the prefix hint is not used
+bool cascade_supported(const AttnArgs& a);
 
 // true if the TMA + tensor-core kernel covers these types / shapes
 bool fast_path_supported(const AttnArgs& a);
@@ -158,11 +173,14 @@ bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
 // n_atoms); one persistent CTA per SM.  tile_ctr (zeroed int, or null):
 // tiles drawn dynamically; after_decode: launched right behind the step's
 // decode kernel, whose output it does not read (starts as its CTAs retire).
+// casc_acc / casc_ml: the shared-prefix tiles' partial rows (cascade steps,
+// a.cascade_blocks > 0, self-planned only).
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
                               const int* n_atoms, int max_atoms,
                               int dec_rows_max, int* tile_ctr, bool after_decode,
-                              int num_sms, cudaStream_t stream);
+                              int num_sms, cudaStream_t stream,
+                              float* casc_acc = nullptr, float* casc_ml = nullptr);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,

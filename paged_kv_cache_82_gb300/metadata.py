@@ -16,6 +16,10 @@ Input: a sequence of requests with ``block_ids``, ``num_computed`` and
 * ``block_tables`` int32 [B, max_blocks] -- unused entries are 0
 * ``slot_mapping`` int64 [T] -- cache slot of every new token
 * ``max_query_len``, ``max_seq_len`` -- host upper bounds for the kernels
+
+``common_prefix_blocks`` gives the number of leading block ids that every
+request of the step shares and whose keys precede every request's queries:
+the shared prefix a cascade step (pa_attention_cascade) reads once.
 """
 from __future__ import annotations
 
@@ -60,3 +64,21 @@ def to_device(md: dict, device) -> dict:
         out[k] = torch.from_numpy(v).to(device) if isinstance(v, np.ndarray) \
             else v
     return out
+
+
+def common_prefix_blocks(requests) -> int:
+    """Leading block ids that all requests share (prefix caching hands the
+    same full blocks to requests with the same prompt prefix, "01. vLLM",
+    KV cache management and prefix caching), cut to the full blocks before
+    every request's first new token; 0 for an empty step."""
+    if not requests:
+        return 0
+    first = requests[0].block_ids
+    n = min(len(first), min(r.num_computed // BLOCK_SIZE for r in requests))
+    for r in requests[1:]:
+        k = 0
+        lim = min(n, len(r.block_ids))
+        while k < lim and r.block_ids[k] == first[k]:
+            k += 1
+        n = k
+    return int(n)

@@ -26,7 +26,9 @@ def half_ulp(ref: np.ndarray, dtype: str) -> np.ndarray:
     return np.ldexp(1.0, (e - OUT_MANT[dtype]).astype(np.int64))
 
 
-def gpu_step(wl, device="cuda", out=None, workspace=None):
+def gpu_step(wl, device="cuda", out=None, workspace=None, cascade_blocks=None):
+    """cascade_blocks: run the step through pa_attention_cascade with that
+    many shared leading blocks (None: pa_attention / pa_attention_window)."""
     md = build_step_metadata(wl.requests, wl.block_size)
     kc = wl.k_cache.to(device)
     vc = wl.v_cache.to(device)
@@ -44,7 +46,11 @@ def gpu_step(wl, device="cuda", out=None, workspace=None):
             torch.from_numpy(md["seq_lens"]).to(device),
             torch.from_numpy(md["query_start_loc"]).to(device),
             md["max_query_len"], md["max_seq_len"], wl.scale)
-    if wl.sliding_window:
+    if cascade_blocks is not None:
+        res = pa.pa_attention_cascade(
+            q, kc, vc, *meta, cascade_blocks, wl.k_scale, wl.v_scale,
+            out=out, workspace=workspace, cache_dtype=cdt)
+    elif wl.sliding_window:
         res = pa.pa_attention_window(
             q, kc, vc, *meta, wl.sliding_window, wl.k_scale, wl.v_scale,
             out=out, workspace=workspace, cache_dtype=cdt)

@@ -159,3 +159,19 @@ def test_attention_flops_counts_visible_pairs():
                                num_q_heads=2, num_kv_heads=1, head_dim=8,
                                num_blocks=4, dtype="bf16", cache_dtype="bf16")
     assert workloads.attention_flops(wl) == (6 + 7 + 8 + 4) * 2 * 8 * 4
+
+
+def test_common_prefix_blocks():
+    """Leading block ids shared by every request, cut to the full blocks
+    before each request's first new token."""
+    from paged_kv_cache_82_gb300.metadata import common_prefix_blocks
+    from workloads import Request
+    a = Request([7, 3, 9, 11, 4], 70, 1)       # 4 full blocks cached
+    b = Request([7, 3, 9, 12], 50, 1)          # shares 3, 3 full blocks
+    c = Request([7, 3, 9, 11, 5, 6], 90, 2)    # shares 4
+    assert common_prefix_blocks([a, c]) == 4
+    assert common_prefix_blocks([a, b, c]) == 3
+    assert common_prefix_blocks([a, Request([7, 3, 9, 11], 40, 8)]) == 2  # cut
+    assert common_prefix_blocks([Request([1, 2], 20, 1), Request([2, 1], 20, 1)]) == 0
+    assert common_prefix_blocks([a]) == 4
+    assert common_prefix_blocks([]) == 0

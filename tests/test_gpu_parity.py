@@ -71,10 +71,10 @@ def test_cfg2_full_size_elementwise():
     assert err <= ATOL["bf16"]
 
 
-def _sampled_check(wl, n_rows, seed):
+def _sampled_check(wl, n_rows, seed, cascade_blocks=None):
     """Full-size step: caches compared where the step wrote, attention on
     sampled output rows the oracle computes one by one."""
-    out, kc, vc, md, flags = gpu_step(wl)
+    out, kc, vc, md, flags = gpu_step(wl, cascade_blocks=cascade_blocks)
     assert flags == 0, f"device error flags 0x{flags:x}"
     # oracle side: copies and writes on host copies of the initial caches
     kco = oracle._as_np(wl.k_cache)[0].copy()

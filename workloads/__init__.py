@@ -338,6 +338,42 @@ def decode_step(name: str, seed: int, *, seq_lens: Sequence[int],
                          v_scale=v_scale, description=description)
 
 
+def shared_prefix_step(name: str, seed: int, *, prefix_blocks: int,
+                       private: Sequence[int], q_lens: Sequence[int],
+                       num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
+                       dtype: str = "bf16", cache_dtype: Optional[str] = None,
+                       num_blocks: Optional[int] = None, k_scale: float = 1.0,
+                       v_scale: float = 1.0, description: str = "") -> Workload:
+    """A step whose requests all begin with the same `prefix_blocks` full
+    blocks (a cached shared prefix, "01. vLLM", prefix caching): request i
+    has `private[i]` more cached tokens of its own after the prefix, then
+    q_lens[i] new tokens (written by the step).  Blocks come from a seeded
+    permutation of the pool."""
+    rng = np.random.default_rng(seed)
+    cache_dtype = cache_dtype or dtype
+    prefix = prefix_blocks * BLOCK_SIZE
+    if num_blocks is None:
+        num_blocks = prefix_blocks + sum(
+            _blocks_for(prefix + p + n) - prefix_blocks
+            for p, n in zip(private, q_lens)) + 5
+    pool = _Pool(rng, num_blocks, True)
+    shared = pool.take(prefix_blocks)
+    filled: dict = {}
+    _leading(filled, shared, prefix)
+    reqs = []
+    for p_, n in zip(private, q_lens):
+        ctx = prefix + int(p_)
+        blocks = shared + pool.take(_blocks_for(ctx + n) - prefix_blocks)
+        _leading(filled, blocks, ctx)
+        reqs.append(Request(blocks, ctx, int(n)))
+    return make_workload(name, seed, num_q_heads=num_q_heads,
+                         num_kv_heads=num_kv_heads, head_dim=head_dim,
+                         num_blocks=num_blocks, q_dtype=dtype,
+                         cache_dtype=cache_dtype, requests=reqs, filled=filled,
+                         write_new=True, k_scale=k_scale, v_scale=v_scale,
+                         shared_blocks=shared, description=description)
+
+
 # --------------------------------------------------------------------------
 # the five named configurations
 # --------------------------------------------------------------------------
