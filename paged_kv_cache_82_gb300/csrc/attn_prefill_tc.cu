@@ -63,7 +63,13 @@ namespace {
 constexpr int kTcRows = 128;               // query rows of a tile (MMA M)
 constexpr int kTcKeys = 128;               // keys of a chunk
 constexpr int kTcPages = kTcKeys / kBS;    // pages of a chunk
-constexpr int kSoftmaxWarps = 8;           // two per row quarter
+#ifndef PA_TC_SOFTMAX_WARPS
+#define PA_TC_SOFTMAX_WARPS 8
+#endif
+constexpr int kSoftmaxWarps = PA_TC_SOFTMAX_WARPS;  // 8 or 16: 2 or 4 per row quarter
+constexpr int kParts = kSoftmaxWarps / 4;           // warps sharing a row
+constexpr int kPartCols = 128 / kParts;             // a part's columns of a chunk
+static_assert(kParts == 2 || kParts == 4, "two or four softmax warps per row quarter");
 constexpr int kKWarp = kSoftmaxWarps;      // tiles, Q and K
 constexpr int kVWarp = kSoftmaxWarps + 1;  // V
 constexpr int kQkWarp = kSoftmaxWarps + 2; // S = Q.K^T MMAs (owns TMEM)
@@ -107,7 +113,7 @@ enum : int {
   kPvDone = kPFull + kSBufs,         // P.V of the buffer done: free, O updated
   kTileFull = kPvDone + kSBufs,      // tile slot filled (index and metadata)
   kTileEmpty = kTileFull + 2,        // slot read by the other 11 warps
-  kXchg = kTileEmpty + 2,            // row halves exchanged, per quarter
+  kXchg = kTileEmpty + 2,            // row parts exchanged, per quarter
   kQkDone = kXchg + 4,               // every S MMA has completed
   kPvDone2 = kQkDone + 1,            // every P.V MMA has completed
   // FP8 caches: the bf16 Q tile has landed (before its widening); the two
@@ -133,10 +139,10 @@ struct TcLayoutT {
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kTileSlot = kAbort + 4;               // int[2][kSlotInts]
-  static constexpr int kXchgSlot = kTileSlot + 2 * kSlotInts * 4;  // float[2][2][128]
+  static constexpr int kXchgSlot = kTileSlot + 2 * kSlotInts * 4;  // float[2][kParts][128]
   // the step's tile list when the kernel plans it: per request, the first
   // tile (x heads) and the tile count; block-scan scratch
-  static constexpr int kPlan = kXchgSlot + 2 * 2 * 128 * 4;  // int[2][kTcMaxSeqs]
+  static constexpr int kPlan = kXchgSlot + 2 * kParts * 128 * 4;  // int[2][kTcMaxSeqs]
   static constexpr int kScan = kPlan + 2 * kTcMaxSeqs * 4;   // int[36]
   // FP8: staging (1024-aligned for the swizzled TMA boxes), then the Q rows'
   // power-of-two shifts of the two tile slots (float[2][128])
@@ -524,7 +530,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t count = 1;
       if (i >= kPFull && i < kPFull + kSBufs) count = kSoftmaxWarps * 32;
-      if (i >= kXchg && i < kXchg + 4) count = 64;
+      if (i >= kXchg && i < kXchg + 4) count = kParts * 32;
       if (i == kTileEmpty || i == kTileEmpty + 1) count = kSoftmaxWarps + 3;
       mbar_init(bars + 8 * i, count);
     }
@@ -945,25 +951,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
     mbar_wait_bounded(bars + 8 * kPvDone2, 0);
   } else {
     // ------------------------------ softmax -------------------------------
-    // Warps w and w + 4 share the rows of lane quarter w % 4: w takes key
-    // columns 0-63 of every chunk, w + 4 columns 64-127.  The two halves of
-    // a row trade their partial max every chunk (and their partial sums at
-    // the end of the tile) through shared memory, on a per-quarter mbarrier.
-    const int quarter = warp & 3, half = warp >> 2;
+    // Warps w, w + 4, ... share the rows of lane quarter w % 4: warp w + 4 k
+    // takes key columns kPartCols k .. kPartCols (k + 1) - 1 of every chunk.
+    // The parts of a row trade their partial max every chunk (and their
+    // partial sums at the end of the tile) through shared memory, on a
+    // per-quarter mbarrier.
+    constexpr int kJ = kPartCols / 32;  // 32-column groups of a part
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;  // tensor-memory lane
     const uint32_t lrow = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_o = tmem + lrow + kColO + half * 64;
+    const uint32_t t_o = tmem + lrow + kColO + part * kPartCols;
     const uint32_t xbar = bars + 8 * (kXchg + quarter);
     float* xslot = reinterpret_cast<float*>(sp + TcLayout::kXchgSlot);
     const int it = row / G, jh = row - it * G;
     uint32_t u = 0, xk = 0;  // chunks done, exchanges done
-    // partner's value of this exchange (bounded wait); false on a timeout
-    auto exchange = [&](float mine, float& theirs) -> bool {
-      float* sl = xslot + (xk & 1) * 256;
-      sl[half * 128 + row] = mine;
+    // every part's value of this exchange (bounded wait); false on a timeout
+    auto exchange = [&](float mine, float (&all)[kParts]) -> bool {
+      float* sl = xslot + (xk & 1) * (kParts * 128);
+      sl[part * 128 + row] = mine;
       mbar_arrive(xbar);
       const bool ok = warp_wait(xbar, xk & 1, abort_flag, p.err);
-      theirs = sl[(half ^ 1) * 128 + row];
+#pragma unroll
+      for (int q = 0; q < kParts; ++q) all[q] = sl[q * 128 + row];
       ++xk;
       return ok;
     };
@@ -986,39 +995,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       for (int c = 0; c < t.nc; ++c) {
         const uint32_t uu = u + c;
         const int b = uu % kSBufs;
-        const uint32_t t_b = tmem + lrow + b * 128 + half * 64;
+        const uint32_t t_b = tmem + lrow + b * 128 + part * kPartCols;
         if (!warp_wait(bars + 8 * (kSFull + b), (uu / kSBufs) & 1, abort_flag, p.err)) {
           go = false;
           break;
         }
         tc_fence_after();
-        uint32_t sr[2][32];
-        tc_ld32(t_b, sr[0]);
-        tc_ld32(t_b + 32, sr[1]);
+        uint32_t sr[kJ][32];
+#pragma unroll
+        for (int j = 0; j < kJ; ++j) tc_ld32(t_b + j * 32, sr[j]);
         tc_wait_ld_dep(sr);
         // partial row max of the raw scores (the scale is positive); keys
         // past the row's limit (only in chunks that reach the diagonal) and
         // keys at or before lim - window (only in chunks that reach the
         // window's edge) become -inf
-        const int vis = lim - t.p0 * kBS - c * kTcKeys - half * 64;  // columns .. vis
-        const int wlo = vis - p.window;                             // columns .. wlo out
+        const int vis = lim - t.p0 * kBS - c * kTcKeys - part * kPartCols;  // columns .. vis
+        const int wlo = vis - p.window;  // columns .. wlo out
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (__any_sync(~0u, vis < 63 || wlo >= 0)) {
+        if (__any_sync(~0u, vis < kPartCols - 1 || wlo >= 0)) {
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
+          for (int j = 0; j < kPartCols; ++j)
             if (j > vis || j <= wlo) sr[j >> 5][j & 31] = __float_as_uint(-INFINITY);
         }
 #pragma unroll
-        for (int j = 0; j < 64; j += 2)
+        for (int j = 0; j < kPartCols; j += 2)
           mx4[(j >> 1) & 3] = fmax3(mx4[(j >> 1) & 3], __uint_as_float(sr[j >> 5][j & 31]),
                                     __uint_as_float(sr[j >> 5][(j & 31) + 1]));
         float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]);
-        float mx_other;
-        if (!exchange(mx, mx_other)) {
+        float mx_all[kParts];
+        if (!exchange(mx, mx_all)) {
           go = false;
           break;
         }
-        mx = fmaxf(mx, mx_other);  // the same value in both halves
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) mx = fmaxf(mx, mx_all[q]);  // the same in every part
         const float m_new = fmaxf(m_ref, mx * sscale);
         const bool grow = m_new > m_ref + kRescaleLog2;
         const float alpha = grow ? exp2f(m_ref - m_new) : 1.f;
@@ -1032,7 +1042,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
           }
           tc_fence_after();
 #pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
+          for (int j = 0; j < kJ; ++j) {
             uint32_t o[32];
             tc_ld32(t_o + j * 32, o);
             tc_wait_ld_dep(o);
@@ -1058,7 +1068,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         const float2 neg_m2 = make_float2(-m_use, -m_use);
         float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < kJ; ++j) {
           uint32_t w[32];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -1079,37 +1089,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
         mbar_arrive(bars + 8 * (kPFull + b));
       }
       if (!go) break;
-      // the row sum: both halves add the two partial sums in the same order
-      float l_other;
-      if (!exchange(l, l_other)) break;
-      const float l_tot = half == 0 ? l + l_other : l_other + l;
+      // the row sum: every part adds the partial sums in part order
+      float l_all[kParts];
+      if (!exchange(l, l_all)) break;
+      float l_tot = l_all[0];
+#pragma unroll
+      for (int q = 1; q < kParts; ++q) l_tot += l_all[q];
       const uint32_t ul = u + t.nc - 1;
       if (!warp_wait(bars + 8 * (kPvDone + ul % kSBufs), (ul / kSBufs) & 1,
                      abort_flag, p.err))
         break;
       tc_fence_after();
       const float inv = p.out_scale / l_tot;
-      // each thread writes 128 contiguous bytes of its row: 32-byte stores
-      // when the output allows them (row starts are 256-byte multiples apart)
+      // each thread writes kPartCols contiguous columns of its row: 32-byte
+      // stores when the output allows them (row starts are 256 bytes apart)
       const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
       TOut* o = static_cast<TOut*>(p.out) +
                 ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128 +
-                half * 64;
+                part * kPartCols;
       // a shared-prefix tile leaves its rows unnormalised, for the merge
       const int64_t crow =
           (int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh;
-      if (t.casc && valid && half == 0) {
+      if (t.casc && valid && part == 0) {
         p.casc_ml[crow * 2] = m_ref;
         p.casc_ml[crow * 2 + 1] = l_tot;
       }
 #pragma unroll 1
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < kJ; ++j) {
         uint32_t v[32];
         tc_ld32(t_o + j * 32, v);
         tc_wait_ld_dep(v);
         if (t.casc) {
           if (valid) {
-            float4* dst = reinterpret_cast<float4*>(p.casc_acc + crow * 128 + half * 64 + j * 32);
+            float4* dst = reinterpret_cast<float4*>(p.casc_acc + crow * 128 +
+                                                    part * kPartCols + j * 32);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               dst[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
