@@ -417,14 +417,15 @@ pa_status pa_get_device_error(pa_stream_t stream, uint32_t* flags);
  *    before any stream capture.  The address is kept until the process
  *    exits; a cudaDeviceReset invalidates it.
  *  - Every decode step needs a fixed floor of split-K partial slots (about
- *    65 KiB per SM); the scratch size is checked against that floor for up
- *    to 160 SMs when the library is compiled.
+ *    98 KiB per SM: two per resident attention CTA, up to three CTAs per
+ *    SM); the scratch size is checked against that floor for up to 160 SMs
+ *    when the library is compiled.
  *  - All calls share the one array, which keeps the previous call's
  *    contents (nothing in it needs to start at zero).  Calls whose work
  *    overlaps on the GPU -- on different streams, or from different host
  *    threads without ordering -- race on it: order them.
  */
-#define PA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define PA_NOALLOC_SCRATCH_BYTES (20u * 1024u * 1024u)
 
 pa_status pa_attention_noalloc(const void* q, pa_dtype q_dtype,
                                const void* k_cache, const void* v_cache,

@@ -2283,7 +2283,9 @@ struct HgLayout {
   using Tr = Traits<kKind>;
   static constexpr int kPageBytes = Tr::kPageBytes;          // one KV head
   static constexpr int kStageBytes = 2 * kHg * kPageBytes;   // K, V of a group
-  static constexpr int kStages = PA_HG_RING_BYTES / kStageBytes;
+  // 4-bit pages: seven stages (~60 KiB), so that three CTAs fit on an SM
+  static constexpr int kCtasPerSm = Tr::k4 ? kCtasPerSm4 : PA_CTAS_PER_SM;
+  static constexpr int kStages = Tr::k4 ? 7 : PA_HG_RING_BYTES / kStageBytes;
   static constexpr int kRing = 0;
   static constexpr int kBars = kRing + kStages * kStageBytes;
   static constexpr int kIds = kBars + 8 * 2 * kStages;       // int [2][32]
@@ -2292,6 +2294,9 @@ struct HgLayout {
   static constexpr int kScan = kPlan + kHgMaxSeqs * 16;
   static constexpr int kBytes = kScan + 34 * 8;
   static constexpr int kSmemBytes = 1024 + kBytes;           // + alignment slack
+  // (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA)
+  static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024,
+                "head-group CTAs per SM do not fit");
 };
 
 // One consumer warp's part of an item: every page of the item, its own KV
@@ -2393,7 +2398,7 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
 }
 
 template <int kKind>
-__global__ void __launch_bounds__(kThreads, PA_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, Traits<kKind>::k4 ? kCtasPerSm4 : PA_CTAS_PER_SM)
 attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ FastParams p) {

@@ -62,7 +62,11 @@ constexpr int kPrefillTileRows = 16 * PA_CONSUMER_WARPS;
 #ifndef PA_CTAS_PER_SM
 #define PA_CTAS_PER_SM 2  // resident attention CTAs per SM the kernels are built for
 #endif
-constexpr int kMaxCtasPerSm = PA_CTAS_PER_SM;  // grid bound of the attention kernels
+// the head-group decode kernel over 4-bit caches: three CTAs per SM (a
+// smaller ring; the kernel is bound by instruction issue, so more warps)
+constexpr int kCtasPerSm4 = 3;
+// grid bound of the attention kernels
+constexpr int kMaxCtasPerSm = PA_CTAS_PER_SM > kCtasPerSm4 ? PA_CTAS_PER_SM : kCtasPerSm4;
 
 // "No sliding window" inside the kernels: a row with causal limit lim sees
 // keys lim - window + 1 .. lim, so a window this wide never cuts.

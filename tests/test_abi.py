@@ -114,7 +114,7 @@ def test_step_metadata_matches_oracle_bit_exact():
 def test_workspace_size_grows_with_the_step_and_stays_bounded():
     """The workspace depends on host-known sizes only: it never shrinks when
     the step grows, it is the partial-slot floor plus a few bytes per request
-    and per query token, and the benchmark steps fit the 16 MiB scratch of
+    and per query token, and the benchmark steps fit the fixed scratch of
     pa_attention_noalloc."""
     import paged_kv_cache_82_gb300 as pa
     ws = pa.pa_attention_workspace_size
@@ -131,7 +131,8 @@ def test_workspace_size_grows_with_the_step_and_stays_bounded():
     assert ws(64, 32, 8, 128, 64, 1, 131072) == ws(64, 32, 8, 128, 64, 1, 512)
     assert ws(1142, 32, 8, 128, 121, 1022, 8193) > ws(121, 32, 8, 128, 121, 1,
                                                       8193)
-    scratch = 16 << 20
+    from tests.test_zz_no_alloc import pa_scratch_bytes
+    scratch = pa_scratch_bytes()
     for T, Hq, Hkv, B, mq, ms in ((64, 32, 8, 64, 1, 4096),        # decode
                                   (1142, 32, 8, 121, 1022, 10193),  # mixed
                                   (32, 32, 32, 32, 1, 8192),       # MHA
