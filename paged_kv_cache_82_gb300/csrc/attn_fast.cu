@@ -2049,12 +2049,47 @@ __device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
       w[k] = pack2<false>(__uint_as_float(w[k] << 16) * down,
                           __uint_as_float(w[k] & 0xFFFF0000u) * down);
   }
+  if constexpr (Tr::k4 == 1) {
+    // INT4: the K decode gives each eight elements as the pairs (0, 4),
+    // (1, 5), (2, 6), (3, 7); Q goes in the same order (the dot product is
+    // the same sum)
 #pragma unroll
-  for (int st = 0; st < 8; ++st) {
-    qa[st][0] = w[2 * st];
-    qa[st][2] = w[2 * st + 1];
-    qa[st][1] = qa[st][3] = 0u;
+    for (int j = 0; j < 4; ++j) {
+      qa[2 * j][0] = __byte_perm(w[4 * j], w[4 * j + 2], 0x5410);
+      qa[2 * j][2] = __byte_perm(w[4 * j], w[4 * j + 2], 0x7632);
+      qa[2 * j + 1][0] = __byte_perm(w[4 * j + 1], w[4 * j + 3], 0x5410);
+      qa[2 * j + 1][2] = __byte_perm(w[4 * j + 1], w[4 * j + 3], 0x7632);
+    }
+  } else {
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      qa[st][0] = w[2 * st];
+      qa[st][2] = w[2 * st + 1];
+    }
   }
+#pragma unroll
+  for (int st = 0; st < 8; ++st) qa[st][1] = qa[st][3] = 0u;
+}
+
+// eight INT4 codes (one word, element 2i in the low nibble of byte i) ->
+// the f16 pairs (0, 4), (1, 5), (2, 6), (3, 7), exact: each nibble pair
+// masked in place under the f16 pattern of 1024 (a high nibble weighs 16
+// there, undone by a fused multiply-add), offset binary code + 8 minus 8
+__device__ __forceinline__ void decode8_int4_k(uint32_t w, uint32_t (&f)[4]) {
+  const uint32_t x = w ^ 0x88888888u, y = x >> 8;
+  const __half2 off = __floats2half2_rn(1032.f, 1032.f);
+  const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
+  const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
+  uint32_t t[4] = {(x & 0x000F000Fu) | 0x64006400u, (x & 0x00F000F0u) | 0x64006400u,
+                   (y & 0x000F000Fu) | 0x64006400u, (y & 0x00F000F0u) | 0x64006400u};
+  __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t[0]), off);
+  __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&t[1]), sixteenth, off16);
+  __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&t[2]), off);
+  __half2 h3 = __hfma2(*reinterpret_cast<__half2*>(&t[3]), sixteenth, off16);
+  f[0] = *reinterpret_cast<uint32_t*>(&h0);
+  f[1] = *reinterpret_cast<uint32_t*>(&h1);
+  f[2] = *reinterpret_cast<uint32_t*>(&h2);
+  f[3] = *reinterpret_cast<uint32_t*>(&h3);
 }
 
 // eight 4-bit codes (one word, element 2i in the low nibble of byte i) ->
@@ -2136,7 +2171,10 @@ __device__ __forceinline__ void process_page_4bit(
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t f[4];
-      decode8<K4>(kw[j], f);
+      if constexpr (K4 == 1)
+        decode8_int4_k(kw[j], f);
+      else
+        decode8<K4>(kw[j], f);
       if constexpr (K4 == 2) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) f[q] = hmul2u(f[q], bsc[j >> 1]);
