@@ -33,6 +33,7 @@
 #include <float.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "pa_common.cuh"
 #include "pa_internal.h"
@@ -193,11 +194,14 @@ struct FastParams {
                       // PA_L2_PREFETCH_PAGES ahead of its loads
   // shared-prefix (cascade) steps, head-group kernel: every request's first
   // cascade_blocks pages are left to the prefix tiles (partial rows from
-  // casc_row0 on, one per token and q head); the decode segments cover the
-  // pages after them, and a segment that no range boundary cuts writes its
-  // partial to slot unc_slot0 + request * (KV heads / kHg) + head group.
+  // casc_row0 on: casc_splits key ranges of the prefix, range s at rows
+  // s * casc_split_rows + token * num_q_heads + q head); the decode segments
+  // cover the pages after them, and a segment that no range boundary cuts
+  // writes its partial to slot unc_slot0 + request * (KV heads / kHg) + head
+  // group.
   int cascade_blocks;
-  int64_t unc_slot0, casc_row0;
+  int casc_splits;
+  int64_t unc_slot0, casc_row0, casc_split_rows;
 };
 
 // ---------------------------------------------------------------------------
@@ -1907,7 +1911,8 @@ merge_self_kernel(FastParams p) {
     const int h = (g * sh + w) * p.group + (rr - i * p.group);
     return SegRow{sh == 1 ? rr : w * 8 + rr, (int64_t)(q0 + i) * p.num_q_heads + h};
   };
-  const int c0 = casc ? 1 : 0;  // the prefix's part comes first
+  // the prefix's parts (one per key range, in range order) come first
+  const int c0 = casc ? p.casc_splits : 0;
   // this CTA takes range boundaries blockIdx.x, + gridDim.x, ...
   for (int b = blockIdx.x; b < g_eff; b += gridDim.x) {
     if (b == 0) continue;
@@ -1941,7 +1946,7 @@ merge_self_kernel(FastParams p) {
       const int64_t pr_casc = p.casc_row0 + sr.row;
       combine(np + c0,
               [&](int s) -> int64_t {
-                if (s < c0) return pr_casc;
+                if (s < c0) return pr_casc + s * p.casc_split_rows;
                 s -= c0;
                 return s == 0 ? pr_tail : pr_head + (s - 1) * pr_step;
               },
@@ -1950,7 +1955,7 @@ merge_self_kernel(FastParams p) {
   }  // boundaries
   if (casc) {
     // cascade steps: a segment that no boundary cuts has one part of its
-    // own (its uncut slot), merged here with the prefix's
+    // own (its uncut slot), merged here after the prefix's
     const int H = p.num_kv_heads / sh;
     const int64_t npairs = (int64_t)p.num_seqs * H;
     for (int64_t x = blockIdx.x; x < npairs; x += gridDim.x) {
@@ -1970,7 +1975,11 @@ merge_self_kernel(FastParams p) {
       for (int y = threadIdx.x >> 5; y < sh * rows[r]; y += nwarps) {
         const SegRow sr = seg_row(g, y, rows[r], rm.q0);
         const int64_t pr_casc = p.casc_row0 + sr.row, pr_unc = unc + sr.prow;
-        combine(2, [&](int s) -> int64_t { return s == 0 ? pr_casc : pr_unc; }, sr.row);
+        combine(c0 + 1,
+                [&](int s) -> int64_t {
+                  return s < c0 ? pr_casc + s * p.casc_split_rows : pr_unc;
+                },
+                sr.row);
       }
     }
   }
@@ -2712,7 +2721,11 @@ bool use_head_groups(const AttnArgs& a, bool tc) {
 // the decode kernel, prefetching into L2 (l2_prefetch) and reading no
 // prefix from L2, keeps HBM busy on fewer SMs: the tiles get their whole
 // balanced share (the 120-decode mixed step after a 125-block prefix: 31
-// SMs; measured 13 -> 0.409 ms, 28 -> 0.387-0.392, 36-44 -> 0.394).
+// SMs; measured 13 -> 0.409 ms, 28 -> 0.387-0.392, 36-44 -> 0.394).  The
+// prefix tiles add their own time: a tile's chunk of 8 blocks takes about
+// 1 us whatever its rows (its TMA copies; FP8 pages about twice that, with
+// the widening), per 128-row tile of the decode tokens (one per request
+// taken) and KV head.
 int prefill_ctas_ahead(const AttnArgs& a, int num_sms) {
   const int64_t n_pf = a.num_tokens - a.num_seqs + 1;
   if (n_pf <= 0 || a.num_seqs <= 0 || num_sms < 16) return 0;
@@ -2723,6 +2736,15 @@ int prefill_ctas_ahead(const AttnArgs& a, int num_sms) {
     const double K = (double)a.max_seq_len;
     const double Kd = std::max(1.0, K - (double)a.cascade_blocks * kBS);
     r *= K / Kd;
+    const bool fp8 = a.cache_dtype == PA_FP8_E4M3;
+    const double elem = fp8 ? 1.0 : 2.0;
+    const double t_dec =
+        (double)a.num_seqs * Kd * a.num_kv_heads * a.head_dim * 2.0 * elem / 6e12;
+    const double tpt = std::max(1.0, 128.0 / G);
+    const double ctiles = std::ceil((double)std::min<int64_t>(a.num_tokens, a.num_seqs) / tpt);
+    const double t_pre = ctiles * a.num_kv_heads * a.cascade_blocks *
+                         (fp8 ? 0.25e-6 : 0.125e-6) / num_sms;
+    r += t_pre / t_dec;
     share = 1.0;
   }
   int p = (int)(share * num_sms * r / (1.0 + r) + 0.5);
@@ -2793,7 +2815,8 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   float* casc_ml = f.cascade_blocks > 0 ? f.ws_ml + f.casc_row0 * 2 : nullptr;
   if (tc && pf_ctas > 0) {
     e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
-                          tile_ctr, false, pf_ctas, stream, casc_acc, casc_ml);
+                          tile_ctr, false, pf_ctas, stream, casc_acc, casc_ml,
+                          f.casc_splits, f.casc_split_rows);
     if (e != cudaSuccess) return e;
   }
   e = cudaLaunchKernelEx(&cfg, attn_decode_hg_kernel<kKind>, tk, tv, f);
@@ -2802,7 +2825,7 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   if (tc) {
     e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
                           tile_ctr, pe.start == nullptr, num_sms, stream, casc_acc,
-                          casc_ml);
+                          casc_ml, f.casc_splits, f.casc_split_rows);
     if (e != cudaSuccess) return e;
   }
   if (pe.stop) cudaEventRecord(pe.stop, stream);
@@ -2898,6 +2921,11 @@ int decode_box_rows(const AttnArgs& a, bool tc) {
   return use_head_groups(a, tc) ? kHg * kBS : kBS;
 }
 
+int cascade_splits(const AttnPlan& plan, int cascade_blocks) {
+  const int want = (cascade_blocks + kCascMinSplitBlocks - 1) / kCascMinSplitBlocks;
+  return std::max(1, std::min(plan.casc_splits, want));
+}
+
 bool cascade_supported(const AttnArgs& a) {
   return a.cascade_blocks > 0 && a.window <= 0 && fast_path_supported(a) &&
          tc_prefill_supported(a) && use_head_groups(a, true);
@@ -2935,20 +2963,33 @@ AttnPlan make_plan(int64_t num_tokens, int num_q_heads, int num_kv_heads,
                 ((num_tokens * pl.group + kPrefillTileRows - 1) / kPrefillTileRows +
                  num_seqs)
           : 0;
+  pl.casc_splits = 1;
   if (pl.cascade) {
     // shared-prefix tiles: the step's tokens, per KV head, in tiles of
-    // 128 / group tokens (128 query rows)
+    // 128 / group tokens (128 query rows), for each of up to casc_splits key
+    // ranges of the prefix: as many as keep the tiles within one per SM,
+    // ranges of at least kCascMinSplitBlocks blocks of the longest prefix
+    // the step allows (its keys lie before some query: < max_seq_len)
     const int64_t tpt = std::max(1, 128 / pl.group);
-    pl.max_atoms += (int64_t)num_kv_heads * ((num_tokens + tpt - 1) / tpt);
+    const int64_t tiles = (int64_t)num_kv_heads * ((num_tokens + tpt - 1) / tpt);
+    const int64_t max_blocks = std::max<int64_t>(1, ((int64_t)max_seq_len - 1) / kBS);
+    int64_t sp = tiles > 0 ? num_sms / tiles : 1;
+    sp = std::min<int64_t>(sp, (max_blocks + kCascMinSplitBlocks - 1) / kCascMinSplitBlocks);
+    pl.casc_splits = (int)std::max<int64_t>(1, std::min<int64_t>(sp, kCascMaxSplits));
+    pl.max_atoms += tiles * pl.casc_splits;
   }
   pl.max_items = pl.max_atoms + (pl.has_decode ? (int64_t)num_seqs * num_kv_heads : 0) +
                  pl.grid_max;
   pl.max_slots = 2 * (int64_t)pl.grid_max;
   pl.unc_slots = pl.cascade && pl.has_decode ? (int64_t)num_seqs * (num_kv_heads / kHg) : 0;
-  // partial rows: the slots', then (cascade) one per token and q head
+  // partial rows: the slots', then (cascade) one per key range, token and
+  // q head
   pl.casc_row0 = (pl.max_slots + pl.unc_slots) * kHgPartRows;
+  pl.casc_split_rows = num_tokens * num_q_heads;
   const int64_t part_rows =
-      pl.has_decode ? pl.casc_row0 + (pl.cascade ? num_tokens * num_q_heads : 0) : 0;
+      pl.has_decode
+          ? pl.casc_row0 + (pl.cascade ? pl.casc_splits * pl.casc_split_rows : 0)
+          : 0;
   auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
   size_t off = 0;
   pl.off_atoms = off;       off = up(off + (size_t)pl.max_atoms * 16);
@@ -3123,6 +3164,8 @@ cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,
       // shared-prefix step: the prefix tiles' rows and the uncut suffix
       // slots follow the split slots in the partial rows
       fp.cascade_blocks = a.cascade_blocks;
+      fp.casc_splits = cascade_splits(plan, a.cascade_blocks);
+      fp.casc_split_rows = plan.casc_split_rows;
       fp.unc_slot0 = plan.max_slots;
       fp.casc_row0 = plan.casc_row0;
     }

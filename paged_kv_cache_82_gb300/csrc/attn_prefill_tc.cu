@@ -190,19 +190,23 @@ struct TcParams {
   // shared-prefix (cascade) steps: N > 0 leading block-table entries that
   // every request shares.  The prefix tiles (after the prefill tiles in the
   // list) take the tokens of the decode-class requests, all of whose keys
-  // 0 .. 16 N - 1 they see, and write partial rows (O unscaled, m, l) at
-  // casc_acc / casc_ml [token * num_q_heads + q head]
+  // 0 .. 16 N - 1 they see, in casc_splits key ranges (blocks s N / S ..
+  // (s + 1) N / S - 1), and write partial rows (O unscaled, m, l) at
+  // casc_acc / casc_ml [s * casc_split_rows + token * num_q_heads + q head]
   int cascade_blocks;
+  int casc_splits;
+  int64_t casc_split_rows;
   float* casc_acc;
   float* casc_ml;
 };
 
 // one tile, as every role of the CTA sees it: its keys are the pages
-// p0 .. p0 + pages - 1 of the request (p0 > 0 only with a sliding window).
-// A shared-prefix tile (casc) reads request 0's block-table row: tokens
-// i0 .. i0 + ntok - 1 of the step, every one of them seeing keys 0 .. L - 1.
+// p0 .. p0 + pages - 1 of the request (p0 > 0 with a sliding window, or in a
+// shared-prefix tile's key range).  A shared-prefix tile (casc) reads
+// request 0's block-table row: tokens i0 .. i0 + ntok - 1 of the step, every
+// one of them seeing all keys of the tile's range cs of the prefix 0 .. L - 1.
 struct TcTile {
-  int r, g, q0, n, L, i0, ntok, p0, pages, nc;
+  int r, g, q0, n, L, i0, ntok, p0, pages, nc, cs;
   bool ok, casc;
 };
 
@@ -210,27 +214,33 @@ struct TcTile {
 // ascending (causal limits growing), KV head fastest: from the planner's
 // list, or located in the kernel's own per-request prefix.  Past the n_real
 // prefill tiles come the shared-prefix tiles of the first casc_tok tokens
-// (tile index, then KV head fastest).
+// (key range, then tile index, then KV head fastest).
 __device__ __forceinline__ TcTile tc_tile(const TcParams& p, const int* pre,
                                           const int* ntl, int li, int n_real,
                                           int casc_tok) {
   int r, g, tt;
   if (li >= n_real) {
     const int j = li - n_real;
+    const int per_split =
+        (casc_tok + p.tokens_per_tile - 1) / p.tokens_per_tile * p.num_kv_heads;
     TcTile t{};
     t.casc = true;
-    tt = j / p.num_kv_heads;
-    t.g = j - tt * p.num_kv_heads;
+    t.cs = j / per_split;
+    const int jj = j - t.cs * per_split;
+    tt = jj / p.num_kv_heads;
+    t.g = jj - tt * p.num_kv_heads;
     t.r = 0;
     t.q0 = 0;
     t.n = casc_tok;
     t.L = p.cascade_blocks * kBS;
     t.i0 = tt * p.tokens_per_tile;
     t.ntok = min(p.tokens_per_tile, casc_tok - t.i0);
-    t.p0 = 0;
-    t.pages = p.cascade_blocks;
+    const int S = p.casc_splits;
+    t.p0 = (int)((int64_t)t.cs * p.cascade_blocks / S);
+    t.pages = (int)((int64_t)(t.cs + 1) * p.cascade_blocks / S) - t.p0;
     t.nc = (t.pages + kTcPages - 1) / kTcPages;
-    t.ok = t.ntok > 0 && p.num_seqs > 0 && p.cascade_blocks <= p.max_blocks_per_seq;
+    t.ok = t.ntok > 0 && t.pages > 0 && t.cs < S && p.num_seqs > 0 &&
+           p.cascade_blocks <= p.max_blocks_per_seq;
     return t;
   }
   if (p.self_plan) {
@@ -350,7 +360,7 @@ __device__ __forceinline__ void put_tile(volatile int* slot, int li, const TcTil
   slot[9] = t.nc;
   slot[10] = t.ok ? 1 : 0;
   slot[11] = t.p0;
-  slot[12] = t.casc ? 1 : 0;
+  slot[12] = t.casc ? 1 + t.cs : 0;
 }
 
 // The k-th tile of a warp that does not draw tiles, from slot k % 2; the
@@ -379,6 +389,7 @@ __device__ __forceinline__ int follow_tile(const TcParams& p, uint32_t bars,
   t.ok = sl[10] != 0;
   t.p0 = sl[11];
   t.casc = sl[12] != 0;
+  t.cs = t.casc ? sl[12] - 1 : 0;
   if (shifts != nullptr) *shift = shifts[s * 128 + row];
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bars + 8 * (kTileEmpty + s));
@@ -560,7 +571,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       p.self_plan ? reinterpret_cast<const int*>(sp + TcLayout::kScan)[33] : 0;
   const int n_tiles =
       n_real + (casc_tok > 0 ? (casc_tok + p.tokens_per_tile - 1) / p.tokens_per_tile *
-                                   p.num_kv_heads
+                                   p.num_kv_heads * p.casc_splits
                              : 0);
 
   // Cache rows of the tile's pages 32 G .. 32 G + 31 (four chunks), one
@@ -988,8 +999,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
       // rows past the tile's tokens compute on the tile's last limit and are
       // never stored
       const bool valid = it < t.ntok;
-      // (a shared-prefix tile: every row sees all of its keys)
-      const int lim = t.casc ? t.L - 1 : t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
+      // (a shared-prefix tile: every row sees all keys of its range, which
+      // also masks the columns of its last chunk past the range)
+      const int lim =
+          t.casc ? (t.p0 + t.pages) * kBS - 1 : t.L - t.n + t.i0 + (valid ? it : t.ntok - 1);
       float m_ref = -INFINITY, l = 0.f;
       bool go = true;
       for (int c = 0; c < t.nc; ++c) {
@@ -1108,8 +1121,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                 ((int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh) * 128 +
                 part * kPartCols;
       // a shared-prefix tile leaves its rows unnormalised, for the merge
-      const int64_t crow =
-          (int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh;
+      const int64_t crow = (int64_t)t.cs * p.casc_split_rows +
+                           (int64_t)(t.q0 + t.i0 + it) * p.num_q_heads + t.g * G + jh;
       if (t.casc && valid && part == 0) {
         p.casc_ml[crow * 2] = m_ref;
         p.casc_ml[crow * 2 + 1] = l_tot;
@@ -1223,10 +1236,14 @@ cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               const int* n_atoms, int max_atoms,
                               int dec_rows_max, int* tile_ctr, bool after_decode,
                               int num_sms, cudaStream_t stream, float* casc_acc,
-                              float* casc_ml) {
+                              float* casc_ml, int casc_splits,
+                              int64_t casc_split_rows) {
   TcParams p{};
-  if (self_plan && a.cascade_blocks > 0 && casc_acc && casc_ml) {
+  p.casc_splits = 1;
+  if (self_plan && a.cascade_blocks > 0 && casc_acc && casc_ml && casc_splits >= 1) {
     p.cascade_blocks = a.cascade_blocks;
+    p.casc_splits = casc_splits;
+    p.casc_split_rows = casc_split_rows;
     p.casc_acc = casc_acc;
     p.casc_ml = casc_ml;
   }

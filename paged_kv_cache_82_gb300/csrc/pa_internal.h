@@ -103,7 +103,22 @@ struct AttnPlan {
   // (token, q head) for the shared prefix (casc_row0 onwards)
   int cascade;
   int64_t unc_slots, casc_row0;
+  // the prefix's key ranges (one tile, and one partial row per token and q
+  // head, each): room for casc_splits ranges of casc_split_rows rows
+  int casc_splits;
+  int64_t casc_split_rows;
 };
+
+// Shared-prefix tiles split the prefix into key ranges of at least
+// kCascMinSplitBlocks blocks (four chunks of the tensor-core kernel), at most
+// kCascMaxSplits ranges, so that a long prefix read by few tokens still
+// spreads over the SMs.
+constexpr int kCascMinSplitBlocks = 32;
+constexpr int kCascMaxSplits = 32;
+
+// key ranges of a cascade step's prefix of cascade_blocks blocks (<= the
+// plan's casc_splits)
+int cascade_splits(const AttnPlan& plan, int cascade_blocks);
 
 // Host planning from host-known sizes only (no device read-back).
 // window: the sliding window in keys (0: none; a window of at least
@@ -178,13 +193,15 @@ bool encode_prefill_tensor_maps(const AttnArgs& a, TcMaps* maps);
 // tiles drawn dynamically; after_decode: launched right behind the step's
 // decode kernel, whose output it does not read (starts as its CTAs retire).
 // casc_acc / casc_ml: the shared-prefix tiles' partial rows (cascade steps,
-// a.cascade_blocks > 0, self-planned only).
+// a.cascade_blocks > 0, self-planned only): casc_splits key ranges of the
+// prefix, range s at rows s * casc_split_rows + token * num_q_heads + head.
 cudaError_t launch_prefill_tc(const AttnArgs& a, const TcMaps& maps,
                               bool self_plan, const int4* atoms,
                               const int* n_atoms, int max_atoms,
                               int dec_rows_max, int* tile_ctr, bool after_decode,
                               int num_sms, cudaStream_t stream,
-                              float* casc_acc = nullptr, float* casc_ml = nullptr);
+                              float* casc_acc = nullptr, float* casc_ml = nullptr,
+                              int casc_splits = 1, int64_t casc_split_rows = 0);
 
 // plan kernel + (tensor-core prefill kernel) + main kernel + split merge
 cudaError_t launch_attention_fast(const AttnArgs& a, const AttnPlan& plan,

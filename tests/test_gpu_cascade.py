@@ -79,6 +79,34 @@ def test_mixed_step_with_shared_prefix(cache_dtype):
     _check(wl, 7)
 
 
+# A long prefix is split into key ranges of at least 32 blocks, each with a
+# tile and a partial row of its own, merged in range order: ranges of
+# unequal length, several token tiles per range, FP8 pages, G = 8, and a
+# prefix far longer than the requests' own contexts (many ranges).
+@pytest.mark.parametrize("prefix_blocks,n_req,cache_dtype,Hq", [
+    (100, 8, "bf16", 32),     # 4 ranges of 25 blocks
+    (77, 40, "bf16", 32),     # 3 ranges (25, 26, 26 blocks), two token tiles
+    (1000, 3, "bf16", 32),    # 19 ranges of 52 or 53 blocks
+    (300, 5, "e4m3", 32),
+    (70, 9, "f16", 64),       # G = 8: tiles of 16 tokens
+])
+def test_long_prefix_in_key_ranges(prefix_blocks, n_req, cache_dtype, Hq):
+    dtype = "f16" if cache_dtype == "f16" else "bf16"
+    private = [PRIVATE[i % len(PRIVATE)] for i in range(n_req)]
+    wl = _step(prefix_blocks, private, [1] * n_req, Hq=Hq, cache_dtype=cache_dtype,
+               dtype=dtype, seed=82310 + prefix_blocks)
+    _check(wl, prefix_blocks)
+
+
+def test_long_prefix_mixed_step():
+    # a chunked prefill (its own tiles, whole rows) beside decodes whose
+    # 90-block prefix runs in key ranges
+    private = PRIVATE + [40]
+    q_lens = [1] * len(PRIVATE) + [200]
+    wl = _step(90, private, q_lens, seed=82320)
+    _check(wl, 90)
+
+
 def test_prefill_requests_first_and_decodes_after():
     # the prefix tiles take the tokens up to the last decode-class request's
     # (rows of prefill requests among them are computed and not used)
