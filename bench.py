@@ -152,7 +152,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
-def _device_inputs(wl, dev):
+def _device_inputs(wl, dev, casc=None):
     import torch
     from paged_kv_cache_82_gb300.metadata import build_step_metadata
     md = build_step_metadata(wl.requests)
@@ -172,10 +172,14 @@ def _device_inputs(wl, dev):
         d["pairs"] = torch.tensor(wl.copy_pairs, dtype=torch.int64, device=dev)
     d["out"] = torch.empty_like(d["q"])
     import paged_kv_cache_82_gb300 as pa
-    from paged_kv_cache_82_gb300.metadata import common_prefix_blocks
-    # a step whose requests share leading blocks runs as a cascade (the
-    # engine knows the shared prefix from its block manager)
-    d["casc"] = common_prefix_blocks(wl.requests)
+    from paged_kv_cache_82_gb300.metadata import cascade_prefix_blocks
+    # a step whose requests share leading blocks runs as a cascade where
+    # that measured faster (the engine knows the shared prefix from its
+    # block manager); casc forces a prefix length (0: the plain step)
+    if casc is None:
+        casc = cascade_prefix_blocks(wl.requests,
+                                     wl.num_q_heads // wl.num_kv_heads)
+    d["casc"] = casc
     size_fn = (pa.pa_attention_cascade_workspace_size if d["casc"] > 0
                else pa.pa_attention_workspace_size)
     nbytes = size_fn(wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
@@ -208,6 +212,29 @@ def _step(pa, wl, d):
                         wl.k_scale, wl.v_scale, out=d["out"], workspace=d["ws"],
                         cache_dtype=cdt)
     return pa.pa_launch_count() - n0
+
+
+def _cascade_vs_plain(pa, wl, dev, steps, warmup, flush):
+    """Step time of a shared-prefix step run as a cascade (the prefix forced)
+    and as the plain step, and the prefix length the host policy picks."""
+    import torch
+    from paged_kv_cache_82_gb300.metadata import (cascade_prefix_blocks,
+                                                  common_prefix_blocks)
+    res = {}
+    for mode, n in (("cascade", common_prefix_blocks(wl.requests)),
+                    ("plain", 0)):
+        d = _device_inputs(wl, dev, casc=n)
+        st, _, _ = _time_steps(pa, wl, d, steps, warmup, flush)
+        flags = pa.pa_get_device_error()
+        if flags:
+            raise RuntimeError(f"device error flags 0x{flags:x} ({mode})")
+        res[mode + "_ms"] = statistics.median(st)
+        del d
+        torch.cuda.empty_cache()
+    res["speedup"] = res["plain_ms"] / res["cascade_ms"]
+    res["policy_blocks"] = cascade_prefix_blocks(
+        wl.requests, wl.num_q_heads // wl.num_kv_heads)
+    return res
 
 
 def _time_steps(pa, wl, d, steps, warmup, flush):
@@ -495,6 +522,24 @@ def run_ours(args):
     pa.load_library()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    if args.only == "cascade-sweep":
+        # the cascade's crossover: decode steps behind a shared prefix,
+        # cascade against plain, over prefix lengths and request counts
+        for priv in ((256, 2048), (1024, 8192)):
+            for pb in (32, 64, 128, 256, 512, 1024, 4096):
+                for n in (2, 8, 32, 64, 128):
+                    if priv[0] == 1024 and (pb not in (128, 256) or n not in (8, 32)):
+                        continue
+                    wls = workloads.shared_prefix_decode(n, pb, *priv)
+                    r = _cascade_vs_plain(pa, wls, dev, args.steps, args.warmup,
+                                          flush)
+                    print(json.dumps({"prefix_blocks": pb, "decodes": n,
+                                      "private": list(priv), **{
+                                          k: round(v, 4) if isinstance(v, float)
+                                          else v for k, v in r.items()}}),
+                          flush=True)
+        return
+
     if args.only != "all":
         make = {"decode": workloads.config2, "mixed": workloads.config4,
                 "prefill": workloads.prefill_chunk, "mha": workloads.config3,
@@ -585,6 +630,22 @@ def run_ours(args):
         "attention_kernels_ms": statistics.mean(m_kern),
     }
     del d4
+
+    # ---- decodes behind a long shared prefix: the cascade against the
+    # plain step (the prefix read once per KV head, in key ranges)
+    wls = workloads.shared_prefix_decode()
+    sp = _cascade_vs_plain(pa, wls, dev, max(3, args.steps // 10), args.warmup,
+                           flush)
+    shared_prefix = {
+        "workload": ("Llama-3.1-8B shape, bf16: " + wls.description +
+                     "; 32 K/V writes, attention"),
+        "unique_kv_bytes": wls.kv_bytes(),
+        "logical_kv_bytes": wls.kv_bytes(unique=False),
+        "tbs_unique_cascade": (wls.kv_bytes() + wls.qo_bytes()) /
+                              (sp["cascade_ms"] * 1e-3) / 1e12,
+        **sp,
+    }
+    del wls
 
     # ---- the other decode workloads of the scope (kernel and step TB/s)
     others = {}
@@ -703,6 +764,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clocks,
         "mixed_step": mixed,
+        "shared_prefix_decode": shared_prefix,
         "prefill_step": prefill,
         "prefill_step_fp8": prefill_fp8,
         "other_decodes": others,
@@ -784,10 +846,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["all", "decode", "mixed", "prefill",
                                        "mha", "fp8long", "int4", "nvfp4",
-                                       "prefillfp8"],
+                                       "prefillfp8", "cascade-sweep"],
                     default="all",
                     help="profiling runs: time just one step kind, no JSON "
-                         "line")
+                         "line (cascade-sweep: one JSON line per shared-"
+                         "prefix decode step, cascade against plain)")
     ap.add_argument("--batch", type=int, default=0,
                     help="with --only decode/mha/fp8long/mixed: that many "
                          "(decode) requests instead of the workload's own")

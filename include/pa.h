@@ -320,7 +320,17 @@ pa_status pa_attention_window_workspace_size(int64_t num_tokens,
  * E4M3 caches, a positive scale, KV heads a multiple of 4, at most 512
  * requests) the N prefix blocks are read once per KV head, for the query
  * rows of every request of at most 8 rows per KV head, on the tensor
- * cores; elsewhere N is not used.  The statement is checked on the device:
+ * cores, in up to 32 key ranges of at least 32 blocks each (a partial row
+ * per range, merged in range order); elsewhere N is not used.
+ *
+ * The cascade is the caller's choice, and it is not always the faster one:
+ * it adds the prefix tiles' start-up and a merge part per key range.
+ * Measured on a GB300 (decode steps of the Llama-3.1-8B shape, bf16), it
+ * beat the plain step wherever N >= 512, or N x (requests of at most 8 rows)
+ * >= 8192 (e.g. 1.04x at 512 blocks x 8 requests, 2.8x at 1024 x 32, 12x at
+ * 4096 x 128), and lost to it below that with few requests (0.69x at 32
+ * blocks x 2 requests).  With a single request nothing is shared: call
+ * pa_attention.  The statement is checked on the device:
  * a request whose block-table row or key count breaks it sets
  * PA_DEV_ERR_METADATA (pa_get_device_error) and the step's output is then
  * undefined.  The workspace must hold pa_attention_cascade_workspace_size
@@ -342,8 +352,11 @@ pa_status pa_attention_cascade(const void* q, pa_dtype q_dtype,
 /*
  * pa_attention_cascade_workspace_size -- bytes of device workspace
  * pa_attention_cascade needs: pa_attention's, plus one partial row
- * ((head_dim + 2) x 4 bytes) per token and q head for the shared prefix and
- * 32 per request and group of 4 KV heads for the requests' own parts.
+ * ((head_dim + 2) x 4 bytes) per token, q head and key range of the shared
+ * prefix (the ranges: as many as keep the prefix tiles within one per SM,
+ * at most 32, and at most one per 32 blocks of a max_seq_len - 1 key
+ * prefix) and 32 per request and group of 4 KV heads for the requests' own
+ * parts.
  */
 pa_status pa_attention_cascade_workspace_size(int64_t num_tokens,
                                               int num_q_heads, int num_kv_heads,

@@ -20,6 +20,8 @@ Input: a sequence of requests with ``block_ids``, ``num_computed`` and
 ``common_prefix_blocks`` gives the number of leading block ids that every
 request of the step shares and whose keys precede every request's queries:
 the shared prefix a cascade step (pa_attention_cascade) reads once.
+``cascade_prefix_blocks`` gives it only where the cascade is the faster way
+to run the step (a measured crossover), else 0.
 """
 from __future__ import annotations
 
@@ -82,3 +84,28 @@ def common_prefix_blocks(requests) -> int:
             k += 1
         n = k
     return int(n)
+
+
+# Where a cascade step beats the plain step (decode steps of the
+# Llama-3.1-8B shape on a GB300, bf16, private contexts of 256 - 8192 tokens
+# after the prefix): a prefix of at least CASCADE_MIN_BLOCKS blocks, or
+# prefix blocks x decode requests of at least CASCADE_MIN_BLOCK_READS.  Below
+# that the plain step re-reads the prefix from L2 for less than the cascade's
+# fixed costs (the prefix tiles' start-up and the extra merge parts).
+CASCADE_MIN_BLOCKS = 512
+CASCADE_MIN_BLOCK_READS = 8192
+
+
+def cascade_prefix_blocks(requests, group: int) -> int:
+    """The shared prefix to run as a cascade (pa_attention_cascade's
+    cascade_blocks), or 0 where the plain step is faster.  Only the
+    decode-class requests (at most 8 query rows: q_len x group <= 8) read the
+    prefix once through the cascade; prefill requests read their whole row
+    either way.  Needs at least two of them."""
+    n = common_prefix_blocks(requests)
+    dec = sum(1 for r in requests if 0 < r.num_new and r.num_new * group <= 8)
+    if n <= 0 or dec < 2:
+        return 0
+    if n >= CASCADE_MIN_BLOCKS or n * dec >= CASCADE_MIN_BLOCK_READS:
+        return int(n)
+    return 0

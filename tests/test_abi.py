@@ -176,3 +176,33 @@ def test_common_prefix_blocks():
     assert common_prefix_blocks([Request([1, 2], 20, 1), Request([2, 1], 20, 1)]) == 0
     assert common_prefix_blocks([a]) == 4
     assert common_prefix_blocks([]) == 0
+
+
+def test_cascade_policy():
+    """The cascade is chosen only where it measured faster: at least two
+    decode requests, and a long prefix or many requests behind it."""
+    from paged_kv_cache_82_gb300.metadata import (
+        CASCADE_MIN_BLOCK_READS, CASCADE_MIN_BLOCKS, cascade_prefix_blocks)
+    from workloads import Request
+
+    def step(prefix, n_dec, q=1, extra=()):
+        shared = list(range(prefix))
+        reqs = [Request(shared + [10000 + i], prefix * 16 + 5, q)
+                for i in range(n_dec)]
+        return reqs + list(extra)
+
+    assert cascade_prefix_blocks(step(600, 1), 4) == 0           # nothing shared
+    assert cascade_prefix_blocks(step(600, 2), 4) == 600
+    assert cascade_prefix_blocks(step(256, 2), 4) == 0
+    assert cascade_prefix_blocks(step(128, 64), 4) == 128
+    assert cascade_prefix_blocks(step(128, 32), 4) == 0
+    assert 128 * 64 >= CASCADE_MIN_BLOCK_READS > 128 * 32
+    assert 600 >= CASCADE_MIN_BLOCKS > 256
+    # query rows: q_len x group <= 8 is a decode (G = 4: two tokens)
+    assert cascade_prefix_blocks(step(600, 2, q=2), 4) == 600
+    assert cascade_prefix_blocks(step(600, 2, q=3), 4) == 0
+    # a prefill request behind the same prefix counts for the prefix, not
+    # as a reader of it
+    pf = Request(list(range(600)) + [20000, 20001], 600 * 16, 30)
+    assert cascade_prefix_blocks(step(600, 1, extra=[pf]), 4) == 0
+    assert cascade_prefix_blocks(step(600, 2, extra=[pf]), 4) == 600
