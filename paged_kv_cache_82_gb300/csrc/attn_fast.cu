@@ -1782,7 +1782,9 @@ constexpr int kMergeThreads = PA_MERGE_THREADS;  // merge_self_kernel CTA
 
 // (at most 64 registers a thread: a merge CTA fits beside the two decode
 // CTAs of an SM, so that its plan runs while the attention kernel does)
-template <typename TOut>
+// kCasc: a cascade step (p.cascade_blocks > 0); the plain steps' build has
+// none of the cascade's code
+template <typename TOut, bool kCasc>
 __global__ void __launch_bounds__(kMergeThreads, 4)
 merge_self_kernel(FastParams p) {
   extern __shared__ long long mplan[];
@@ -1802,8 +1804,7 @@ merge_self_kernel(FastParams p) {
   // partial slots hold kHg x 8 rows)
   const int sh = p.seg_heads;
   const int part_rows = sh == 1 ? 16 : kHgPartRows;
-  const bool casc = p.cascade_blocks > 0;
-  if (casc) {
+  if constexpr (kCasc) {
     // a cascade step's requests all start with request 0's first
     // cascade_blocks block-table entries (checked while the attention runs)
     const int64_t total = (int64_t)p.num_seqs * p.cascade_blocks;
@@ -1912,7 +1913,7 @@ merge_self_kernel(FastParams p) {
     return SegRow{sh == 1 ? rr : w * 8 + rr, (int64_t)(q0 + i) * p.num_q_heads + h};
   };
   // the prefix's parts (one per key range, in range order) come first
-  const int c0 = casc ? p.casc_splits : 0;
+  const int c0 = kCasc ? p.casc_splits : 0;
   // this CTA takes range boundaries blockIdx.x, + gridDim.x, ...
   for (int b = blockIdx.x; b < g_eff; b += gridDim.x) {
     if (b == 0) continue;
@@ -1953,7 +1954,7 @@ merge_self_kernel(FastParams p) {
               sr.row);
     }
   }  // boundaries
-  if (casc) {
+  if constexpr (kCasc) {
     // cascade steps: a segment that no boundary cuts has one part of its
     // own (its uncut slot), merged here after the prefix's
     const int H = p.num_kv_heads / sh;
@@ -2834,7 +2835,9 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
   cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
   attr[0].val.programmaticStreamSerializationAllowed =
       (pe.start == nullptr && !tc) ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
+  e = f.cascade_blocks > 0
+          ? cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>, true>, f)
+          : cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>, false>, f);
   if (e == cudaSuccess) count_launch();
   return e;
 }
@@ -2904,7 +2907,7 @@ cudaError_t launch_kind(const AttnArgs& a, const FastParams& fp, PlanArgs pa,
     if (f.self_plan) {
       cfg.blockDim = dim3(kMergeThreads);
       cfg.dynamicSmemBytes = (size_t)f.num_seqs * 16;
-      e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>>, f);
+      e = cudaLaunchKernelEx(&cfg, merge_self_kernel<OutT<kKind>, false>, f);
     } else {
       cfg.blockDim = dim3(128);
       cfg.dynamicSmemBytes = 0;
