@@ -78,6 +78,16 @@ static_assert(kHgPartRows == kPartialRowsPerSlot, "partial slot rows");
 #ifndef PA_STAGES_16BIT
 #define PA_STAGES_16BIT 8       // ring depth in pages, bf16 / fp16 caches
 #endif
+// head_dim 64 in the head-group kernel: three CTAs per SM with four-stage
+// rings (64 KiB) instead of two with six, the same bytes in flight per SM and
+// half again the warps (Llama-3.1-8B-shaped batch at D = 64: kernel 0.0560
+// -> 0.0539-0.0545 ms)
+#ifndef PA_HG_D64_CTAS
+#define PA_HG_D64_CTAS 3
+#endif
+#ifndef PA_HG_D64_STAGES
+#define PA_HG_D64_STAGES 4  // (0: the ring's bytes, PA_HG_RING_BYTES)
+#endif
 #ifndef PA_HG_RING_BYTES
 #define PA_HG_RING_BYTES 98304  // ring of the head-group kernel (96 KiB)
 #endif
@@ -2332,8 +2342,12 @@ struct HgLayout {
   static constexpr int kPageBytes = Tr::kPageBytes;          // one KV head
   static constexpr int kStageBytes = 2 * kHg * kPageBytes;   // K, V of a group
   // 4-bit pages: seven stages (~60 KiB), so that three CTAs fit on an SM
-  static constexpr int kCtasPerSm = Tr::k4 ? kCtasPerSm4 : PA_CTAS_PER_SM;
-  static constexpr int kStages = Tr::k4 ? 7 : PA_HG_RING_BYTES / kStageBytes;
+  static constexpr int kCtasPerSm =
+      Tr::k4 ? kCtasPerSm4 : (Tr::kD == 64 ? PA_HG_D64_CTAS : PA_CTAS_PER_SM);
+  static constexpr int kStages =
+      Tr::k4 ? 7
+             : (Tr::kD == 64 && PA_HG_D64_STAGES > 0 ? PA_HG_D64_STAGES
+                                                      : PA_HG_RING_BYTES / kStageBytes);
   static constexpr int kRing = 0;
   static constexpr int kBars = kRing + kStages * kStageBytes;
   static constexpr int kIds = kBars + 8 * 2 * kStages;       // int [2][32]
@@ -2345,6 +2359,7 @@ struct HgLayout {
   // (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA)
   static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024,
                 "head-group CTAs per SM do not fit");
+  static_assert(kCtasPerSm <= kMaxCtasPerSm, "partial slots sized for fewer CTAs per SM");
 };
 
 // One consumer warp's part of an item: every page of the item, its own KV
@@ -2446,7 +2461,7 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
 }
 
 template <int kKind>
-__global__ void __launch_bounds__(kThreads, Traits<kKind>::k4 ? kCtasPerSm4 : PA_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, HgLayout<kKind>::kCtasPerSm)
 attn_decode_hg_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v,
                       const __grid_constant__ FastParams p) {
