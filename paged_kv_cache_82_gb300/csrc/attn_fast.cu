@@ -2091,17 +2091,24 @@ __device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
   for (int st = 0; st < 8; ++st) qa[st][1] = qa[st][3] = 0u;
 }
 
+// Offset binary of a masked nibble pair under the f16 pattern of 1024 in
+// one logic operation: (x ^ 0x8 per nibble) & mask | 0x6400 per half equals
+// (x & mask) ^ (0x8 per nibble | 0x6400 per half), the 0x6400 bits lying
+// outside the mask.
+constexpr uint32_t kNibLo = 0x000F000Fu, kNibLoFlip = 0x64086408u;  // low nibbles
+constexpr uint32_t kNibHi = 0x00F000F0u, kNibHiFlip = 0x64806480u;  // high nibbles
+
 // eight INT4 codes (one word, element 2i in the low nibble of byte i) ->
 // the f16 pairs (0, 4), (1, 5), (2, 6), (3, 7), exact: each nibble pair
 // masked in place under the f16 pattern of 1024 (a high nibble weighs 16
 // there, undone by a fused multiply-add), offset binary code + 8 minus 8
 __device__ __forceinline__ void decode8_int4_k(uint32_t w, uint32_t (&f)[4]) {
-  const uint32_t x = w ^ 0x88888888u, y = x >> 8;
+  const uint32_t y = w >> 8;
   const __half2 off = __floats2half2_rn(1032.f, 1032.f);
   const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
   const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
-  uint32_t t[4] = {(x & 0x000F000Fu) | 0x64006400u, (x & 0x00F000F0u) | 0x64006400u,
-                   (y & 0x000F000Fu) | 0x64006400u, (y & 0x00F000F0u) | 0x64006400u};
+  uint32_t t[4] = {(w & kNibLo) ^ kNibLoFlip, (w & kNibHi) ^ kNibHiFlip,
+                   (y & kNibLo) ^ kNibLoFlip, (y & kNibHi) ^ kNibHiFlip};
   __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t[0]), off);
   __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&t[1]), sixteenth, off16);
   __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&t[2]), off);
@@ -2302,12 +2309,11 @@ __device__ __forceinline__ void process_page_4bit(
     const uint32_t xcd = __byte_perm(wc, wd, sel);
     uint32_t a[4];
     if constexpr (K4 == 1) {
-      const uint32_t u = xab ^ 0x00880088u, v = xcd ^ 0x00880088u;
       const __half2 off = __floats2half2_rn(1032.f, 1032.f);
       const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
       const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
-      uint32_t t0 = (u & 0x000F000Fu) | 0x64006400u, t1 = (u & 0x00F000F0u) | 0x64006400u;
-      uint32_t t2 = (v & 0x000F000Fu) | 0x64006400u, t3 = (v & 0x00F000F0u) | 0x64006400u;
+      uint32_t t0 = (xab & kNibLo) ^ kNibLoFlip, t1 = (xab & kNibHi) ^ kNibHiFlip;
+      uint32_t t2 = (xcd & kNibLo) ^ kNibLoFlip, t3 = (xcd & kNibHi) ^ kNibHiFlip;
       __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t0), off);
       __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&t1), sixteenth, off16);
       __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&t2), off);
