@@ -2150,6 +2150,31 @@ __device__ __forceinline__ void decode8(uint32_t w, uint32_t (&f)[4]) {
   }
 }
 
+// the two E2M1 codes of byte b of w (low nibble first) -> f16 pair (exact);
+// b is a constant after unrolling, so the switch folds away
+__device__ __forceinline__ uint32_t e2m1x2_byte(uint32_t w, int b) {
+  uint32_t r;
+  switch (b) {
+    case 0:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t}" : "=r"(r) : "r"(w));
+      break;
+    case 1:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b1;\n\t}" : "=r"(r) : "r"(w));
+      break;
+    case 2:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b2;\n\t}" : "=r"(r) : "r"(w));
+      break;
+    default:
+      asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %1;\n\t"
+          "cvt.rn.f16x2.e2m1x2 %0, b3;\n\t}" : "=r"(r) : "r"(w));
+      break;
+  }
+  return r;
+}
+
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
                       *reinterpret_cast<const __half2*>(&b));
@@ -2304,11 +2329,11 @@ __device__ __forceinline__ void process_page_4bit(
     const uint32_t wb = (mt >> 2) ? vw[1].y : vw[1].x;
     const uint32_t wc = (mt >> 2) ? vw[2].y : vw[2].x;
     const uint32_t wd = (mt >> 2) ? vw[3].y : vw[3].x;
-    // byte mt of keys (0, 1) in bytes 0 and 2, of keys (2, 3) likewise
-    const uint32_t xab = __byte_perm(wa, wb, sel);
-    const uint32_t xcd = __byte_perm(wc, wd, sel);
     uint32_t a[4];
     if constexpr (K4 == 1) {
+      // byte mt of keys (0, 1) in bytes 0 and 2, of keys (2, 3) likewise
+      const uint32_t xab = __byte_perm(wa, wb, sel);
+      const uint32_t xcd = __byte_perm(wc, wd, sel);
       const __half2 off = __floats2half2_rn(1032.f, 1032.f);
       const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
       const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
@@ -2323,20 +2348,14 @@ __device__ __forceinline__ void process_page_4bit(
       a[2] = *reinterpret_cast<uint32_t*>(&h2);
       a[3] = *reinterpret_cast<uint32_t*>(&h3);
     } else {
-      // nibble pairs (key 0, key 1) as one byte each, then E2M1 -> f16
-      const uint32_t lo = xab & 0x000F000Fu, hi = (xab >> 4) & 0x000F000Fu;
-      const uint32_t lo2 = xcd & 0x000F000Fu, hi2 = (xcd >> 4) & 0x000F000Fu;
-      // bytes: (key 0 | key 1 << 4) low nibbles, high nibbles, then keys 2, 3
-      const uint32_t packed =
-          __byte_perm(__byte_perm(lo | (lo >> 12), hi | (hi >> 12), 0x0040),
-                      __byte_perm(lo2 | (lo2 >> 12), hi2 | (hi2 >> 12), 0x0040),
-                      0x5410);
-      uint32_t f[4];
-      decode8<2>(packed, f);
-      a[0] = hmul2u(f[0], vsc[0]);
-      a[1] = hmul2u(f[1], vsc[0]);
-      a[2] = hmul2u(f[2], vsc[1]);
-      a[3] = hmul2u(f[3], vsc[1]);
+      // each key's byte mt -> its (row r, row r + 8) pair, then the pairs of
+      // keys (0, 1) and (2, 3) regrouped by row
+      const uint32_t k0 = e2m1x2_byte(wa, m), k1 = e2m1x2_byte(wb, m);
+      const uint32_t k2 = e2m1x2_byte(wc, m), k3 = e2m1x2_byte(wd, m);
+      a[0] = hmul2u(__byte_perm(k0, k1, 0x5410), vsc[0]);
+      a[1] = hmul2u(__byte_perm(k0, k1, 0x7632), vsc[0]);
+      a[2] = hmul2u(__byte_perm(k2, k3, 0x5410), vsc[1]);
+      a[3] = hmul2u(__byte_perm(k2, k3, 0x7632), vsc[1]);
     }
     mma16816<false>(st.o[mt], a, b0, b1);
   }
