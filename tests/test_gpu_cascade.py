@@ -178,3 +178,14 @@ def test_mixed_step_full_size_sampled():
     blocks), with the prefix as a cascade: sampled rows against the oracle."""
     wl = workloads.config4()
     _sampled_check(wl, 48, 41, cascade_blocks=len(wl.shared_blocks))
+
+
+def test_shared_prefix_decode_full_size_sampled():
+    """The bench's shared-prefix decode step: 32 decodes behind a 1024-block
+    (16,384-token) prefix, run as a cascade in key ranges (as many as keep
+    the prefix tiles within one per SM): sampled rows against the oracle."""
+    wl = workloads.shared_prefix_decode()
+    from paged_kv_cache_82_gb300.metadata import cascade_prefix_blocks
+    n = cascade_prefix_blocks(wl.requests, wl.num_q_heads // wl.num_kv_heads)
+    assert n == len(wl.shared_blocks) == 1024
+    _sampled_check(wl, 32, 43, cascade_blocks=n)
