@@ -50,6 +50,8 @@ import struct
 from dataclasses import dataclass, field
 from typing import Dict, Iterator, List, Optional, Sequence, Tuple
 
+import numpy as np
+
 BLOCK_SIZE = 16
 
 
@@ -126,13 +128,16 @@ def hash_block(parent: Optional[bytes], token_ids: Sequence[int],
     """SHA-256 over the parent block's hash, the block's token ids and its
     extra keys, in a fixed encoding (a present parent and an absent one, or
     different extra keys, never encode alike)."""
-    h = hashlib.sha256()
-    if parent is None:
-        h.update(b"\x00")
-    else:
-        h.update(b"\x01" + parent)
-    h.update(struct.pack(f"<I{len(token_ids)}q", len(token_ids),
-                         *[int(t) for t in token_ids]))
+    ids = np.asarray(token_ids, dtype="<i8")
+    return _hash_encoded(parent, struct.pack("<I", len(ids)) + ids.tobytes(), extra)
+
+
+def _hash_encoded(parent: Optional[bytes], ids: bytes,
+                  extra: Optional[Tuple] = None) -> bytes:
+    """hash_block with the token ids already encoded (count, then each id as
+    a little-endian int64)."""
+    h = hashlib.sha256(b"\x00" if parent is None else b"\x01" + parent)
+    h.update(ids)
     if extra:
         h.update(b"\x02" + repr(tuple(extra)).encode())
     return h.digest()
@@ -206,6 +211,9 @@ class SeqState:
     block_hashes: List[bytes] = field(default_factory=list)
     num_cached_blocks: int = 0    # leading blocks registered in the cache
     arrival: int = 0
+    # the ids of `blocks`, kept alongside it (a step's block-table row is a
+    # copy of this list, not a walk over the blocks)
+    block_ids: List[int] = field(default_factory=list)
 
     @property
     def num_tokens(self) -> int:
@@ -236,13 +244,20 @@ class KVCacheManager:
     # -- hashes --------------------------------------------------------------
     def _extend_hashes(self, seq: SeqState) -> None:
         bs = self.block_size
-        while len(seq.block_hashes) < seq.num_tokens // bs:
-            k = len(seq.block_hashes)
+        k0, k1 = len(seq.block_hashes), seq.num_tokens // bs
+        if k1 <= k0:
+            return
+        # the new full blocks' ids, encoded once (hash_block's encoding)
+        ids = np.asarray(seq.token_ids[k0 * bs:k1 * bs], dtype="<i8").tobytes()
+        count = struct.pack("<I", bs)
+        step = 8 * bs
+        for k in range(k0, k1):
             parent = seq.block_hashes[-1] if k else None
             extra = (("salt", seq.cache_salt),) if (k == 0 and seq.cache_salt) \
                 else None
+            off = (k - k0) * step
             seq.block_hashes.append(
-                hash_block(parent, seq.token_ids[k * bs:(k + 1) * bs], extra))
+                _hash_encoded(parent, count + ids[off:off + step], extra))
 
     # -- admission -----------------------------------------------------------
     def computed_blocks(self, seq: SeqState) -> List[KVBlock]:
@@ -265,6 +280,7 @@ class KVCacheManager:
         for b in hits:
             self.pool.touch(b)
         seq.blocks = list(hits)
+        seq.block_ids = [b.block_id for b in hits]
         seq.num_computed = len(hits) * self.block_size
         seq.num_cached_blocks = len(hits)
 
@@ -296,10 +312,13 @@ class KVCacheManager:
             new = self.pool.allocate()
             copies.append((old.block_id, new.block_id))
             seq.blocks[k] = new
+            seq.block_ids[k] = new.block_id
             self.pool.release(old)
         total = -(-(seq.num_computed + num_new) // self.block_size)
         while len(seq.blocks) < total:
-            seq.blocks.append(self.pool.allocate())
+            b = self.pool.allocate()
+            seq.blocks.append(b)
+            seq.block_ids.append(b.block_id)
         return True
 
     def commit(self, seq: SeqState, num_new: int) -> None:
@@ -320,6 +339,7 @@ class KVCacheManager:
         for b in reversed(seq.blocks):
             self.pool.release(b)
         seq.blocks = []
+        seq.block_ids = []
         seq.num_computed = 0
         seq.num_cached_blocks = 0
 
@@ -332,7 +352,8 @@ class KVCacheManager:
                          parent.max_tokens if max_tokens is None else max_tokens,
                          parent.cache_salt, parent.num_computed,
                          list(parent.blocks), list(parent.block_hashes),
-                         parent.num_cached_blocks, parent.arrival)
+                         parent.num_cached_blocks, parent.arrival,
+                         list(parent.block_ids))
         for b in child.blocks:
             self.pool.touch(b)
         return child
@@ -457,8 +478,7 @@ class Scheduler:
         reqs, toks, poss = [], [], []
         for seq in order:
             n = scheduled[seq.request_id]
-            reqs.append(StepRequest(seq.request_id,
-                                    [b.block_id for b in seq.blocks],
+            reqs.append(StepRequest(seq.request_id, list(seq.block_ids),
                                     seq.num_computed, n))
             toks += seq.token_ids[seq.num_computed:seq.num_computed + n]
             poss += list(range(seq.num_computed, seq.num_computed + n))

@@ -25,6 +25,8 @@ to run the step (a measured crossover), else 0.
 """
 from __future__ import annotations
 
+import itertools
+
 import numpy as np
 
 BLOCK_SIZE = 16
@@ -38,10 +40,15 @@ def build_step_metadata(requests, block_size: int = BLOCK_SIZE) -> dict:
     lens = n_done + n_new
     qsl = np.zeros(len(requests) + 1, dtype=np.int64)
     np.cumsum(n_new, out=qsl[1:])
-    width = max([len(r.block_ids) for r in requests] + [1])
+    nb = np.fromiter((len(r.block_ids) for r in requests), dtype=np.int64,
+                     count=len(requests))
+    width = max(int(nb.max()) if len(requests) else 0, 1)
     tables = np.zeros((len(requests), width), dtype=np.int32)
-    for b, r in enumerate(requests):
-        tables[b, :len(r.block_ids)] = r.block_ids
+    # every row's ids in one pass: the mask's row-major order is the
+    # concatenated lists' order
+    flat = np.fromiter(itertools.chain.from_iterable(r.block_ids for r in requests),
+                       dtype=np.int32, count=int(nb.sum()))
+    tables[np.arange(width)[None, :] < nb[:, None]] = flat
     T = int(qsl[-1])
     # request index and position of every new token
     req_of_tok = np.repeat(np.arange(len(requests)), n_new)

@@ -305,3 +305,32 @@ def test_planned_steps_are_valid_attention_metadata():
         sched.update(plan, {r: 0 for r in plan.scheduled})
     assert kv.pool.num_free == 200
     assert all(b.ref_cnt == 0 for b in kv.pool.blocks)
+
+
+def test_block_id_rows_follow_the_blocks():
+    """Each request's block-id list (the step's block-table row) stays equal
+    to its blocks' ids through admissions with prefix hits, chunked
+    prompts, copy-on-write of forked requests, preemption and release."""
+    import random
+    rnd = random.Random(7)
+    head = [rnd.randrange(1000) for _ in range(40)]
+    sched = Scheduler(KVCacheManager(64), token_budget=96, max_num_seqs=8,
+                      long_prefill_threshold=24)
+    for i in range(12):
+        tail = [rnd.randrange(1000) for _ in range(rnd.randrange(1, 30))]
+        sched.add_request(f"r{i}", head + tail, rnd.randrange(1, 20))
+    forked = False
+    for _ in range(400):
+        if not (sched.waiting or sched.running):
+            break
+        plan = sched.schedule()
+        for req in plan.requests:
+            seq = next(s for s in sched.running if s.request_id == req.request_id)
+            assert req.block_ids == [b.block_id for b in seq.blocks]
+        sched.update(plan, {rid: rnd.randrange(1000) for rid in plan.scheduled})
+        if not forked and sched.running and sched.running[0].num_computed > 20:
+            sched.fork(sched.running[0].request_id, "child", 5)
+            forked = True
+        for seq in sched.running:
+            assert seq.block_ids == [b.block_id for b in seq.blocks]
+    assert not sched.waiting and not sched.running
