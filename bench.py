@@ -180,10 +180,14 @@ def _device_inputs(wl, dev, casc=None):
         casc = cascade_prefix_blocks(wl.requests,
                                      wl.num_q_heads // wl.num_kv_heads)
     d["casc"] = casc
-    size_fn = (pa.pa_attention_cascade_workspace_size if d["casc"] > 0
-               else pa.pa_attention_workspace_size)
-    nbytes = size_fn(wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
-                     len(wl.requests), md["max_query_len"], md["max_seq_len"])
+    sizes = (wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
+             len(wl.requests), md["max_query_len"], md["max_seq_len"])
+    if wl.sliding_window > 0:
+        nbytes = pa.pa_attention_window_workspace_size(*sizes, wl.sliding_window)
+    elif d["casc"] > 0:
+        nbytes = pa.pa_attention_cascade_workspace_size(*sizes)
+    else:
+        nbytes = pa.pa_attention_workspace_size(*sizes)
     d["ws"] = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     return d
 
@@ -201,7 +205,13 @@ def _step(pa, wl, d):
                                 d["slots"], k_scale=wl.k_scale,
                                 v_scale=wl.v_scale, cache_dtype=cdt)
     md = d["md"]
-    if d.get("casc", 0) > 0:
+    if wl.sliding_window > 0:
+        pa.pa_attention_window(d["q"], d["kc"], d["vc"], d["bt"], d["sl"],
+                               d["qsl"], md["max_query_len"], md["max_seq_len"],
+                               wl.scale, wl.sliding_window, wl.k_scale,
+                               wl.v_scale, out=d["out"], workspace=d["ws"],
+                               cache_dtype=cdt)
+    elif d.get("casc", 0) > 0:
         pa.pa_attention_cascade(d["q"], d["kc"], d["vc"], d["bt"], d["sl"],
                                 d["qsl"], md["max_query_len"], md["max_seq_len"],
                                 wl.scale, d["casc"], wl.k_scale, wl.v_scale,
@@ -235,6 +245,75 @@ def _cascade_vs_plain(pa, wl, dev, steps, warmup, flush):
     res["policy_blocks"] = cascade_prefix_blocks(
         wl.requests, wl.num_q_heads // wl.num_kv_heads)
     return res
+
+
+def _window_decode(pa, dev, flush, steps, warmup, peak_gbs):
+    """A sliding-window layer's decode step: every query sees its last
+    `window` keys (pa_attention_window: the window's view, then the head-group
+    decode kernel over the view's pages), against pa_attention over the whole
+    contexts of the same batch."""
+    import torch
+    import workloads
+    wl = workloads.sliding_window_decode()
+    byts = wl.kv_bytes() + wl.qo_bytes()
+    res = {"workload": "Llama-3.1-8B shape: " + wl.description,
+           "window_kv_bytes": wl.kv_bytes()}
+    for mode in ("window", "whole_context"):
+        if mode == "whole_context":
+            W, wl.sliding_window = wl.sliding_window, 0
+        d = _device_inputs(wl, dev)
+        st, kt, _ = _time_steps(pa, wl, d, steps, warmup, flush)
+        flags = pa.pa_get_device_error()
+        if flags:
+            raise RuntimeError(f"device error flags 0x{flags:x} ({mode})")
+        res[mode + "_step_ms"] = statistics.mean(st)
+        if mode == "window":
+            res["kernel_ms"] = statistics.mean(kt)
+        del d
+        torch.cuda.empty_cache()
+    wl.sliding_window = W
+    res["step_tbs"] = byts / (res["window_step_ms"] * 1e-3) / 1e12
+    res["kernel_tbs"] = byts / (res["kernel_ms"] * 1e-3) / 1e12
+    res["frac_of_measured_hbm"] = res["kernel_tbs"] * 1e3 / peak_gbs
+    res["speedup_vs_whole_context"] = (res["whole_context_step_ms"] /
+                                       res["window_step_ms"])
+    return res
+
+
+def _block_manager_host(n_requests=160, prompt=2000, shared=1024,
+                        out_tokens=64):
+    """Host cost of the block manager and step planner: a first-come
+    first-served serving loop over requests that share a 1024-token prompt
+    prefix (prefix-cache hits), 2048-token budget, up to 128 running
+    requests; per step schedule() + the step's metadata + update().  Pure
+    host work (no GPU): microseconds per planned step."""
+    import random
+    from paged_kv_cache_82_gb300.block_manager import KVCacheManager, Scheduler
+    from paged_kv_cache_82_gb300.metadata import build_step_metadata
+    rnd = random.Random(82009)
+    head = [rnd.randrange(32000) for _ in range(shared)]
+    sched = Scheduler(KVCacheManager(40000), token_budget=2048,
+                      max_num_seqs=128, long_prefill_threshold=512)
+    for i in range(n_requests):
+        tail = [rnd.randrange(32000) for _ in range(prompt - shared)]
+        sched.add_request(f"r{i}", head + tail, out_tokens)
+    t0 = time.perf_counter()
+    steps = tokens = 0
+    while (sched.waiting or sched.running) and steps < 5000:
+        plan = sched.schedule()
+        if plan.requests:
+            build_step_metadata(plan.requests)
+        tokens += sum(plan.scheduled.values())
+        sched.update(plan, {rid: 1 for rid in plan.scheduled})
+        steps += 1
+    dt = time.perf_counter() - t0
+    return {"workload": (f"{n_requests} requests, {prompt}-token prompts sharing "
+                         f"a {shared}-token prefix, {out_tokens} output tokens "
+                         "each; budget 2048 tokens, <= 128 running, prompt "
+                         "chunks <= 512"),
+            "steps": steps, "tokens": tokens,
+            "us_per_step": dt / max(steps, 1) * 1e6,
+            "finished": len(sched.finished)}
 
 
 def _time_steps(pa, wl, d, steps, warmup, flush):
@@ -647,6 +726,11 @@ def run_ours(args):
     }
     del wls
 
+    # ---- a sliding-window layer's decode step (the window's keys only),
+    # against the same batch without the window
+    window = _window_decode(pa, dev, flush, max(3, args.steps // 10),
+                            args.warmup, peak_gbs)
+
     # ---- the other decode workloads of the scope (kernel and step TB/s)
     others = {}
     for name, make in (("mha_fp16_32x8192", workloads.config3),
@@ -765,6 +849,8 @@ def run_ours(args):
         "clocks": clocks,
         "mixed_step": mixed,
         "shared_prefix_decode": shared_prefix,
+        "sliding_window_decode": window,
+        "block_manager_host": _block_manager_host(),
         "prefill_step": prefill,
         "prefill_step_fp8": prefill_fp8,
         "other_decodes": others,

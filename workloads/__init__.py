@@ -94,22 +94,29 @@ class Workload:
         return self.num_q_heads // self.num_kv_heads
 
     def kv_bytes(self, unique: bool = True) -> int:
-        """Bytes of K and V the step's attention must read: every key of
-        every request once (a block shared by several requests counted once
-        when unique=True); a 4-bit cache's scales included."""
+        """Bytes of K and V the step's attention must read: every key some
+        query of a request sees, once (a block shared by several requests
+        counted once when unique=True); a 4-bit cache's scales included.
+        With a sliding window of W keys a request of n new tokens after L - n
+        cached sees keys max(0, L - n - W + 1) .. L - 1."""
         if self.cache_dtype in FOUR_BIT:
             per_token = 2 * self.num_kv_heads * page_bytes_4bit(
                 self.cache_dtype, self.head_dim) // BLOCK_SIZE
         else:
             per_token = (2 * _ELEM_BYTES[self.cache_dtype] *
                          self.num_kv_heads * self.head_dim)
+        W = self.sliding_window
+
+        def first_key(r):
+            return max(0, r.seq_len - r.num_new - W + 1) if W > 0 else 0
         if not unique:
-            return per_token * sum(r.seq_len for r in self.requests)
+            return per_token * sum(r.seq_len - first_key(r)
+                                   for r in self.requests)
         seen = {}
         for r in self.requests:
-            L = r.seq_len
+            L, lo = r.seq_len, first_key(r)
             for k, b in enumerate(r.block_ids):
-                n = min(BLOCK_SIZE, L - k * BLOCK_SIZE)
+                n = min(BLOCK_SIZE, L - k * BLOCK_SIZE) - max(0, lo - k * BLOCK_SIZE)
                 if n > 0:
                     seen[b] = max(seen.get(b, 0), n)
         return per_token * sum(seen.values())
@@ -534,6 +541,25 @@ def shared_prefix_decode(num_decodes: int = 32, prefix_blocks: int = 1024,
         description=(f"{num_decodes} decodes behind a shared "
                      f"{prefix_blocks * BLOCK_SIZE}-token prefix, private "
                      f"context U[{lo},{hi}), bf16"))
+
+
+def sliding_window_decode(batch: int = 64, lo: int = 2048, hi: int = 12288,
+                          window: int = 1024) -> Workload:
+    """Decodes of a sliding-window layer ("01. vLLM", the hybrid KV cache
+    manager paragraph: layers whose queries see only the last `window`
+    keys), Llama-3.1-8B shape, bf16: `batch` requests with contexts U[lo,
+    hi], each query seeing its last `window` keys."""
+    seed = 82008
+    rng = np.random.default_rng(seed)
+    lens = [int(x) for x in rng.integers(lo, hi, size=batch, endpoint=True)]
+    wl = decode_step("sliding_window_decode_llama31_8b", seed, seq_lens=lens,
+                     num_q_heads=32, num_kv_heads=8, head_dim=128,
+                     num_blocks=sum(_blocks_for(L) for L in lens) + 64,
+                     dtype="bf16",
+                     description=(f"{batch} decodes, L~U[{lo},{hi}], window "
+                                  f"{window}, bf16"))
+    wl.sliding_window = window
+    return wl
 
 
 def attention_flops(wl: Workload) -> int:
