@@ -48,7 +48,8 @@ def _peaks():
 
 def _tensor_peak():
     """Dense bf16 tensor peak (burst figure: the prefill kernel is timed in
-    isolation), measured on this machine, else the fallback."""
+    isolation), as measured on these GPUs (MEASURED_PEAKS.json), else the
+    fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
