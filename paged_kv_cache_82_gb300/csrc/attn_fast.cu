@@ -2025,7 +2025,8 @@ merge_self_kernel(FastParams p) {
 template <int kKind>
 __device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
                                         int nrows, int lane,
-                                        uint32_t (&qa)[8][4], float& rscale) {
+                                        uint32_t (&qa)[8][4], float& rscale,
+                                        float& qbias) {
   using Tr = Traits<kKind>;
   const int r = lane >> 2, c = lane & 3;
   const int G = p.group;
@@ -2080,6 +2081,25 @@ __device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
       qa[2 * j + 1][0] = __byte_perm(w[4 * j + 1], w[4 * j + 3], 0x5410);
       qa[2 * j + 1][2] = __byte_perm(w[4 * j + 1], w[4 * j + 3], 0x7632);
     }
+    // The K decode leaves each code c as its f16 pattern: 1032 + c for an
+    // even element (low nibble), 1152 + 16 c for an odd one (high nibble).
+    // Q's odd elements are taken / 16 (exact), so that a score comes out as
+    // Q.K + 1032 * sum(even q) + 1152 * sum(odd q / 16): that sum, the row's
+    // bias, is taken off each score.
+    const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
+    float even = 0.f, odd = 0.f;
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&qa[st][2]), sixteenth);
+      qa[st][2] = *reinterpret_cast<uint32_t*>(&h);
+      const float2 e = __half22float2(*reinterpret_cast<const __half2*>(&qa[st][0]));
+      const float2 o = __half22float2(h);
+      even += e.x + e.y;
+      odd += o.x + o.y;
+    }
+    qbias = 1032.f * even + 1152.f * odd;
+    qbias += __shfl_xor_sync(~0u, qbias, 1);
+    qbias += __shfl_xor_sync(~0u, qbias, 2);
   } else {
 #pragma unroll
     for (int st = 0; st < 8; ++st) {
@@ -2098,25 +2118,18 @@ __device__ __forceinline__ void load_q4(const FastParams& p, int q0, int g,
 constexpr uint32_t kNibLo = 0x000F000Fu, kNibLoFlip = 0x64086408u;  // low nibbles
 constexpr uint32_t kNibHi = 0x00F000F0u, kNibHiFlip = 0x64806480u;  // high nibbles
 
-// eight INT4 codes (one word, element 2i in the low nibble of byte i) ->
-// the f16 pairs (0, 4), (1, 5), (2, 6), (3, 7), exact: each nibble pair
-// masked in place under the f16 pattern of 1024 (a high nibble weighs 16
-// there, undone by a fused multiply-add), offset binary code + 8 minus 8
+// eight INT4 K codes (one word, element 2i in the low nibble of byte i) ->
+// the f16 pairs (0, 4), (1, 5), (2, 6), (3, 7): each nibble pair masked in
+// place under the f16 pattern of 1024, offset binary code + 8, and left
+// there — 1032 + c for a low nibble, 1152 + 16 c for a high one, exact f16
+// values; the Q side absorbs the 16, and the offsets become a per-row bias
+// taken off the scores (load_q4)
 __device__ __forceinline__ void decode8_int4_k(uint32_t w, uint32_t (&f)[4]) {
   const uint32_t y = w >> 8;
-  const __half2 off = __floats2half2_rn(1032.f, 1032.f);
-  const __half2 sixteenth = __floats2half2_rn(0.0625f, 0.0625f);
-  const __half2 off16 = __floats2half2_rn(-72.f, -72.f);
-  uint32_t t[4] = {(w & kNibLo) ^ kNibLoFlip, (w & kNibHi) ^ kNibHiFlip,
-                   (y & kNibLo) ^ kNibLoFlip, (y & kNibHi) ^ kNibHiFlip};
-  __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&t[0]), off);
-  __half2 h1 = __hfma2(*reinterpret_cast<__half2*>(&t[1]), sixteenth, off16);
-  __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&t[2]), off);
-  __half2 h3 = __hfma2(*reinterpret_cast<__half2*>(&t[3]), sixteenth, off16);
-  f[0] = *reinterpret_cast<uint32_t*>(&h0);
-  f[1] = *reinterpret_cast<uint32_t*>(&h1);
-  f[2] = *reinterpret_cast<uint32_t*>(&h2);
-  f[3] = *reinterpret_cast<uint32_t*>(&h3);
+  f[0] = (w & kNibLo) ^ kNibLoFlip;
+  f[1] = (w & kNibHi) ^ kNibHiFlip;
+  f[2] = (y & kNibLo) ^ kNibLoFlip;
+  f[3] = (y & kNibHi) ^ kNibHiFlip;
 }
 
 // eight 4-bit codes (one word, element 2i in the low nibble of byte i) ->
@@ -2196,7 +2209,7 @@ template <int kKind>
 __device__ __forceinline__ void process_page_4bit(
     uint32_t k_base, uint32_t v_base, const uint32_t (&qa)[8][4],
     NarrowState& st, int key0, int valid_keys, bool need_mask, int lim,
-    int win, float sscale, int lane) {
+    int win, float sscale, int lane, float qbias) {
   using Tr = Traits<kKind>;
   constexpr int K4 = Tr::k4;
   constexpr int kCodes = 16 * 64;  // the scales follow the codes
@@ -2254,7 +2267,7 @@ __device__ __forceinline__ void process_page_4bit(
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float v = s[nt][e] * (sscale * ks[nt][e]);
+      float v = (K4 == 1 ? s[nt][e] - qbias : s[nt][e]) * (sscale * ks[nt][e]);
       const int key = key0 + nt * 8 + 2 * c + e;
       // keys past the sequence end (their scales may be NaN), past the
       // causal limit or outside the window
@@ -2401,8 +2414,9 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
   const int G = p.group;
   uint32_t qa[8][4];
   float rscale[2];
+  float qbias = 0.f;  // INT4: the row's score bias (load_q4)
   if constexpr (Traits<kKind>::k4) {
-    load_q4<kKind>(p, rm.q0, g, rows, lane, qa, rscale[0]);
+    load_q4<kKind>(p, rm.q0, g, rows, lane, qa, rscale[0], qbias);
     rscale[1] = rscale[0];
   } else {
     load_q<kKind, false>(p, rm.q0, g, 0, rows, lane, qa, rscale);
@@ -2442,7 +2456,7 @@ __device__ void consume_hg_item(const FastParams& p, uint32_t ring,
     const uint32_t kb = ring + s * Ly::kStageBytes + warp * Ly::kPageBytes;
     if constexpr (Traits<kKind>::k4)
       process_page_4bit<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
-                               valid, need_mask, lim, p.window, ss, lane);
+                               valid, need_mask, lim, p.window, ss, lane, qbias);
     else
       process_page_narrow<kKind>(kb, kb + kHg * Ly::kPageBytes, qa, st, key0,
                                  valid, need_mask, lim, p.window, ss, lane);
