@@ -303,7 +303,7 @@ def _block_manager_host(n_requests=160, prompt=2000, shared=1024,
     while (sched.waiting or sched.running) and steps < 5000:
         plan = sched.schedule()
         if plan.requests:
-            build_step_metadata(plan.requests)
+            build_step_metadata(plan.requests, block_tables=plan.block_tables)
         tokens += sum(plan.scheduled.values())
         sched.update(plan, {rid: 1 for rid in plan.scheduled})
         steps += 1

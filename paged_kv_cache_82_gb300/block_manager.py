@@ -212,8 +212,26 @@ class SeqState:
     num_cached_blocks: int = 0    # leading blocks registered in the cache
     arrival: int = 0
     # the ids of `blocks`, kept alongside it (a step's block-table row is a
-    # copy of this list, not a walk over the blocks)
+    # copy of this list, not a walk over the blocks) and as an int32 array
+    # whose first len(blocks) entries are valid (the step's block table is
+    # filled from it row by row)
     block_ids: List[int] = field(default_factory=list)
+    ids: np.ndarray = field(default_factory=lambda: np.zeros(16, dtype=np.int32))
+
+    def _set_ids(self, ids: Sequence[int]) -> None:
+        self.block_ids = list(ids)
+        cap = max(16, 1 << max(0, len(self.block_ids) - 1).bit_length())
+        self.ids = np.zeros(cap, dtype=np.int32)
+        self.ids[:len(self.block_ids)] = self.block_ids
+
+    def _append_id(self, block_id: int) -> None:
+        n = len(self.block_ids)
+        if n == len(self.ids):
+            grown = np.zeros(2 * n, dtype=np.int32)
+            grown[:n] = self.ids
+            self.ids = grown
+        self.ids[n] = block_id
+        self.block_ids.append(block_id)
 
     @property
     def num_tokens(self) -> int:
@@ -280,7 +298,7 @@ class KVCacheManager:
         for b in hits:
             self.pool.touch(b)
         seq.blocks = list(hits)
-        seq.block_ids = [b.block_id for b in hits]
+        seq._set_ids([b.block_id for b in hits])
         seq.num_computed = len(hits) * self.block_size
         seq.num_cached_blocks = len(hits)
 
@@ -313,12 +331,13 @@ class KVCacheManager:
             copies.append((old.block_id, new.block_id))
             seq.blocks[k] = new
             seq.block_ids[k] = new.block_id
+            seq.ids[k] = new.block_id
             self.pool.release(old)
         total = -(-(seq.num_computed + num_new) // self.block_size)
         while len(seq.blocks) < total:
             b = self.pool.allocate()
             seq.blocks.append(b)
-            seq.block_ids.append(b.block_id)
+            seq._append_id(b.block_id)
         return True
 
     def commit(self, seq: SeqState, num_new: int) -> None:
@@ -339,7 +358,7 @@ class KVCacheManager:
         for b in reversed(seq.blocks):
             self.pool.release(b)
         seq.blocks = []
-        seq.block_ids = []
+        seq._set_ids([])
         seq.num_computed = 0
         seq.num_cached_blocks = 0
 
@@ -353,7 +372,7 @@ class KVCacheManager:
                          parent.cache_salt, parent.num_computed,
                          list(parent.blocks), list(parent.block_hashes),
                          parent.num_cached_blocks, parent.arrival,
-                         list(parent.block_ids))
+                         list(parent.block_ids), parent.ids.copy())
         for b in child.blocks:
             self.pool.touch(b)
         return child
@@ -362,11 +381,17 @@ class KVCacheManager:
 @dataclass
 class StepRequest:
     """One request of a planned step, in the form the attention metadata is
-    built from (see metadata.build_step_metadata)."""
+    built from (see metadata.build_step_metadata): its block-table row is
+    row[:num_blocks] of the plan's block table, `block_ids` as a list."""
     request_id: str
-    block_ids: List[int]
+    row: np.ndarray
+    num_blocks: int
     num_computed: int
     num_new: int
+
+    @property
+    def block_ids(self) -> List[int]:
+        return self.row[:self.num_blocks].tolist()
 
 
 @dataclass
@@ -378,6 +403,9 @@ class StepPlan:
     new_token_ids: List[int]                  # ids of the step's tokens, in order
     new_positions: List[int]                  # their positions in their sequences
     preempted: List[str]
+    # the requests' block-table rows, int32 [len(requests), max blocks]
+    # (unused entries 0): build_step_metadata's block_tables
+    block_tables: Optional[np.ndarray] = None
 
 
 class Scheduler:
@@ -476,14 +504,18 @@ class Scheduler:
             order.append(seq)
             budget -= n
         reqs, toks, poss = [], [], []
-        for seq in order:
+        width = max([len(seq.blocks) for seq in order] + [1])
+        table = np.zeros((len(order), width), dtype=np.int32)
+        for i, seq in enumerate(order):
             n = scheduled[seq.request_id]
-            reqs.append(StepRequest(seq.request_id, list(seq.block_ids),
+            nb = len(seq.blocks)
+            table[i, :nb] = seq.ids[:nb]
+            reqs.append(StepRequest(seq.request_id, table[i], nb,
                                     seq.num_computed, n))
             toks += seq.token_ids[seq.num_computed:seq.num_computed + n]
             poss += list(range(seq.num_computed, seq.num_computed + n))
         return StepPlan(self.step_no, scheduled, reqs, copies, toks, poss,
-                        preempted)
+                        preempted, table)
 
     def update(self, plan: StepPlan, sampled: Dict[str, int]) -> List[str]:
         """After the step ran: commit the computed tokens; a request whose

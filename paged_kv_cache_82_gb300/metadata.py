@@ -32,7 +32,12 @@ import numpy as np
 BLOCK_SIZE = 16
 
 
-def build_step_metadata(requests, block_size: int = BLOCK_SIZE) -> dict:
+def build_step_metadata(requests, block_size: int = BLOCK_SIZE,
+                        block_tables=None) -> dict:
+    """The step's metadata (module docstring).  block_tables: the requests'
+    block-table rows already as an int32 array (a planner that keeps them,
+    e.g. block_manager's StepPlan.block_tables); else built from the
+    requests' block_ids."""
     n_new = np.fromiter((r.num_new for r in requests), dtype=np.int64,
                         count=len(requests))
     n_done = np.fromiter((r.num_computed for r in requests), dtype=np.int64,
@@ -40,15 +45,18 @@ def build_step_metadata(requests, block_size: int = BLOCK_SIZE) -> dict:
     lens = n_done + n_new
     qsl = np.zeros(len(requests) + 1, dtype=np.int64)
     np.cumsum(n_new, out=qsl[1:])
-    nb = np.fromiter((len(r.block_ids) for r in requests), dtype=np.int64,
-                     count=len(requests))
-    width = max(int(nb.max()) if len(requests) else 0, 1)
-    tables = np.zeros((len(requests), width), dtype=np.int32)
-    # every row's ids in one pass: the mask's row-major order is the
-    # concatenated lists' order
-    flat = np.fromiter(itertools.chain.from_iterable(r.block_ids for r in requests),
-                       dtype=np.int32, count=int(nb.sum()))
-    tables[np.arange(width)[None, :] < nb[:, None]] = flat
+    if block_tables is not None:
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    else:
+        nb = np.fromiter((len(r.block_ids) for r in requests), dtype=np.int64,
+                         count=len(requests))
+        width = max(int(nb.max()) if len(requests) else 0, 1)
+        tables = np.zeros((len(requests), width), dtype=np.int32)
+        # every row's ids in one pass: the mask's row-major order is the
+        # concatenated lists' order
+        flat = np.fromiter(itertools.chain.from_iterable(r.block_ids for r in requests),
+                           dtype=np.int32, count=int(nb.sum()))
+        tables[np.arange(width)[None, :] < nb[:, None]] = flat
     T = int(qsl[-1])
     # request index and position of every new token
     req_of_tok = np.repeat(np.arange(len(requests)), n_new)

@@ -324,6 +324,10 @@ def test_block_id_rows_follow_the_blocks():
         if not (sched.waiting or sched.running):
             break
         plan = sched.schedule()
+        md = build_step_metadata(plan.requests)
+        md2 = build_step_metadata(plan.requests, block_tables=plan.block_tables)
+        for k in ("block_tables", "slot_mapping", "seq_lens", "query_start_loc"):
+            assert np.array_equal(md[k], md2[k]), k
         for req in plan.requests:
             seq = next(s for s in sched.running if s.request_id == req.request_id)
             assert req.block_ids == [b.block_id for b in seq.blocks]
@@ -333,4 +337,5 @@ def test_block_id_rows_follow_the_blocks():
             forked = True
         for seq in sched.running:
             assert seq.block_ids == [b.block_id for b in seq.blocks]
+            assert list(seq.ids[:len(seq.blocks)]) == seq.block_ids
     assert not sched.waiting and not sched.running
