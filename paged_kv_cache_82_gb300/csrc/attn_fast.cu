@@ -2854,6 +2854,17 @@ cudaError_t launch_hg(const AttnArgs& a, const FastParams& fp,
                                       plan.off_pref) + 1;
     e = cudaMemsetAsync(tile_ctr, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
+    // A step of one request with more than 8 query rows per KV head has no
+    // decode work (its rows all go to the tiles): the tensor-core kernel runs
+    // alone, one CTA per SM, with no decode kernel and no merge.
+    const int G = a.num_q_heads / a.num_kv_heads;
+    if (a.num_seqs == 1 && a.num_tokens * G > 8 && f.cascade_blocks == 0) {
+      if (pe.start) cudaEventRecord(pe.start, stream);
+      e = launch_prefill_tc(a, *tc, true, nullptr, nullptr, (int)plan.max_atoms, 8,
+                            tile_ctr, false, num_sms, stream);
+      if (pe.stop) cudaEventRecord(pe.stop, stream);
+      return e;
+    }
     // (with the profiling events on, launches are plain and run one after
     // the other: no grid ahead, the tiles all behind the decode kernel)
     pf_ctas = pe.start == nullptr ? prefill_ctas_ahead(a, num_sms) : 0;

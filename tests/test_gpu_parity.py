@@ -351,6 +351,15 @@ def test_launches_per_step_kind():
     n0 = pa.pa_launch_count()
     gpu_step(_custom([(300, 1), (40, 1)], 32, 8))
     assert pa.pa_launch_count() - n0 == 2
+    # one request of more than 8 rows per KV head: no decode work, the
+    # tensor-core kernel alone (no decode kernel, no merge); two query
+    # tokens at G = 4 (8 rows) are a decode
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 64)], 32, 8))
+    assert pa.pa_launch_count() - n0 == 1
+    n0 = pa.pa_launch_count()
+    gpu_step(_custom([(300, 2)], 32, 8))
+    assert pa.pa_launch_count() - n0 == 2
     # K/V write + a step with bf16 prefill tiles: a tensor-core prefill grid
     # beside the decode kernel, a second one behind it (both plan
     # themselves), then the merge
