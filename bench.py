@@ -786,7 +786,7 @@ def run_ours(args):
     prefill = {
         "workload": ("Llama-3.1-8B shape, bf16: one request, 4096-token "
                      "chunk after 4096 cached tokens (causal)"),
-        "kernel": "prefill_tc_kernel (bf16, tcgen05) + the empty decode launch",
+        "kernel": "prefill_tc_kernel (bf16, tcgen05): one grid, the step has no decode work",
         "bound": "tensor", "achieved": p_tflops, "peak": bf16_peak,
         "unit": "TFLOP/s", "frac": p_tflops / bf16_peak,
         "peak_kind": bf16_kind, "kernels_ms": p_km,
@@ -810,7 +810,7 @@ def run_ours(args):
         "workload": ("Llama-3.1-8B shape, bf16 q, FP8 E4M3 KV: one request, "
                      "4096-token chunk after 4096 cached tokens (causal)"),
         "kernel": ("prefill_tc_kernel (FP8 pages widened to f16 in shared "
-                   "memory, f16 tcgen05) + the empty decode launch"),
+                   "memory, f16 tcgen05): one grid, the step has no decode work"),
         "bound": "tensor", "achieved": p8_tflops, "peak": bf16_peak,
         "unit": "TFLOP/s", "frac": p8_tflops / bf16_peak,
         "peak_kind": bf16_kind + " (f16 rate = bf16 rate)",
