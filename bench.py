@@ -179,7 +179,8 @@ def _device_inputs(wl, dev, casc=None):
     # block manager); casc forces a prefix length (0: the plain step)
     if casc is None:
         casc = cascade_prefix_blocks(wl.requests,
-                                     wl.num_q_heads // wl.num_kv_heads)
+                                     wl.num_q_heads // wl.num_kv_heads,
+                                     wl.cache_dtype)
     d["casc"] = casc
     sizes = (wl.q.shape[0], wl.num_q_heads, wl.num_kv_heads, wl.head_dim,
              len(wl.requests), md["max_query_len"], md["max_seq_len"])
@@ -244,7 +245,7 @@ def _cascade_vs_plain(pa, wl, dev, steps, warmup, flush):
         torch.cuda.empty_cache()
     res["speedup"] = res["plain_ms"] / res["cascade_ms"]
     res["policy_blocks"] = cascade_prefix_blocks(
-        wl.requests, wl.num_q_heads // wl.num_kv_heads)
+        wl.requests, wl.num_q_heads // wl.num_kv_heads, wl.cache_dtype)
     return res
 
 
@@ -605,16 +606,18 @@ def run_ours(args):
     if args.only == "cascade-sweep":
         # the cascade's crossover: decode steps behind a shared prefix,
         # cascade against plain, over prefix lengths and request counts
+        cdt = args.cache_dtype
         for priv in ((256, 2048), (1024, 8192)):
             for pb in (32, 64, 128, 256, 512, 1024, 4096):
                 for n in (2, 8, 32, 64, 128):
                     if priv[0] == 1024 and (pb not in (128, 256) or n not in (8, 32)):
                         continue
-                    wls = workloads.shared_prefix_decode(n, pb, *priv)
+                    wls = workloads.shared_prefix_decode(n, pb, *priv,
+                                                         cache_dtype=cdt)
                     r = _cascade_vs_plain(pa, wls, dev, args.steps, args.warmup,
                                           flush)
                     print(json.dumps({"prefix_blocks": pb, "decodes": n,
-                                      "private": list(priv), **{
+                                      "private": list(priv), "cache": cdt, **{
                                           k: round(v, 4) if isinstance(v, float)
                                           else v for k, v in r.items()}}),
                           flush=True)
@@ -938,6 +941,8 @@ def main():
                     help="profiling runs: time just one step kind, no JSON "
                          "line (cascade-sweep: one JSON line per shared-"
                          "prefix decode step, cascade against plain)")
+    ap.add_argument("--cache-dtype", choices=["bf16", "e4m3"], default="bf16",
+                    help="with --only cascade-sweep: the cache type")
     ap.add_argument("--batch", type=int, default=0,
                     help="with --only decode/mha/fp8long/mixed: that many "
                          "(decode) requests instead of the workload's own")

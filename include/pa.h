@@ -325,11 +325,14 @@ pa_status pa_attention_window_workspace_size(int64_t num_tokens,
  *
  * The cascade is the caller's choice, and it is not always the faster one:
  * it adds the prefix tiles' start-up and a merge part per key range.
- * Measured on a GB300 (decode steps of the Llama-3.1-8B shape, bf16), it
- * beat the plain step wherever N >= 512, or N x (requests of at most 8 rows)
- * >= 8192 (e.g. 1.04x at 512 blocks x 8 requests, 2.8x at 1024 x 32, 12x at
- * 4096 x 128), and lost to it below that with few requests (0.69x at 32
- * blocks x 2 requests).  With a single request nothing is shared: call
+ * Measured on a GB300 (decode steps of the Llama-3.1-8B shape), with a
+ * bf16 cache it beat the plain step wherever N >= 512, or N x (requests of
+ * at most 8 rows) >= 8192 (e.g. 1.04x at 512 blocks x 8 requests, 2.8x at
+ * 1024 x 32, 12x at 4096 x 128), and lost to it below that with few
+ * requests (0.69x at 32 blocks x 2 requests); with an FP8 cache (prefix
+ * pages widened on the way, the plain step reading half the bytes) wherever
+ * N x requests >= 16384 (1.1x at 512 x 32, 5x at 4096 x 128), and lost below
+ * that (0.79x at 1024 x 8).  With a single request nothing is shared: call
  * pa_attention.  The statement is checked on the device:
  * a request whose block-table row or key count breaks it sets
  * PA_DEV_ERR_METADATA (pa_get_device_error) and the step's output is then

@@ -102,25 +102,33 @@ def common_prefix_blocks(requests) -> int:
 
 
 # Where a cascade step beats the plain step (decode steps of the
-# Llama-3.1-8B shape on a GB300, bf16, private contexts of 256 - 8192 tokens
-# after the prefix): a prefix of at least CASCADE_MIN_BLOCKS blocks, or
-# prefix blocks x decode requests of at least CASCADE_MIN_BLOCK_READS.  Below
-# that the plain step re-reads the prefix from L2 for less than the cascade's
-# fixed costs (the prefix tiles' start-up and the extra merge parts).
+# Llama-3.1-8B shape on a GB300, private contexts of 256 - 8192 tokens after
+# the prefix), in prefix blocks N and decode requests n.  16-bit caches: N of
+# at least CASCADE_MIN_BLOCKS, or N x n of at least CASCADE_MIN_BLOCK_READS.
+# FP8 caches (the prefix tiles widen E4M3 pages on the way, the plain step
+# reads half the bytes): N x n of at least CASCADE_MIN_BLOCK_READS_FP8 only.
+# Below that the plain step re-reads the prefix from L2 for less than the
+# cascade's fixed costs (the prefix tiles' start-up and the extra merge
+# parts).  Caches without a cascade path (4-bit) never take it.
 CASCADE_MIN_BLOCKS = 512
 CASCADE_MIN_BLOCK_READS = 8192
+CASCADE_MIN_BLOCK_READS_FP8 = 16384
 
 
-def cascade_prefix_blocks(requests, group: int) -> int:
+def cascade_prefix_blocks(requests, group: int, cache_dtype: str = "bf16") -> int:
     """The shared prefix to run as a cascade (pa_attention_cascade's
     cascade_blocks), or 0 where the plain step is faster.  Only the
     decode-class requests (at most 8 query rows: q_len x group <= 8) read the
     prefix once through the cascade; prefill requests read their whole row
     either way.  Needs at least two of them."""
+    if cache_dtype not in ("bf16", "f16", "e4m3"):
+        return 0
     n = common_prefix_blocks(requests)
     dec = sum(1 for r in requests if 0 < r.num_new and r.num_new * group <= 8)
     if n <= 0 or dec < 2:
         return 0
+    if cache_dtype == "e4m3":
+        return int(n) if n * dec >= CASCADE_MIN_BLOCK_READS_FP8 else 0
     if n >= CASCADE_MIN_BLOCKS or n * dec >= CASCADE_MIN_BLOCK_READS:
         return int(n)
     return 0

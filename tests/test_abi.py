@@ -218,3 +218,13 @@ def test_cascade_policy():
     pf = Request(list(range(600)) + [20000, 20001], 600 * 16, 30)
     assert cascade_prefix_blocks(step(600, 1, extra=[pf]), 4) == 0
     assert cascade_prefix_blocks(step(600, 2, extra=[pf]), 4) == 600
+    # FP8 caches: many requests behind the prefix, whatever its length;
+    # 4-bit caches have no cascade path
+    from paged_kv_cache_82_gb300.metadata import CASCADE_MIN_BLOCK_READS_FP8
+    assert cascade_prefix_blocks(step(1024, 8), 4, "e4m3") == 0
+    assert cascade_prefix_blocks(step(1024, 16), 4, "e4m3") == 1024
+    assert cascade_prefix_blocks(step(128, 128), 4, "e4m3") == 128
+    assert cascade_prefix_blocks(step(128, 64), 4, "e4m3") == 0
+    assert 128 * 128 >= CASCADE_MIN_BLOCK_READS_FP8 > 128 * 64
+    assert cascade_prefix_blocks(step(600, 64), 4, "int4") == 0
+    assert cascade_prefix_blocks(step(600, 64), 4, "nvfp4") == 0

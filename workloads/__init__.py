@@ -525,22 +525,26 @@ def prefill_chunk(ctx: int = 4096, new: int = 4096,
 
 def shared_prefix_decode(num_decodes: int = 32, prefix_blocks: int = 1024,
                          lo: int = 256, hi: int = 2048,
-                         seed: Optional[int] = None) -> Workload:
+                         seed: Optional[int] = None,
+                         cache_dtype: str = "bf16") -> Workload:
     """Decodes behind one long shared prompt prefix (prefix caching hands
     every request the same `prefix_blocks` full blocks, "01. vLLM", prefix
     caching), Llama-3.1-8B shape, bf16: each request has a private context of
     U[lo, hi) tokens after the prefix, then one new token (written by the
-    step).  The default is 32 decodes behind a 16,384-token prefix."""
+    step).  The default is 32 decodes behind a 16,384-token prefix.  With
+    cache_dtype "e4m3" the cache is FP8 (scales 0.02 / 0.03)."""
     seed = 82007 + num_decodes + 7 * prefix_blocks if seed is None else seed
     rng = np.random.default_rng(seed)
     private = [int(x) for x in rng.integers(lo, hi, size=num_decodes)]
+    fp8 = cache_dtype == "e4m3"
     return shared_prefix_step(
         "shared_prefix_decode_llama31_8b", seed, prefix_blocks=prefix_blocks,
         private=private, q_lens=[1] * num_decodes, num_q_heads=32,
-        num_kv_heads=8, head_dim=128, dtype="bf16",
+        num_kv_heads=8, head_dim=128, dtype="bf16", cache_dtype=cache_dtype,
+        k_scale=0.02 if fp8 else 1.0, v_scale=0.03 if fp8 else 1.0,
         description=(f"{num_decodes} decodes behind a shared "
                      f"{prefix_blocks * BLOCK_SIZE}-token prefix, private "
-                     f"context U[{lo},{hi}), bf16"))
+                     f"context U[{lo},{hi}), {cache_dtype} KV"))
 
 
 def sliding_window_decode(batch: int = 64, lo: int = 2048, hi: int = 12288,
